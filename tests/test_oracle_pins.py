@@ -1,0 +1,367 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: hand-worked
+values (tests/golden), a library routine (torch's float8_e4m3fn conversion,
+torch's scaled_dot_product_attention), exact rational arithmetic, brute force
+over every subset on tiny inputs, closed forms and invariants.
+"""
+
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_block_sparse_m3s_gb300 import workloads as W
+from oracle import m3s_oracle as O
+
+GOLDEN = __file__.rsplit("/", 1)[0] + "/golden/nvfp4_quant_blocks.txt"
+
+
+def _golden_cases():
+    cases, cur = [], None
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("case "):
+            cur = {"name": line[5:]}
+            cases.append(cur)
+        else:
+            k, v = line.split(":", 1)
+            cur[k] = v.split()
+    return cases
+
+
+def _block(values):
+    """16 decimal values -> a 128-element BF16 row (group 0 = values, rest zero)."""
+    x = np.zeros(128, dtype=np.float32)
+    x[:16] = [float(v) for v in values]
+    bits = W.f32_to_bf16_bits(x)
+    # the golden inputs are BF16-exact: the rounding must not have moved them
+    assert np.array_equal(W.bf16_bits_to_f32(bits)[:16], x[:16])
+    return bits
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c["name"])
+def test_quantiser_hand_worked(case):
+    codes, scales = O.quantize(_block(case["x"]))
+    assert scales[0] == int(case["scale"][0], 16)
+    got = [(codes[i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+    assert got == [int(c, 16) for c in case["codes"]]
+    # the other 7 groups are zero
+    assert not codes[8:].any() and not scales[1:].any()
+
+
+def test_e4m3_table_matches_torch():
+    """Every E4M3 byte decodes as torch's float8_e4m3fn does (library routine)."""
+    allb = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).float().double().numpy()
+    ours = O.E4M3_ALL
+    nan = np.isnan(allb)
+    assert np.array_equal(nan, np.isnan(ours))
+    assert np.array_equal(allb[~nan], ours[~nan])
+    assert O.E4M3_POS[-1] == 448.0 and O.E4M3_POS[1] == 2.0 ** -9
+
+
+def test_e4m3_encoder_matches_torch_rne():
+    """Nearest / ties-to-even E4M3 rounding agrees with torch's float32 -> e4m3fn cast
+    on every in-range float32 value tried (all midpoints, neighbours of every
+    value, and random reals)."""
+    v = O.E4M3_POS
+    mids = (v[:-1] + v[1:]) / 2
+    rng = np.random.default_rng(0)
+    cand = np.concatenate([v, mids, np.nextafter(mids, 0), np.nextafter(mids, 1000),
+                           rng.uniform(0, 448, 20000), rng.uniform(0, 2 ** -6, 20000)])
+    cand = cand.astype(np.float32).astype(np.float64)      # exactly float32
+    cand = cand[cand <= 448.0]
+    t = torch.from_numpy(cand.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert np.array_equal(O.e4m3_encode_nonneg(cand), t.numpy())
+
+
+def _exact_quantise_group(xs):
+    """Independent restatement in exact rationals (Fraction) of one 16-group."""
+    fr = [Fraction(float(x)) for x in xs]
+    amax = max(abs(x) for x in fr)
+    target = amax / 6
+    vals = [Fraction(float(O.e4m3_value(c))) for c in range(0x7F)]
+    best = min(range(0x7F), key=lambda c: (abs(vals[c] - target), c % 2))
+    s = vals[best]
+    grid = [Fraction(g) for g in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    codes = []
+    for x, xf in zip(xs, fr):
+        if s == 0:
+            codes.append(0)
+            continue
+        q = abs(xf) / s
+        m = min(range(8), key=lambda i: (abs(grid[i] - q), i % 2))
+        codes.append(m | (8 if math.copysign(1.0, float(x)) < 0 else 0))
+    return best, codes
+
+
+def test_quantiser_equals_exact_rational_definition():
+    """Vectorised oracle == exact-rational brute force on random groups spanning the
+    whole E4M3 scale range, with ties planted."""
+    rng = np.random.default_rng(1)
+    rows = []
+    for i in range(48):
+        e = rng.integers(-14, 12)
+        x = rng.standard_normal(128) * 2.0 ** e
+        if i % 3 == 0:        # plant exact ties: grid midpoints x a power-of-two scale
+            x[:7] = np.array([.25, .75, 1.25, 1.75, 2.5, 3.5, 5]) * 2.0 ** e
+            x[7] = 6 * 2.0 ** e
+        rows.append(x)
+    bits = W.f32_to_bf16_bits(np.array(rows, dtype=np.float32))
+    xs = W.bf16_bits_to_f32(bits).astype(np.float64)
+    codes, scales = O.quantize(bits)
+    for r in range(len(rows)):
+        for g in range(8):
+            s, c = _exact_quantise_group(xs[r, 16 * g: 16 * g + 16])
+            assert scales[r, g] == s
+            got = [(codes[r, 8 * g + i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+            assert got == c, (r, g)
+
+
+def test_round_trip_error_bound_and_idempotence():
+    """|x - x_hat| <= half the local e2m1 step x s for unsaturated elements, and
+    quantising the dequantised values again gives the same bytes when the group's
+    largest code is 7."""
+    bits = W.bf16_tensor(7, "rt", (512, 128), 4, 20.0)
+    x = W.bf16_bits_to_f32(bits).astype(np.float64)
+    c, s = O.quantize(bits)
+    xh = O.dequantize(c, s)
+    sv = np.repeat(O.E4M3_ALL[s], 16, axis=-1)
+    q = np.abs(x) / np.where(sv > 0, sv, 1)
+    step = np.where(q < 2, 0.5, np.where(q < 4, 1.0, 2.0))
+    unsat = q <= 6
+    assert np.all(np.abs(x - xh)[unsat] <= (0.5 * step * sv)[unsat] + 0.0)
+    cmax = np.stack([(c >> 4) & 7, c & 7], -1).reshape(512, 8, 16).max(-1)
+    again_c, again_s = O.quantize(W.f32_to_bf16_bits(xh.astype(np.float32)))
+    full = cmax == 7
+    assert np.array_equal(again_s[full], s[full])
+    cg = c.reshape(512, 8, 8)
+    assert np.array_equal(again_c.reshape(512, 8, 8)[full], cg[full])
+
+
+def test_store_head_split_and_pad_rows():
+    """An H-head store equals H single-head stores ("NVFP4 sparse KV", Tests:
+    kv_nvfp4_store over H heads equals the per-head index store); pad rows
+    (slot < 0) leave the planes untouched; an out-of-range slot is reported."""
+    H, T, P = 3, 40, 4
+    src = W.bf16_tensor(3, "st", (T, H, 128), 2, 10.0)
+    slots = W.permutation(3, "slots", P * 128)[:T].astype(np.int64)
+    slots[5] = -1
+    slots[17] = -7
+    c, s = O.new_planes(P, H)
+    c[:] = 0xA5
+    s[:] = 0x5A
+    assert O.nvfp4_store(src, slots, c, s) == 0
+    for h in range(H):
+        ch, sh = O.new_planes(P, 1)
+        ch[:] = 0xA5
+        sh[:] = 0x5A
+        O.nvfp4_store(src[:, h: h + 1], slots, ch, sh)
+        assert np.array_equal(ch[:, 0], c[:, h]) and np.array_equal(sh[:, 0], s[:, h])
+    written = set(int(v) for v in slots if v >= 0)
+    for slot in range(P * 128):
+        if slot not in written:
+            assert (c[slot // 128, :, slot % 128] == 0xA5).all()
+            assert (s[slot // 128, :, slot % 128] == 0x5A).all()
+    bad = slots.copy()
+    bad[3] = P * 128
+    c2, s2 = O.new_planes(P, H)
+    assert O.nvfp4_store(src, bad, c2, s2) == O.ERR_SLOT
+
+
+def test_record_size_reproduces_pages_block_bytes():
+    """72 B per token and head reproduces the pages' KV block bytes: the drop from
+    3,179,520 to 1,827,840 B per 128-token block over 60 sparse layers is exactly
+    2 x (132 - 72) + (128 - 72) bytes per token per layer ("NVFP4 sparse KV",
+    Results / KV capacity; FP8 record 128 + 4 B, FP8 index key 128 B)."""
+    c, s = O.quantize(np.zeros((1, 128), dtype=np.uint16))
+    rec = c.shape[-1] + s.shape[-1]
+    assert rec == 72
+    per_token = (3_179_520 - 1_827_840) // 128
+    assert per_token * 128 == 3_179_520 - 1_827_840
+    assert per_token == 60 * (2 * (132 - rec) + (128 - rec))
+
+
+def test_row_map_closed_form_vs_searchsorted():
+    """decode_rows against a brute-force mapping built the way the pages' prefill
+    row map is (searchsorted over the row offsets)."""
+    rng = np.random.default_rng(2)
+    for trial in range(50):
+        B = int(rng.integers(1, 12))
+        qb = rng.integers(0, 9, B)
+        seq = (qb + rng.integers(0, 500, B)).astype(np.int32)
+        cu = np.concatenate([[0], np.cumsum(qb)]).astype(np.int32)
+        R = int(cu[-1] + rng.integers(0, 4))
+        rr, rl = O.decode_rows(cu, seq, R)
+        r = np.arange(R)
+        b = np.searchsorted(cu, r, side="right") - 1
+        valid = r < cu[-1]
+        exp_req = np.where(valid, b, -1)
+        bb = np.clip(b, 0, B - 1)
+        exp_len = np.where(valid, seq[bb] - (cu[bb + 1] - cu[bb]) + (r - cu[bb]) + 1, 0)
+        assert np.array_equal(rr, exp_req) and np.array_equal(rl, exp_len)
+
+
+def _tiny_index_case(seed, L, hi=2, nb_pages=None):
+    """A tiny request of L tokens on shuffled pages, quantised by the oracle."""
+    nb = (L + 127) // 128
+    P = nb_pages or nb + 2
+    pages = W.permutation(seed, "tp", P)[:nb]
+    bt = pages[None, :].astype(np.int32)
+    src = W.bf16_tensor(seed, "tk", (nb * 128, 1, 128), 2, 10.0)
+    c, s = O.new_planes(P, 1)
+    slots = (pages[np.arange(nb * 128) // 128] * 128 + np.arange(nb * 128) % 128)
+    O.nvfp4_store(src, slots, c, s)
+    q = W.bf16_tensor(seed, "tq", (1, hi, 128))
+    w = W.uniform(seed, "tw", 0, hi).astype(np.float32).reshape(1, hi)
+    return bt, c, s, q, w, src
+
+
+def test_scores_brute_force_and_topk_all_subsets():
+    """Token scores by explicit Python loops; the top-k set is the best of every
+    k-subset under (higher block score, then lower id)."""
+    for seed, L, k in [(11, 300, 2), (12, 512, 3), (13, 129, 1), (14, 385, 2)]:
+        bt, c, s, q, w, _ = _tiny_index_case(seed, L)
+        rr, rl = np.array([0], np.int32), np.array([L], np.int32)
+        ids, bsc, err = O.index_score_topk(q, w, c, s, bt, rr, rl, k)
+        assert err == 0
+        qf = W.bf16_bits_to_f32(q[0]).astype(np.float64)
+        nb = (L + 127) // 128
+        brute = []
+        for b in range(nb):
+            best = -math.inf
+            for t in range(b * 128, min(b * 128 + 128, L)):
+                page = bt[0, t // 128]
+                kh = O.dequantize(c[page, 0, t % 128], s[page, 0, t % 128])
+                tot = 0.0
+                for h in range(q.shape[1]):
+                    dot = sum(float(qf[h, d]) * float(kh[d]) for d in range(128))
+                    tot += float(w[0, h]) * max(dot, 0.0)
+                best = max(best, tot)
+            brute.append(best)
+        np.testing.assert_allclose(bsc[0], brute, rtol=1e-12, atol=1e-12)
+        kk = min(k, nb)
+
+        def rank_key(sub):
+            return sorted(((brute[i], -i) for i in sub), reverse=True)
+
+        best_sub = max(itertools.combinations(range(nb), kk), key=rank_key)
+        assert list(ids[0][:kk]) == sorted(best_sub)
+        assert (ids[0][kk:] == -1).all()
+
+
+def test_zero_queries_select_lowest_ids():
+    """All-zero queries give every block the score 0; ties go to the lower block id
+    (the pages' fused top-k tie test uses zero queries)."""
+    bt, c, s, q, w, _ = _tiny_index_case(21, 1000)
+    q[:] = 0
+    ids, bsc, _ = O.index_score_topk(q, w, c, s, bt, np.array([0], np.int32),
+                                     np.array([1000], np.int32), 3)
+    assert (bsc[0] == 0).all() and list(ids[0]) == [0, 1, 2]
+
+
+def test_hot_token_is_selected():
+    """A key aligned with the query planted in block b* wins the top-1."""
+    for bstar in range(4):
+        bt, c, s, q, w, src = _tiny_index_case(30 + bstar, 512)
+        t = bstar * 128 + 77
+        hot = W.bf16_bits_to_f32(q[0, 0]).astype(np.float32) * 8
+        row = W.f32_to_bf16_bits(hot)[None, None, :]
+        page = int(bt[0, t // 128])
+        O.nvfp4_store(row, np.array([page * 128 + t % 128]), c, s)
+        w[:] = [[1.0, 0.0]]
+        ids, _, _ = O.index_score_topk(q, w, c, s, bt, np.array([0], np.int32),
+                                       np.array([512], np.int32), 1)
+        assert ids[0, 0] == bstar
+
+
+def _attn_case(seed, L, hq=4, hkv=1):
+    nb = (L + 127) // 128
+    P = nb + 1
+    pages = W.permutation(seed, "ap", P)[:nb]
+    bt = pages[None, :].astype(np.int32)
+    kc, ks = O.new_planes(P, hkv)
+    vc, vs = O.new_planes(P, hkv)
+    t = np.arange(nb * 128)
+    slots = pages[t // 128] * 128 + t % 128
+    O.nvfp4_store(W.bf16_tensor(seed, "ak", (nb * 128, hkv, 128), 2, 10.0), slots, kc, ks)
+    O.nvfp4_store(W.bf16_tensor(seed, "av", (nb * 128, hkv, 128), 2, 10.0), slots, vc, vs)
+    q = W.bf16_tensor(seed, "aq", (1, hq, 128))
+    return bt, kc, ks, vc, vs, q
+
+
+def test_attention_full_cover_equals_dense_sdpa():
+    """Top-k covering every causal block == dense causal softmax attention over the
+    whole dequantised cache (torch scaled_dot_product_attention, float64)."""
+    for L, hq, hkv in [(300, 4, 1), (640, 8, 2), (128, 2, 1)]:
+        bt, kc, ks, vc, vs, q = _attn_case(L, L, hq, hkv)
+        nb = (L + 127) // 128
+        ids = np.arange(nb, dtype=np.int32)[None, :]
+        sm = 1 / math.sqrt(128)
+        out, lse, err = O.sparse_attention(q, hkv, kc, ks, vc, vs, bt, np.array([0]),
+                                           np.array([L]), ids, sm)
+        assert err == 0
+        pages = bt[0]
+        K = O.dequantize(kc[pages], ks[pages]).transpose(1, 0, 2, 3).reshape(hkv, -1, 128)[:, :L]
+        V = O.dequantize(vc[pages], vs[pages]).transpose(1, 0, 2, 3).reshape(hkv, -1, 128)[:, :L]
+        G = hq // hkv
+        Kt = torch.from_numpy(np.repeat(K, G, axis=0))[None]
+        Vt = torch.from_numpy(np.repeat(V, G, axis=0))[None]
+        Qt = torch.from_numpy(W.bf16_bits_to_f32(q[0]).astype(np.float64))[None, :, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(Qt, Kt, Vt, scale=sm)
+        np.testing.assert_allclose(out[0], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-13)
+        logits = torch.einsum("hd,htd->ht", Qt[0, :, 0], Kt[0]) * sm
+        np.testing.assert_allclose(lse[0], torch.logsumexp(logits, -1).numpy(), rtol=1e-13)
+
+
+def test_attention_special_cases():
+    bt, kc, ks, vc, vs, q = _attn_case(41, 256)
+    p0 = bt[0, 0]
+    v0 = O.dequantize(vc[p0, 0, 0], vs[p0, 0, 0])
+    # row_len = 1: the output is exactly the first value row
+    out, lse, _ = O.sparse_attention(q, 1, kc, ks, vc, vs, bt, np.array([0]), np.array([1]),
+                                     np.array([[0, -1]]), 0.088)
+    assert np.array_equal(out[0, 0], v0)
+    # all keys equal: the output is the plain mean of V; lse = logit + log(n)
+    kc2, ks2 = kc.copy(), ks.copy()
+    kc2[:] = kc[p0, 0, 3]
+    ks2[:] = ks[p0, 0, 3]
+    L = 200
+    out, lse, _ = O.sparse_attention(q, 1, kc2, ks2, vc, vs, bt, np.array([0]), np.array([L]),
+                                     np.array([[0, 1]]), 0.088)
+    V = np.concatenate([O.dequantize(vc[bt[0, 0], 0], vs[bt[0, 0], 0]),
+                        O.dequantize(vc[bt[0, 1], 0], vs[bt[0, 1], 0])])[:L]
+    np.testing.assert_allclose(out[0, 0], V.mean(0), rtol=1e-12, atol=1e-14)
+    k0 = O.dequantize(kc[p0, 0, 3], ks[p0, 0, 3])
+    qf = W.bf16_bits_to_f32(q[0, 0]).astype(np.float64)
+    assert math.isclose(lse[0, 0], 0.088 * float(qf @ k0) + math.log(L), rel_tol=1e-12)
+    # pad rows and empty id lists give zeros and -inf
+    out, lse, err = O.sparse_attention(q, 1, kc, ks, vc, vs, bt, np.array([-1]), np.array([0]),
+                                       np.array([[0, 1]]), 0.088)
+    assert not out.any() and np.isneginf(lse).all() and err == 0
+    # an id beyond the causal blocks is an error and is skipped
+    _, _, err = O.sparse_attention(q, 1, kc, ks, vc, vs, bt, np.array([0]), np.array([100]),
+                                   np.array([[0, 1]]), 0.088)
+    assert err == O.ERR_BLOCK_ID
+
+
+def test_verify_equals_rowmap_plus_score_topk():
+    """The fused verify selection equals row map + score + top-k ("[MiniMax-M3.1]
+    FP4 index cache ...", Tests: the fused top-k selects what score + top-k selects)."""
+    wl = W.make("verify", ctx=(700, 1500, 333), q_rows=(3, 8, 1))
+    P = wl.num_pages
+    c, s = O.new_planes(P, 1)
+    O.nvfp4_store(wl.ik_src, wl.slot_all, c, s)
+    R = wl.spec.rows
+    ids_v, err = O.verify_score_topk(wl.q_idx, wl.w, c, s, wl.block_table, wl.cu_q,
+                                     wl.seq_len, R, 4)
+    rr, rl = O.decode_rows(wl.cu_q, wl.seq_len, R)
+    ids_u, _, _ = O.index_score_topk(wl.q_idx, wl.w, c, s, wl.block_table, rr, rl, 4)
+    assert err == 0 and np.array_equal(ids_v, ids_u)
+    # row j of a request sees one more token than row j-1
+    assert list(rl[3:11]) == [1500 - 8 + j + 1 for j in range(8)]
