@@ -1,0 +1,455 @@
+"""Benchmark of the NVFP4 block-sparse decode step on GB300.
+
+One step = quantise-store of the step's new K / V / index-K rows + row map +
+index score and block top-k (or the fused verify path) + block-sparse
+attention, on one batch of a synthetic workload whose cache is already
+resident in HBM. Default workload: the skewed decode batch (one 450K-token and
+seven 150K-token requests, 16 q heads, 16 index heads, top-k 16).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the fp64 CPU oracle arm
+
+Prints one JSON line (rank 0). Under torchrun every rank runs its own replica
+of the workload (the step shards by request; there is no exchange), so the
+aggregate rows/s is weak-scaled.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("sparse-attn+index rows/s and achieved HBM GB/s vs ~8 TB/s peak, bs8 mixed ctx")
+SM_SCALE = 1.0 / math.sqrt(128)
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="skewed",
+                    choices=["tiny", "decode", "verify", "skewed", "prefill"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-reps", type=int, default=2, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_config(spec, ntok):
+    return {
+        "workload": spec.description,
+        "name": spec.name,
+        "requests": spec.batch,
+        "rows": spec.rows,
+        "cached_tokens": ntok,
+        "q_heads": spec.hq,
+        "kv_heads": spec.hkv,
+        "index_heads": spec.hi,
+        "topk": spec.topk,
+        "cache_format": "NVFP4 (e2m1 + E4M3 per 16), 72 B per token and head",
+        "l2": "flushed between timed steps (a 2 x L2 scratch write outside the timed events)",
+    }
+
+
+# --------------------------------------------------------------------------
+# The CPU oracle arm (also the cpu_baseline sample)
+# --------------------------------------------------------------------------
+
+def oracle_sample(spec_name: str, reps: int):
+    """Time the oracle's step for one request of the workload.
+
+    The sample is the step of one request (its new K / V / index-K rows
+    stored, row map, score + top-k over its causal keys, attention over its
+    selected blocks). The step of the whole batch is extrapolated from it by
+    the ratio of causal keys scored (scoring dominates the oracle's time).
+    Returns (seconds per sample step, description, rows in the sample, scale).
+    """
+    import numpy as np
+
+    from nvfp4_block_sparse_m3s_gb300 import workloads as W
+    from oracle import m3s_oracle as O
+
+    wl = W.make(spec_name, with_cache_src=False)
+    s = wl.spec
+    # the sampled request: the last one (a 150K-token request for the skewed batch)
+    b = s.batch - 1
+    L = int(wl.seq_len[b])
+    t0, t1 = int(wl.tok_off[b]), int(wl.tok_off[b + 1])
+    nb = (L + 127) // 128
+    pages = wl.block_table[b, :nb].astype(np.int64)
+    kc, ks = O.new_planes(wl.num_pages, s.hkv)
+    vc, vs = O.new_planes(wl.num_pages, s.hkv)
+    ic, is_ = O.new_planes(wl.num_pages, 1)
+    ntok = wl.ntok
+    srcs = {}
+    for name, h, c, sc in (("k", s.hkv, kc, ks), ("v", s.hkv, vc, vs), ("ik", 1, ic, is_)):
+        src = W.bf16_tensor(s.seed, name, (ntok, h, 128), s.n_out, s.out_factor, rows=(t0, t1))
+        srcs[name] = src
+        O.nvfp4_store(src, wl.slot_all[t0:t1], c, sc)          # the resident cache (setup)
+    qb = int(wl.cu_q[b + 1] - wl.cu_q[b])
+    r0 = int(wl.cu_q[b])
+    cu = np.array([0, qb], dtype=np.int32)
+    seq = np.array([L], dtype=np.int32)
+    bt = wl.block_table[b: b + 1]
+    new = np.arange(L - qb, L)
+    times = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        for name, c, sc in (("k", kc, ks), ("v", vc, vs), ("ik", ic, is_)):
+            O.nvfp4_store(srcs[name][new], wl.slot_all[t0 + new], c, sc)
+        rr, rl = O.decode_rows(cu, seq, qb)
+        ids, _, _ = O.index_score_topk(wl.q_idx[r0: r0 + qb], wl.w[r0: r0 + qb], ic, is_, bt, rr,
+                                       rl, s.topk)
+        O.sparse_attention(wl.q[r0: r0 + qb], s.hkv, kc, ks, vc, vs, bt, rr, rl, ids, SM_SCALE)
+        times.append(time.perf_counter() - t)
+    t_sample = min(times)
+    keys_all = float(np.sum(wl.seq_len.astype(np.float64)))
+    scale = keys_all / L
+    desc = (f"oracle step of request {b} ({L} cached tokens, {qb} row(s)) timed {reps}x (best),"
+            f" scaled by causal keys x{scale:.2f} to the batch of {s.rows} rows")
+    return t_sample, desc, s.rows, scale
+
+
+def run_oracle_leg(args):
+    t, desc, rows, scale = oracle_sample(args.workload, args.oracle_reps)
+    print(json.dumps({"seconds_per_sample": t, "sample": desc, "rows": rows, "scale": scale,
+                      "value": rows / (t * scale), "cores": 1}))
+
+
+def cpu_baseline(workload: str, reps: int = 2):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload",
+                        workload, "--oracle-reps", str(reps)], capture_output=True, text=True,
+                       env=env, timeout=900)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["value"], "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": d["sample"]}
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from nvfp4_block_sparse_m3s_gb300 import workloads as W
+    spec = W.SPECS[args.workload]
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    # each step is one bounded sample (one request's step), extrapolated to the batch
+    t, desc, rows, scale = oracle_sample(args.workload, 1 + 0 * warm)
+    samples = [t]
+    for _ in range(min(steps, 3) - 1):
+        t2, _, _, _ = oracle_sample(args.workload, 1)
+        samples.append(t2)
+    t_best = min(samples)
+    value = rows / (t_best * scale)
+    ms = t_best * scale * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+            "n_gpus": args.gpus, "steps": len(samples), "warmup": 0, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": workload_config(spec, int(sum(spec.ctx))),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": desc + f"; {len(samples)} timed samples"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------
+# Our arm
+# --------------------------------------------------------------------------
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        sm.sort()
+        med = sm[len(sm) // 2] if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    from nvfp4_block_sparse_m3s_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    M.load()
+
+    spec = W.SPECS[args.workload]
+    wl = W.make(spec)
+    s = wl.spec
+    R = s.rows
+    fused = s.name in ("verify", "prefill")
+
+    def bf16(x):
+        return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    # ---- resident cache: planes filled by our store (setup, untimed) ----
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kc, ks = M.new_plane(wl.num_pages, s.hkv, dev)
+    vc, vs = M.new_plane(wl.num_pages, s.hkv, dev)
+    ic, is_ = M.new_plane(wl.num_pages, 1, dev)
+    slot_all = torch.from_numpy(wl.slot_all).to(dev)
+    for src, c, sc in ((wl.k_src, kc, ks), (wl.v_src, vc, vs), (wl.ik_src, ic, is_)):
+        t = bf16(src)
+        M.m3s_nvfp4_store(t, slot_all, c, sc, err)
+        del t
+    torch.cuda.synchronize()
+    new = wl.new_tok
+    host_in = {
+        "k_new": np.ascontiguousarray(wl.k_src[new]), "v_new": np.ascontiguousarray(wl.v_src[new]),
+        "ik_new": np.ascontiguousarray(wl.ik_src[new]), "slots": wl.slot_all[new].copy(),
+        "q": wl.q, "q_idx": wl.q_idx, "w": wl.w, "cu_q": wl.cu_q, "seq_len": wl.seq_len,
+    }
+    del wl.k_src, wl.v_src, wl.ik_src
+    d = {k: (bf16(v) if v.dtype == np.uint16 else torch.from_numpy(np.ascontiguousarray(v)).to(dev))
+         for k, v in host_in.items()}
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    B, bt_stride = bt.shape
+    row_req = torch.empty(R, dtype=torch.int32, device=dev)
+    row_len = torch.empty(R, dtype=torch.int32, device=dev)
+    ids = torch.empty((R, s.topk), dtype=torch.int32, device=dev)
+    bscores = torch.empty((R, bt_stride), dtype=torch.float32, device=dev)
+    out = torch.empty((R, s.hq, 128), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, s.hq), dtype=torch.float32, device=dev)
+    ws_v = torch.empty(max(16, M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, R, B, bt_stride, 0, 0,
+                                                     s.hi, s.topk, max(s.q_rows))),
+                       dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(max(16, M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, R, B, bt_stride, s.hq,
+                                                     s.hkv, 0, s.topk)),
+                       dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev_s0, ev_s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def step(score_events=None):
+        M.m3s_nvfp4_store(d["k_new"], d["slots"], kc, ks, err)
+        M.m3s_nvfp4_store(d["v_new"], d["slots"], vc, vs, err)
+        M.m3s_nvfp4_store(d["ik_new"], d["slots"], ic, is_, err)
+        M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
+        if score_events:
+            score_events[0].record(stream)
+        if fused:
+            M.m3s_verify_score_topk(d["q_idx"], d["w"], ic, is_, bt, d["cu_q"], row_len,
+                                    max(s.q_rows), s.topk, ids, ws_v, err)
+            if score_events:
+                score_events[1].record(stream)
+        else:
+            M.m3s_index_block_scores(d["q_idx"], d["w"], ic, is_, bt, row_req, row_len, bscores, err)
+            if score_events:
+                score_events[1].record(stream)
+            M.m3s_block_topk(bscores, row_req, row_len, B, bt_stride, s.topk, ids)
+        M.m3s_sparse_attention(d["q"], s.hkv, kc, ks, vc, vs, bt, row_req, row_len, ids, SM_SCALE,
+                               out, lse, ws_a, err)
+
+    nsplit_ws = ws_a.numel() > 16
+    launches_per_step = 3 + 1 + 2 + 1 + (1 if nsplit_ws else 0)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+        flush()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+
+    # algorithmic bytes (what the method must move)
+    ids_h = ids.cpu().numpy()
+    req_h = row_req.cpu().numpy()
+    distinct = 0
+    for b in range(B):
+        sel = ids_h[req_h == b]
+        distinct += len(set(int(x) for x in sel.ravel() if x >= 0))
+    keys = int(np.sum(host_in["seq_len"].astype(np.int64)))
+    nb_rows = int(np.sum((row_len.cpu().numpy().astype(np.int64) + 127) // 128))
+    score_bytes = keys * 72 + R * s.hi * (256 + 4) + nb_rows * 4
+    attn_bytes = distinct * 128 * 144 * s.hkv + R * s.hq * 256 * 2
+    store_bytes = R * (2 * s.hkv + 1) * (256 + 72)
+    step_bytes = score_bytes + attn_bytes + store_bytes + R * 8
+
+    # ---- timed region (device time, per step, L2 flushed between steps) ----
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        evs[i][0].record(stream)
+        step(sevs[i])
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    score_ms = sum(a.elapsed_time(b) for a, b in sevs) / args.steps
+    if world > 1:
+        t = torch.tensor([ms, score_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, score_ms = float(t[0]), float(t[1])
+    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
+
+    # ---- end to end through the public API with host buffers ----
+    pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host_in.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    ids_hp = torch.empty(ids.shape, dtype=ids.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = out_h.numel() * out_h.element_size() + ids_hp.numel() * ids_hp.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+
+    def copy_in():
+        for k, v in pin.items():
+            dst = d[k]
+            if dst.dtype == torch.bfloat16:
+                dst.view(torch.int16).copy_(v.view(torch.int16), non_blocking=True)
+            else:
+                dst.copy_(v, non_blocking=True)
+
+    for i in range(args.steps):
+        flush()
+        e2e_ev[i][0].record(stream)
+        copy_in()
+        step()
+        out_h.copy_(out, non_blocking=True)
+        ids_hp.copy_(ids, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    peak, src = peaks()
+    achieved = score_bytes / (score_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * R / (ms * 1e-3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(3, args.warmup),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16xf16->f32 (NVFP4 storage, exact dequant)",
+        "data": "synthetic",
+        "config": workload_config(s, keys),
+        "achieved_gbs_step": world * step_bytes / (ms * 1e-3) / 1e9,
+        "algorithmic_bytes_per_step": step_bytes,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": ("score_kernel<8> + topk (m3s_verify_score_topk)" if fused
+                                else "score_kernel<1> (m3s_index_block_scores)"),
+                     "kernel_ms": score_ms, "bytes_per_launch": score_bytes,
+                     "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)" if src == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.oracle_leg:
+        run_oracle_leg(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

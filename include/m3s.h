@@ -1,0 +1,226 @@
+/*
+ * m3s.h -- C ABI of libm3s: the decode / verify step of indexed (top-k block)
+ * sparse attention over a paged NVFP4 KV cache, hand-written CUDA for sm_103a.
+ *
+ * Source of the method: the pull requests "NVFP4 sparse KV" (ROCm/ATOM #2746)
+ * and "[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache" (ROCm/ATOM
+ * #2744), with the page layout of "MXFP4 KV cache for MiniMax-M3.1 on gfx950"
+ * (vllm-project/vllm #64198). Each entry point below names the passage that
+ * defines its operation.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Ownership: every pointer argument is caller-owned memory. Tensor
+ *    arguments are DEVICE pointers; the library never allocates, frees,
+ *    synchronises or reads device data on the host, so every call can be
+ *    captured in a CUDA graph. Host-only arguments are passed by value.
+ *  - BF16 tensors are passed as their raw 16-bit patterns (uint16_t).
+ *  - head_dim is 128 and a page (= a block) holds 128 tokens; these are the
+ *    only built values (the pages' guard requires page == 128).
+ *  - Every call returns an m3s status. Argument errors are detected on the
+ *    host before any launch and nothing is launched.
+ *  - Data-dependent errors found on the device (a slot, page or block id out
+ *    of range) never fault and are never wrapped: the kernel skips the access
+ *    and ORs an M3S_DEVERR_* bit into the caller's int32 error word `err`
+ *    (device memory, may be NULL to ignore; it is never cleared by the
+ *    library).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). All work
+ *    of a call is enqueued on it, in order.
+ *  - Alignment: plane, tensor and workspace pointers must be 16-byte aligned;
+ *    the BF16 row stride of the store must be a multiple of 8 elements.
+ */
+#ifndef M3S_H_
+#define M3S_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (return values) ---- */
+#define M3S_OK 0
+#define M3S_ERR_INVALID 1     /* null pointer, negative size, misalignment, bad stride */
+#define M3S_ERR_UNSUPPORTED 2 /* a shape outside the built bounds (head counts, top-k, ...) */
+#define M3S_ERR_WORKSPACE 3   /* ws_bytes below m3s_workspace_bytes() */
+#define M3S_ERR_LAUNCH 4      /* the CUDA launch itself failed */
+
+/* ---- device error bits (OR-ed into *err) ---- */
+#define M3S_DEVERR_SLOT 1     /* store: slot >= num_pages * 128 (row skipped) */
+#define M3S_DEVERR_BLOCK_ID 2 /* attention: a top-k id >= the row's block count or the table width */
+#define M3S_DEVERR_PAGE 4     /* a block-table entry outside [0, num_pages) (block skipped) */
+#define M3S_DEVERR_ROW 8      /* a row's request outside [0, B) or its length beyond the table */
+#define M3S_DEVERR_QRANGE 16  /* a query element beyond +-65504 (the fp16 operand range) */
+#define M3S_DEVERR_TIMEOUT 32 /* a bounded wait for an asynchronous copy gave up (kernel returned) */
+
+/* ---- limits of this build ---- */
+#define M3S_HEAD_DIM 128
+#define M3S_PAGE 128
+#define M3S_MAX_TOPK 64
+#define M3S_MAX_INDEX_HEADS 16
+#define M3S_MAX_GQA 16 /* q heads per KV head */
+
+/*
+ * A paged NVFP4 plane pair (the pool of one K, V or index-K tensor).
+ * "NVFP4 sparse KV" (ROCm/ATOM #2746), Summary: the pool's k/v and scale fields
+ * are uint8 planes; per token and head a 64 B e2m1 payload plus 8 B of E4M3
+ * scales. Within a page the payloads of the 128 tokens come first and the
+ * scales sit in their own plane (vllm #64198, Claims: [128 x payload][128 x scales]).
+ *
+ *   codes  : uint8 [num_pages][num_heads][128][64]; byte i of a token holds
+ *            element 2i in its low nibble and element 2i+1 in its high nibble;
+ *            nibble = sign(bit 3) | e2m1 magnitude code (bits 0-2).
+ *   scales : uint8 [num_pages][num_heads][128][8]; byte j is the E4M3 scale
+ *            of elements 16j .. 16j+15.
+ *   A token's slot is page * 128 + position within the page.
+ */
+typedef struct {
+  uint8_t* codes;
+  uint8_t* scales;
+  int32_t num_pages;
+  int32_t num_heads;
+} m3s_nvfp4_plane;
+
+/* ops for m3s_workspace_bytes */
+#define M3S_OP_INDEX_SCORE_TOPK 1
+#define M3S_OP_VERIFY_SCORE_TOPK 2
+#define M3S_OP_SPARSE_ATTENTION 3
+
+/*
+ * Workspace bytes an op needs (device memory the caller provides as `ws`).
+ * A pure host function of its arguments; 0 for unknown ops.
+ *   R rows, B requests, max_blocks = block-table width (bt_stride), Hq / Hkv
+ *   q and KV heads, Hi index heads, topk, max_q = the largest rows-per-request
+ *   the verify call will see (the cu_q differences).
+ * Index / verify: R * max_blocks fp32 block scores (index: 0 when the caller
+ * passes its own block_scores). Attention: the split-K partials.
+ */
+size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int32_t Hq,
+                           int32_t Hkv, int32_t Hi, int32_t topk, int32_t max_q);
+
+/*
+ * Quantise-store. "[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache"
+ * (ROCm/ATOM #2744), Design / Write path: the step's BF16 rows are quantised
+ * into the paged planes at their real slots; per 16 elements
+ * scale = e4m3(amax / 6) (saturating at 448), codes rounded half-to-even on the
+ * e2m1 grid and saturating at 6. A group whose scale rounds to 0 stores zero
+ * codes; a code's sign bit is the sign bit of the input.
+ *
+ *   src          : BF16 [T][H][128] (row r, head h at src + r*src_row_stride + h*128)
+ *   src_row_stride: elements between consecutive rows (>= H*128, multiple of 8)
+ *   slot_mapping : int64 [T]; slot < 0 = pad row, skipped and its bytes untouched
+ *                  ("NVFP4 sparse KV", Tests: pad rows stay unwritten)
+ *   dst          : the plane pair; dst.num_heads must equal H
+ * A slot >= dst.num_pages*128 sets M3S_DEVERR_SLOT and the row is skipped.
+ * T == 0 is a no-op.
+ */
+int m3s_nvfp4_store(const uint16_t* src, int64_t src_row_stride, int32_t T, int32_t H,
+                    const int64_t* slot_mapping, m3s_nvfp4_plane dst, int32_t* err,
+                    void* stream);
+
+/*
+ * Row map. #2744, Design / Attention: one launch maps each row to its request
+ * and causal length, on device, so it is valid under CUDA-graph capture.
+ * Request b owns rows cu_q[b] .. cu_q[b+1]-1 (Q_b rows) and holds seq_len[b]
+ * tokens including them; its row j attends to seq_len[b] - Q_b + j + 1 tokens.
+ * Rows r >= cu_q[B] are padding and get (row_req, row_len) = (-1, 0).
+ *   cu_q int32 [B+1] (non-decreasing, cu_q[0] = 0), seq_len int32 [B],
+ *   row_req, row_len int32 [R] outputs. B == 0 makes every row padding.
+ */
+int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int32_t R,
+                    int32_t* row_req, int32_t* row_len, void* stream);
+
+/*
+ * Lightning-indexer scoring with block top-k. #2744, Design / Index and Decode
+ * score grid; "NVFP4 sparse KV", Summary (fused verify top-k emits ids only).
+ * For row r of request b = row_req[r] with causal length L = row_len[r]:
+ *   score[t] = sum_h w[r,h] * ReLU(q_idx[r,h,:] . k_hat[t,:]),  t < L,
+ *   k_hat = the dequantised NVFP4 index key (index plane, one head),
+ *   block_score[blk] = max of score over the block's causal tokens,
+ *   topk_ids[r] = the topk blocks with the highest block score, the lower id
+ *                 on equal scores, sorted ascending, padded with -1.
+ *   q_idx BF16 [R][Hi][128], w fp32 [R][Hi], Hi <= 16,
+ *   idx_k.num_heads == 1, block_table int32 [B][bt_stride] (logical block ->
+ *   physical page), row_req / row_len from m3s_decode_rows,
+ *   topk_ids int32 [R][topk] (topk <= 64),
+ *   block_scores fp32 [R][bt_stride] or NULL: when given, receives every
+ *   row's block scores (entries past the row's block count are left as is).
+ * Rows with row_req < 0 or row_len <= 0 produce -1 ids. Needs
+ * ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, ...).
+ */
+int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
+                         m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
+                         const int32_t* row_req, const int32_t* row_len, int32_t R, int32_t B,
+                         int32_t topk, int32_t* topk_ids, float* block_scores, void* ws,
+                         size_t ws_bytes, int32_t* err, void* stream);
+
+/*
+ * The two halves of m3s_index_score_topk, for callers that want the block
+ * scores alone or time the scorer by itself.
+ * m3s_index_block_scores: block_scores fp32 [R][bs_stride] (bs_stride >=
+ * bt_stride) receives, for every valid row, the block score of each of its
+ * ceil(row_len/128) blocks; other entries are left as is.
+ * m3s_block_topk: topk_ids [R][topk] from those scores (ties to the lower id,
+ * ascending, -1 padded); row_req may be NULL (then rows are taken as valid
+ * when 0 < row_len <= bt_stride*128 and B > 0).
+ */
+int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int32_t Hi,
+                           m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
+                           const int32_t* row_req, const int32_t* row_len, int32_t R, int32_t B,
+                           float* block_scores, int32_t bs_stride, int32_t* err, void* stream);
+int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* row_req,
+                   const int32_t* row_len, int32_t R, int32_t B, int32_t bt_stride, int32_t topk,
+                   int32_t* topk_ids, void* stream);
+
+/*
+ * Fused verify score + top-k. #2744, Design / Fused verify top-k: for
+ * speculative-verify rows, index scoring and top-k in one pass over each
+ * request's keys, emitting top-k ids only (all the sparse attention reads).
+ * Same result as m3s_index_score_topk on the same rows; here the rows of one
+ * request are scored together (their queries share every key read), which
+ * also serves a prefill chunk (one request, many rows).
+ *   cu_q int32 [B+1] groups rows by request (as for m3s_decode_rows),
+ *   row_len int32 [R] their causal lengths (m3s_decode_rows),
+ *   max_q >= every cu_q[b+1]-cu_q[b] (sizes the request-row tiling).
+ * Other arguments as for m3s_index_score_topk.
+ */
+int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
+                          m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
+                          const int32_t* cu_q, const int32_t* row_len, int32_t B, int32_t R,
+                          int32_t max_q, int32_t topk, int32_t* topk_ids, void* ws,
+                          size_t ws_bytes, int32_t* err, void* stream);
+
+/*
+ * Block-sparse attention over the selected NVFP4 pages. "NVFP4 sparse KV",
+ * Summary / Attention and #2744 Design / Attention: decode and prefill rows
+ * attend over their top-k blocks, addressed by the top-k block ids and the
+ * request block table, against the dequantised K/V.
+ * For row r (request b = row_req[r], causal length L = row_len[r]) and q head h
+ * (KV head h / (Hq/Hkv)), over the tokens t of the listed blocks with t < L:
+ *   out[r,h] = sum_t softmax_t(sm_scale * q[r,h] . k_hat[t]) v_hat[t],
+ *   lse[r,h] = log sum_t exp(sm_scale * q[r,h] . k_hat[t])   (natural log).
+ *   q BF16 [R][Hq][128], out BF16 [R][Hq][128], lse fp32 [R][Hq] or NULL,
+ *   k / v planes with num_heads == Hkv, topk_ids int32 [R][topk] LOGICAL
+ *   block ids within the request (-1 = skip). Hq/Hkv <= 16, topk <= 64,
+ *   block_table int32 [B][bt_stride]; a row with row_req outside [0, B) or a
+ *   length beyond the table sets M3S_DEVERR_ROW and outputs zeros.
+ * An id >= the row's block count (or >= bt_stride) sets M3S_DEVERR_BLOCK_ID
+ * and is skipped (never wrapped onto another page). A row with no token
+ * (pad row, all ids -1) outputs zeros and lse = -inf. Duplicate ids count
+ * their block once per occurrence.
+ */
+int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_nvfp4_plane k,
+                         m3s_nvfp4_plane v, const int32_t* block_table, int32_t bt_stride,
+                         int32_t B, const int32_t* row_req, const int32_t* row_len, const int32_t* topk_ids,
+                         int32_t topk, int32_t R, float sm_scale, uint16_t* out, float* lse,
+                         void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/* Library version string (static storage). */
+const char* m3s_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* M3S_H_ */

@@ -1,0 +1,217 @@
+"""Thin ctypes binding of libm3s (argument marshalling only).
+
+The functions carry the C-ABI names and call straight into the CUDA library;
+every step of the computation runs in its kernels. Torch is used for device
+memory and streams: tensors are passed by ``data_ptr()``, the stream is
+``torch.cuda.current_stream()`` unless given. Missing outputs are allocated
+with torch on the inputs' device. A nonzero status raises ``M3SError``;
+loading fails loudly when the library has not been built.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import build as _build
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_LAUNCH = 0, 1, 2, 3, 4
+STATUS = {1: "M3S_ERR_INVALID", 2: "M3S_ERR_UNSUPPORTED", 3: "M3S_ERR_WORKSPACE",
+          4: "M3S_ERR_LAUNCH"}
+DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_PAGE, DEVERR_ROW, DEVERR_QRANGE, DEVERR_TIMEOUT = \
+    1, 2, 4, 8, 16, 32
+OP_INDEX_SCORE_TOPK, OP_VERIFY_SCORE_TOPK, OP_SPARSE_ATTENTION = 1, 2, 3
+HEAD_DIM = PAGE = 128
+
+
+class M3SError(RuntimeError):
+    pass
+
+
+class Plane(ctypes.Structure):
+    """m3s_nvfp4_plane: codes [P, H, 128, 64] and scales [P, H, 128, 8] (uint8, device)."""
+
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("num_heads", ctypes.c_int32)]
+
+
+_P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+_SIGS = {
+    "m3s_workspace_bytes": (_SZ, [ctypes.c_int, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32]),
+    "m3s_nvfp4_store": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, Plane, _P, _P]),
+    "m3s_decode_rows": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
+    "m3s_index_score_topk": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
+                                            _I32, _P, _P, _P, _SZ, _P, _P]),
+    "m3s_index_block_scores": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
+                                              _P, _I32, _P, _P]),
+    "m3s_block_topk": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "m3s_verify_score_topk": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
+                                             _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "m3s_sparse_attention": (ctypes.c_int, [_P, _I32, _I32, Plane, Plane, _P, _I32, _I32, _P, _P,
+                                            _P, _I32, _I32, _F32, _P, _P, _P, _SZ, _P, _P]),
+    "m3s_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+
+
+def load(build_if_stale: bool = True) -> ctypes.CDLL:
+    """Load libm3s.so (building it first when its sources are newer)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_stale and _build.stale():
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise M3SError(f"libm3s.so is missing ({_build.LIB}); run build() first")
+    lib = ctypes.CDLL(_build.LIB)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(rc: int, name: str) -> None:
+    if rc != OK:
+        raise M3SError(f"{name} returned {STATUS.get(rc, rc)}")
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def plane(codes: torch.Tensor, scales: torch.Tensor) -> Plane:
+    assert codes.dtype == torch.uint8 and scales.dtype == torch.uint8
+    assert codes.dim() == 4 and codes.shape[2:] == (PAGE, HEAD_DIM // 2)
+    assert scales.shape == codes.shape[:3] + (HEAD_DIM // 16,)
+    assert codes.is_contiguous() and scales.is_contiguous()
+    return Plane(codes.data_ptr(), scales.data_ptr(), codes.shape[0], codes.shape[1])
+
+
+def new_plane(num_pages: int, heads: int, device="cuda") -> tuple[torch.Tensor, torch.Tensor]:
+    return (torch.zeros((num_pages, heads, PAGE, HEAD_DIM // 2), dtype=torch.uint8, device=device),
+            torch.zeros((num_pages, heads, PAGE, HEAD_DIM // 16), dtype=torch.uint8, device=device))
+
+
+def m3s_workspace_bytes(op: int, R: int, B: int, max_blocks: int, Hq: int = 0, Hkv: int = 0,
+                        Hi: int = 0, topk: int = 0, max_q: int = 1) -> int:
+    return int(load().m3s_workspace_bytes(op, R, B, max_blocks, Hq, Hkv, Hi, topk, max_q))
+
+
+def m3s_nvfp4_store(src: torch.Tensor, slot_mapping: torch.Tensor, codes: torch.Tensor,
+                    scales: torch.Tensor, err: torch.Tensor | None = None, stream=None) -> None:
+    """src bf16 [T, H, 128] (rows may be strided), slot_mapping int64 [T]."""
+    assert src.dtype == torch.bfloat16 and src.dim() == 3 and src.shape[2] == HEAD_DIM
+    assert src.stride(2) == 1 and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
+    assert slot_mapping.dtype == torch.int64
+    T, H = src.shape[0], src.shape[1]
+    rc = load().m3s_nvfp4_store(_ptr(src), src.stride(0), T, H, _ptr(slot_mapping),
+                                plane(codes, scales), _ptr(err), _stream(stream))
+    _check(rc, "m3s_nvfp4_store")
+
+
+def m3s_decode_rows(cu_q: torch.Tensor, seq_len: torch.Tensor, R: int,
+                    row_req: torch.Tensor | None = None, row_len: torch.Tensor | None = None,
+                    stream=None):
+    B = seq_len.shape[0]
+    dev = cu_q.device
+    if row_req is None:
+        row_req = torch.empty(R, dtype=torch.int32, device=dev)
+    if row_len is None:
+        row_len = torch.empty(R, dtype=torch.int32, device=dev)
+    rc = load().m3s_decode_rows(_ptr(cu_q), _ptr(seq_len), B, R, _ptr(row_req), _ptr(row_len),
+                                _stream(stream))
+    _check(rc, "m3s_decode_rows")
+    return row_req, row_len
+
+
+def m3s_index_score_topk(q_idx, w, codes, scales, block_table, row_req, row_len, topk: int,
+                         topk_ids=None, block_scores=None, ws=None, err=None, stream=None):
+    R, Hi = q_idx.shape[0], q_idx.shape[1]
+    B, bt_stride = block_table.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((R, topk), dtype=torch.int32, device=q_idx.device)
+    if ws is None and block_scores is None:
+        nb = m3s_workspace_bytes(OP_INDEX_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
+    rc = load().m3s_index_score_topk(
+        _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride,
+        _ptr(row_req), _ptr(row_len), R, B, topk, _ptr(topk_ids), _ptr(block_scores), _ptr(ws),
+        0 if ws is None else ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
+    _check(rc, "m3s_index_score_topk")
+    return topk_ids
+
+
+def m3s_index_block_scores(q_idx, w, codes, scales, block_table, row_req, row_len, block_scores,
+                           err=None, stream=None):
+    R, Hi = q_idx.shape[0], q_idx.shape[1]
+    B, bt_stride = block_table.shape
+    rc = load().m3s_index_block_scores(
+        _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride,
+        _ptr(row_req), _ptr(row_len), R, B, _ptr(block_scores), block_scores.shape[1], _ptr(err),
+        _stream(stream))
+    _check(rc, "m3s_index_block_scores")
+    return block_scores
+
+
+def m3s_block_topk(block_scores, row_req, row_len, B: int, bt_stride: int, topk: int,
+                   topk_ids=None, stream=None):
+    R = row_len.shape[0]
+    if topk_ids is None:
+        topk_ids = torch.empty((R, topk), dtype=torch.int32, device=row_len.device)
+    rc = load().m3s_block_topk(_ptr(block_scores), block_scores.shape[1], _ptr(row_req),
+                               _ptr(row_len), R, B, bt_stride, topk, _ptr(topk_ids),
+                               _stream(stream))
+    _check(rc, "m3s_block_topk")
+    return topk_ids
+
+
+def m3s_verify_score_topk(q_idx, w, codes, scales, block_table, cu_q, row_len, max_q: int,
+                          topk: int, topk_ids=None, ws=None, err=None, stream=None):
+    R, Hi = q_idx.shape[0], q_idx.shape[1]
+    B, bt_stride = block_table.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((R, topk), dtype=torch.int32, device=q_idx.device)
+    if ws is None:
+        nb = m3s_workspace_bytes(OP_VERIFY_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, max_q)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
+    rc = load().m3s_verify_score_topk(
+        _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride, _ptr(cu_q),
+        _ptr(row_len), B, R, max_q, topk, _ptr(topk_ids), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(err), _stream(stream))
+    _check(rc, "m3s_verify_score_topk")
+    return topk_ids
+
+
+def m3s_sparse_attention(q, hkv: int, k_codes, k_scales, v_codes, v_scales, block_table, row_req,
+                         row_len, topk_ids, sm_scale: float | None = None, out=None, lse=None,
+                         ws=None, err=None, stream=None):
+    R, Hq = q.shape[0], q.shape[1]
+    B, bt_stride = block_table.shape
+    topk = topk_ids.shape[1]
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(HEAD_DIM)
+    if out is None:
+        out = torch.empty_like(q)
+    if ws is None:
+        nb = m3s_workspace_bytes(OP_SPARSE_ATTENTION, R, B, bt_stride, Hq, hkv, 0, topk)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    rc = load().m3s_sparse_attention(
+        _ptr(q), Hq, hkv, plane(k_codes, k_scales), plane(v_codes, v_scales), _ptr(block_table),
+        bt_stride, B, _ptr(row_req), _ptr(row_len), _ptr(topk_ids), topk, R, float(sm_scale),
+        _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
+        _stream(stream))
+    _check(rc, "m3s_sparse_attention")
+    return out

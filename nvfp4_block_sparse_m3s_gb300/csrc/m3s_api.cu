@@ -1,0 +1,38 @@
+// Host-side entry points that launch nothing: workspace sizing and version.
+#include <cuda_runtime.h>
+
+#include "../../include/m3s.h"
+
+namespace m3s {
+int attention_splits(int R, int Hkv, int topk, int* ips);
+}
+
+namespace {
+size_t round16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
+}  // namespace
+
+extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int32_t Hq,
+                                      int32_t Hkv, int32_t Hi, int32_t topk, int32_t max_q) {
+  (void)B;
+  (void)Hi;
+  (void)max_q;
+  if (R <= 0) return 0;
+  switch (op) {
+    case M3S_OP_INDEX_SCORE_TOPK:
+    case M3S_OP_VERIFY_SCORE_TOPK: {
+      const size_t stride = max_blocks > 0 ? static_cast<size_t>(max_blocks) : 1;
+      return round16(static_cast<size_t>(R) * stride * sizeof(float));
+    }
+    case M3S_OP_SPARSE_ATTENTION: {
+      if (Hq <= 0 || Hkv <= 0) return 0;
+      int ips = 0;
+      const int nsplit = m3s::attention_splits(R, Hkv, topk, &ips);
+      if (nsplit <= 1) return 0;
+      return round16(static_cast<size_t>(R) * Hq * nsplit * (128 + 1) * sizeof(float));
+    }
+    default:
+      return 0;
+  }
+}
+
+extern "C" const char* m3s_version(void) { return "m3s 0.1 (sm_103a)"; }

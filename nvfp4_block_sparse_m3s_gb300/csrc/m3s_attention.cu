@@ -1,0 +1,420 @@
+// Block-sparse softmax attention over the selected NVFP4 pages.
+//
+// "NVFP4 sparse KV" (ROCm/ATOM #2746), Summary / Attention and "[MiniMax-M3.1]
+// FP4 index cache and NVFP4 sparse KV cache" (#2744), Design / Attention: a
+// row attends over its top-k blocks, addressed through the request's block
+// table, against the dequantised K/V. Bad ids are reported, never wrapped
+// (review of #2744: a modulo silently mapped an invalid id onto a valid page).
+//
+// Split-K: CTA (split, kv head, row) runs an online softmax over its share of
+// the row's blocks and, when the row has several splits, leaves (o, lse) for a
+// combine pass. Inside a CTA the four warps take 32 tokens each of every
+// 128-token block: S = Q K^T with the q heads of the KV head as M (m16), then
+// P V with P re-used from the S accumulators as the A operand. K and V are
+// dequantised from the shared-memory copy of the page straight into mma
+// fragments: K in a permuted head-dim order (each thread reads one 16-byte
+// chunk of a token, the q fragments follow the same order), V two tokens at a
+// time with the nibbles of the same byte interleaved (each n8 tile covers
+// every other dimension).
+#include <cuda_runtime.h>
+
+#include "m3s_device.cuh"
+
+namespace m3s {
+namespace {
+
+constexpr int kAttWarps = 4;
+constexpr int kAttThreads = kAttWarps * 32;
+constexpr int kBlockBytes = 2 * (kPageCodeBytes + kPageScaleBytes);  // K and V: 18432
+constexpr int kPartStride = kHeadDim + 1;                            // o[128], lse
+
+struct AttnArgs {
+  const uint16_t* q;
+  int Hq, Hkv, G;
+  const uint8_t *kc, *ks, *vc, *vs;
+  int num_pages;
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t* row_req;
+  const int32_t* row_len;
+  const int32_t* ids;
+  int topk, R, B;
+  float scale_log2;  // sm_scale * log2(e)
+  int nsplit, ips;
+  uint16_t* out;
+  float* lse;
+  float* part;  // [R][Hq][nsplit][129]
+  int32_t* err;
+};
+
+struct __align__(16) AttnSmem {
+  union {
+    uint8_t stage[2][kBlockBytes];
+    struct {
+      float o[kAttWarps][16][kHeadDim];
+      float m[kAttWarps][16];
+      float l[kAttWarps][16];
+    } merge;
+  };
+  uint64_t bar[2];
+  int page[M3S_MAX_TOPK];
+  int ntok[M3S_MAX_TOPK];
+  int nblocks;
+};
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a) {
+  __shared__ AttnSmem sm;
+  const int split = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  const int len = a.row_len[r];
+  const int req = a.row_req[r];
+  const bool row_ok = req >= 0 && len > 0;
+  if (tid == 0) {
+    int n = 0;
+    if (row_ok && (req >= a.B || len > a.bt_stride * kPage)) {
+      if (split == 0 && kvh == 0) raise(a.err, M3S_DEVERR_ROW);
+    } else if (row_ok) {
+      const int nb = (len + kPage - 1) / kPage;
+      const int i0 = split * a.ips, i1 = min(a.topk, i0 + a.ips);
+      for (int i = i0; i < i1; ++i) {
+        const int id = a.ids[static_cast<size_t>(r) * a.topk + i];
+        if (id < 0) continue;
+        if (id >= nb || id >= a.bt_stride) {
+          if (kvh == 0) raise(a.err, M3S_DEVERR_BLOCK_ID);
+          continue;
+        }
+        const int page = a.block_table[static_cast<size_t>(req) * a.bt_stride + id];
+        if (page < 0 || page >= a.num_pages) {
+          if (kvh == 0) raise(a.err, M3S_DEVERR_PAGE);
+          continue;
+        }
+        sm.page[n] = page;
+        sm.ntok[n] = min(kPage, len - id * kPage);
+        ++n;
+      }
+    }
+    sm.nblocks = n;
+    mbar_init(&sm.bar[0], 1);
+    mbar_init(&sm.bar[1], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const int nblocks = sm.nblocks;
+
+  auto issue = [&](int i) {
+    const int s = i & 1;
+    const size_t rec = static_cast<size_t>(sm.page[i]) * a.Hkv + kvh;
+    uint8_t* dst = sm.stage[s];
+    fence_proxy_async();
+    mbar_expect_tx(&sm.bar[s], kBlockBytes);
+    bulk_g2s(dst, a.kc + rec * kPageCodeBytes, kPageCodeBytes, &sm.bar[s]);
+    bulk_g2s(dst + kPageCodeBytes, a.ks + rec * kPageScaleBytes, kPageScaleBytes, &sm.bar[s]);
+    bulk_g2s(dst + kPageCodeBytes + kPageScaleBytes, a.vc + rec * kPageCodeBytes, kPageCodeBytes,
+             &sm.bar[s]);
+    bulk_g2s(dst + 2 * kPageCodeBytes + kPageScaleBytes, a.vs + rec * kPageScaleBytes,
+             kPageScaleBytes, &sm.bar[s]);
+  };
+  if (tid == 0) {
+    if (nblocks > 0) issue(0);
+    if (nblocks > 1) issue(1);
+  }
+
+  // q fragments (A operand, heads as rows) in the permuted head-dim order:
+  // k-step j covers dims 32t+4j .. 32t+4j+3 for thread t.
+  uint32_t qa[8][4];
+  bool qbad = false;
+  {
+    const int h0 = g, h1 = g + 8;
+    const uint16_t* q0 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h0) * kHeadDim + 32 * t;
+    const uint16_t* q1 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h1) * kHeadDim + 32 * t;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint2 v0 = make_uint2(0u, 0u), v1 = make_uint2(0u, 0u);
+      if (h0 < a.G) v0 = *reinterpret_cast<const uint2*>(q0 + 4 * j);
+      if (h1 < a.G) v1 = *reinterpret_cast<const uint2*>(q1 + 4 * j);
+      qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
+      qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
+      qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
+      qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
+    }
+  }
+  if (qbad) raise(a.err, M3S_DEVERR_QRANGE);
+
+  float o[16][4];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 units) of heads g, g+8
+  float l0 = 0.f, l1 = 0.f;              // this thread's share of the sums
+  bool aborted = false;
+
+  for (int i = 0; i < nblocks; ++i) {
+    const int s = i & 1;
+    if (!aborted && !mbar_wait(&sm.bar[s], (i >> 1) & 1)) {
+      aborted = true;
+      if (tid == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
+      // give the copies still in flight one more bounded wait before leaving
+      mbar_wait(&sm.bar[s], (i >> 1) & 1);
+      if (i + 1 < nblocks) mbar_wait(&sm.bar[s ^ 1], ((i + 1) >> 1) & 1);
+    }
+    if (!aborted) {
+      const uint8_t* kcs = sm.stage[s];
+      const uint8_t* kss = kcs + kPageCodeBytes;
+      const uint8_t* vcs = kss + kPageScaleBytes;
+      const uint8_t* vss = vcs + kPageCodeBytes;
+      const int ntok = sm.ntok[i];
+      const int tb = warp * 32;  // this warp's first token in the block
+
+      // ---- S = Q K^T for 32 tokens (4 n8 tiles) ----
+      float sacc[4][4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        sacc[c][0] = sacc[c][1] = sacc[c][2] = sacc[c][3] = 0.f;
+        const int tok = tb + 8 * c + g;
+        const uint4 kw = *reinterpret_cast<const uint4*>(kcs + tok * kCodeBytes + 16 * t);
+        const uint32_t sc = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(kss + tok * kScaleBytes + 2 * t));
+        const uint32_t s0 = bcast_lo(sc), s1 = bcast_hi(sc);
+        const uint32_t wv[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
+          const uint32_t sj = j < 4 ? s0 : s1;
+          const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
+          const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
+          mma16816(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+        }
+      }
+      // ---- online softmax (log2 domain), causal mask inside the block ----
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int tk = tb + 8 * c + 2 * t;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool live = tk + e < ntok;
+          sacc[c][e] = live ? sacc[c][e] * a.scale_log2 : -INFINITY;
+          sacc[c][2 + e] = live ? sacc[c][2 + e] * a.scale_log2 : -INFINITY;
+          mx0 = fmaxf(mx0, sacc[c][e]);
+          mx1 = fmaxf(mx1, sacc[c][2 + e]);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+      const float c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      m0 = n0;
+      m1 = n1;
+      l0 *= c0;
+      l1 *= c1;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) {
+        o[n][0] *= c0;
+        o[n][1] *= c0;
+        o[n][2] *= c1;
+        o[n][3] *= c1;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float p0 = n0 == -INFINITY ? 0.f : exp2f(sacc[c][e] - n0);
+          const float p1 = n1 == -INFINITY ? 0.f : exp2f(sacc[c][2 + e] - n1);
+          sacc[c][e] = p0;
+          sacc[c][2 + e] = p1;
+          l0 += p0;
+          l1 += p1;
+        }
+      }
+      // ---- O += P V over the warp's 32 tokens (2 k-steps of 16) ----
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t pa0 = pack_f16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
+        const uint32_t pa1 = pack_f16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
+        const uint32_t pa2 = pack_f16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+        const uint32_t pa3 = pack_f16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+        const int t0 = tb + 16 * kk + 2 * t;  // tokens t0, t0+1 (b0) and t0+8, t0+9 (b1)
+        // bytes 8g .. 8g+7 of each token: dims 16g .. 16g+15 (scale group g)
+        const uint2 v0 = *reinterpret_cast<const uint2*>(vcs + t0 * kCodeBytes + 8 * g);
+        const uint2 v1 = *reinterpret_cast<const uint2*>(vcs + (t0 + 1) * kCodeBytes + 8 * g);
+        const uint2 v2 = *reinterpret_cast<const uint2*>(vcs + (t0 + 8) * kCodeBytes + 8 * g);
+        const uint2 v3 = *reinterpret_cast<const uint2*>(vcs + (t0 + 9) * kCodeBytes + 8 * g);
+        const uint32_t s01 = e4m3x2_to_f16x2(vss[t0 * kScaleBytes + g] | (vss[(t0 + 1) * kScaleBytes + g] << 8));
+        const uint32_t s23 = e4m3x2_to_f16x2(vss[(t0 + 8) * kScaleBytes + g] | (vss[(t0 + 9) * kScaleBytes + g] << 8));
+        const uint32_t wa[2] = {v0.x, v0.y}, wb[2] = {v1.x, v1.y};
+        const uint32_t wc[2] = {v2.x, v2.y}, wd[2] = {v3.x, v3.y};
+#pragma unroll
+        for (int hw = 0; hw < 2; ++hw) {
+          // interleave the nibbles of the two tokens: byte jj of lo01 holds
+          // (token t0, token t0+1) low nibbles = dim 16g + 2jj of both tokens
+          const uint32_t lo01 = (wa[hw] & 0x0F0F0F0Fu) | ((wb[hw] & 0x0F0F0F0Fu) << 4);
+          const uint32_t hi01 = ((wa[hw] >> 4) & 0x0F0F0F0Fu) | (wb[hw] & 0xF0F0F0F0u);
+          const uint32_t lo23 = (wc[hw] & 0x0F0F0F0Fu) | ((wd[hw] & 0x0F0F0F0Fu) << 4);
+          const uint32_t hi23 = ((wc[hw] >> 4) & 0x0F0F0F0Fu) | (wd[hw] & 0xF0F0F0F0u);
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const int jj = 4 * hw + bb;
+            const uint32_t sh = 8 * bb;
+            const uint32_t be0 = hmul2(e2m1x2_to_f16x2((lo01 >> sh) & 0xFFu), s01);
+            const uint32_t be1 = hmul2(e2m1x2_to_f16x2((lo23 >> sh) & 0xFFu), s23);
+            const uint32_t bo0 = hmul2(e2m1x2_to_f16x2((hi01 >> sh) & 0xFFu), s01);
+            const uint32_t bo1 = hmul2(e2m1x2_to_f16x2((hi23 >> sh) & 0xFFu), s23);
+            mma16816(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
+            mma16816(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
+          }
+        }
+      }
+    }
+    __syncthreads();  // every warp is done with stage s
+    if (tid == 0 && !aborted && i + 2 < nblocks) issue(i + 2);
+  }
+
+  // ---- merge the four warps ----
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  __syncthreads();
+  if (t == 0) {
+    sm.merge.m[warp][g] = m0;
+    sm.merge.m[warp][g + 8] = m1;
+    sm.merge.l[warp][g] = l0;
+    sm.merge.l[warp][g + 8] = l1;
+  }
+  // o[2jj + odd][e]: head g (e < 2) or g+8, dim 16*(2t + (e&1)) + 2jj + odd
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj)
+#pragma unroll
+    for (int odd = 0; odd < 2; ++odd)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int head = e < 2 ? g : g + 8;
+        const int dim = 16 * (2 * t + (e & 1)) + 2 * jj + odd;
+        sm.merge.o[warp][head][dim] = o[2 * jj + odd][e];
+      }
+  __syncthreads();
+
+  const int G = a.G;
+  for (int e = tid; e < G * kHeadDim; e += kAttThreads) {
+    const int head = e / kHeadDim, dim = e % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int wv = 0; wv < kAttWarps; ++wv) M = fmaxf(M, sm.merge.m[wv][head]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int wv = 0; wv < kAttWarps; ++wv) {
+        const float f = exp2f(sm.merge.m[wv][head] - M);
+        L += f * sm.merge.l[wv][head];
+        O += f * sm.merge.o[wv][head][dim];
+      }
+    }
+    const float val = L > 0.f ? O / L : 0.f;
+    const float lse_nat = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    const int qh = kvh * G + head;
+    if (a.nsplit == 1) {
+      a.out[(static_cast<size_t>(r) * a.Hq + qh) * kHeadDim + dim] = f32_to_bf16_bits(val);
+      if (a.lse && dim == 0) a.lse[static_cast<size_t>(r) * a.Hq + qh] = lse_nat;
+    } else {
+      float* p = a.part + ((static_cast<size_t>(r) * a.Hq + qh) * a.nsplit + split) * kPartStride;
+      p[dim] = val;
+      if (dim == 0) p[kHeadDim] = lse_nat;
+    }
+  }
+}
+
+// One warp per (row, q head): merge the splits' (o, lse).
+__global__ void combine_kernel(const float* __restrict__ part, int nsplit, int rows_heads,
+                               uint16_t* __restrict__ out, float* __restrict__ lse) {
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= rows_heads) return;
+  const float* p = part + static_cast<size_t>(wid) * nsplit * kPartStride;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p[s * kPartStride + kHeadDim]);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < nsplit; ++s) {
+      const float ls = p[s * kPartStride + kHeadDim];
+      if (ls == -INFINITY) continue;
+      const float f = __expf(ls - M);
+      L += f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] += f * p[s * kPartStride + 4 * lane + e];
+    }
+  }
+  uint16_t* o = out + static_cast<size_t>(wid) * kHeadDim + 4 * lane;
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const uint32_t lo = f32_to_bf16_bits(acc[0] * inv) | (static_cast<uint32_t>(f32_to_bf16_bits(acc[1] * inv)) << 16);
+  const uint32_t hi = f32_to_bf16_bits(acc[2] * inv) | (static_cast<uint32_t>(f32_to_bf16_bits(acc[3] * inv)) << 16);
+  *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
+  if (lse && lane == 0) lse[wid] = L > 0.f ? M + __logf(L) : -INFINITY;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+// Split count: enough CTAs to cover the GPU twice, at most one block per split.
+int attention_splits(int R, int Hkv, int topk, int* ips) {
+  if (topk <= 0) { *ips = 0; return 1; }
+  const long long ctas = static_cast<long long>(R) * Hkv;
+  long long want = ctas > 0 ? (2 * 152 + ctas - 1) / ctas : 1;
+  if (want < 1) want = 1;
+  if (want > topk) want = topk;
+  const int per = static_cast<int>((topk + want - 1) / want);
+  *ips = per;
+  return (topk + per - 1) / per;
+}
+
+}  // namespace m3s
+
+extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_nvfp4_plane k,
+                                    m3s_nvfp4_plane v, const int32_t* block_table,
+                                    int32_t bt_stride, int32_t B, const int32_t* row_req,
+                                    const int32_t* row_len, const int32_t* topk_ids, int32_t topk,
+                                    int32_t R, float sm_scale, uint16_t* out, float* lse, void* ws,
+                                    size_t ws_bytes, int32_t* err, void* stream) {
+  using namespace m3s;
+  if (R < 0 || B < 0 || Hq < 1 || Hkv < 1 || topk < 0 || bt_stride < 0) return M3S_ERR_INVALID;
+  if (Hq % Hkv != 0) return M3S_ERR_INVALID;
+  if (Hq / Hkv > M3S_MAX_GQA || topk > M3S_MAX_TOPK) return M3S_ERR_UNSUPPORTED;
+  if (k.num_heads != Hkv || v.num_heads != Hkv || k.num_pages != v.num_pages || k.num_pages < 0)
+    return M3S_ERR_INVALID;
+  if (R == 0) return M3S_OK;
+  if (R > 65535) return M3S_ERR_UNSUPPORTED;
+  if (!q || !out || !row_req || !row_len || (topk > 0 && !topk_ids)) return M3S_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(out)) return M3S_ERR_INVALID;
+  if (k.num_pages > 0 && (!k.codes || !k.scales || !v.codes || !v.scales || !aligned16(k.codes) ||
+                          !aligned16(k.scales) || !aligned16(v.codes) || !aligned16(v.scales)))
+    return M3S_ERR_INVALID;
+  if (B > 0 && (bt_stride < 1 || !block_table)) return M3S_ERR_INVALID;
+  int ips = 0;
+  const int nsplit = attention_splits(R, Hkv, topk, &ips);
+  if (nsplit > 1) {
+    if (ws_bytes < m3s_workspace_bytes(M3S_OP_SPARSE_ATTENTION, R, 0, bt_stride, Hq, Hkv, 0, topk, 1))
+      return M3S_ERR_WORKSPACE;
+    if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
+  }
+  AttnArgs a{q, Hq, Hkv, Hq / Hkv, k.codes, k.scales, v.codes, v.scales, k.num_pages, block_table,
+             bt_stride, row_req, row_len, topk_ids, topk, R, B,
+             sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, static_cast<float*>(ws), err};
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  attention_kernel<<<dim3(nsplit, Hkv, R), kAttThreads, 0, st>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return M3S_ERR_LAUNCH;
+  if (nsplit > 1) {
+    const int rh = R * Hq;
+    combine_kernel<<<(rh * 32 + 255) / 256, 256, 0, st>>>(static_cast<float*>(ws), nsplit, rh, out, lse);
+    if (cudaGetLastError() != cudaSuccess) return M3S_ERR_LAUNCH;
+  }
+  return M3S_OK;
+}

@@ -1,0 +1,162 @@
+// Quantise-store of BF16 rows into paged NVFP4 planes, and the row map.
+//
+// Quantisation: "[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache"
+// (ROCm/ATOM #2744), Design / Write path -- per 16 elements
+// scale = e4m3(amax / 6), codes rounded half-to-even on the e2m1 grid and
+// saturating at 6. Row map: same page, Design / Attention (one launch maps
+// each row to its request and causal length).
+#include <cuda_runtime.h>
+
+#include "m3s_device.cuh"
+
+namespace m3s {
+namespace {
+
+// e2m1 magnitude code of |x| for scale s, decided without division: the seven
+// decision points are the grid midpoints times s, which are exact in fp32 (s
+// has 4 significant bits, the midpoints at most 3). A tie (|x| equal to a
+// midpoint) goes to the even code, hence '>' below an even code and '>=' below
+// an odd one. Values beyond 5*s saturate to code 7 (6*s).
+__device__ __forceinline__ uint32_t e2m1_code(uint32_t bf16, const float (&thr)[7]) {
+  const float ax = __uint_as_float((bf16 & 0x7FFFu) << 16);
+  const uint32_t mag = (ax > thr[0]) + (ax >= thr[1]) + (ax > thr[2]) + (ax >= thr[3]) +
+                       (ax > thr[4]) + (ax >= thr[5]) + (ax > thr[6]);
+  return mag | ((bf16 >> 12) & 8u);  // sign = the sign bit of the BF16 input
+}
+
+// One 16-element group held as 8 words of BF16 pairs -> 2 words of packed codes
+// (element e in nibble e) and the scale byte.
+__device__ __forceinline__ void quantise_group(const uint32_t (&x)[8], uint32_t& lo, uint32_t& hi,
+                                               float scale) {
+  float thr[7];
+  const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+#pragma unroll
+  for (int i = 0; i < 7; ++i) thr[i] = mids[i] * scale;
+  lo = hi = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    lo |= e2m1_code(x[i] & 0xFFFFu, thr) << (8 * i);
+    lo |= e2m1_code(x[i] >> 16, thr) << (8 * i + 4);
+    hi |= e2m1_code(x[i + 4] & 0xFFFFu, thr) << (8 * i);
+    hi |= e2m1_code(x[i + 4] >> 16, thr) << (8 * i + 4);
+  }
+  if (scale == 0.0f) lo = hi = 0;  // a zero (or underflowed) scale stores zero codes
+}
+
+// Largest |x| of a group, as BF16 magnitude bits (non-negative floats order as
+// their bit patterns).
+__device__ __forceinline__ uint32_t group_amax_bits(const uint32_t (&x)[8]) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = __vmaxu2(m, x[i] & 0x7FFF7FFFu);
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// One thread quantises 32 elements (two scale groups) of one (row, head): it
+// reads 64 B, writes 16 B of codes with one 128-bit store, and the four
+// threads of a (row, head) gather their scale pairs so one of them writes the
+// 8 scale bytes with one 64-bit store.
+__global__ void __launch_bounds__(256) nvfp4_store_kernel(
+    const uint16_t* __restrict__ src, int64_t stride, int64_t total_threads, int32_t H,
+    const int64_t* __restrict__ slots, uint8_t* __restrict__ codes,
+    uint8_t* __restrict__ scales, int64_t capacity, int32_t* err) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= total_threads) return;
+  const int part = static_cast<int>(idx & 3);
+  const int64_t rh = idx >> 2;
+  const int h = static_cast<int>(rh % H);
+  const int64_t r = rh / H;
+  const int64_t slot = slots[r];
+  if (slot < 0) return;  // pad row: untouched
+  if (slot >= capacity) {
+    if (part == 0 && h == 0) raise(err, M3S_DEVERR_SLOT);
+    return;
+  }
+  const uint4* p = reinterpret_cast<const uint4*>(src + r * stride + h * kHeadDim + part * 32);
+  const uint4 v0 = __ldg(p), v1 = __ldg(p + 1), v2 = __ldg(p + 2), v3 = __ldg(p + 3);
+  const uint32_t g0[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  const uint32_t g1[8] = {v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+
+  // scale = E4M3(amax / 6): the correctly rounded fp32 quotient cannot sit on or
+  // across an E4M3 rounding boundary unless the exact quotient does (amax has 8
+  // significant bits), so fp32 division followed by a round-to-nearest-even,
+  // saturate-finite conversion gives the exact result.
+  const float q0 = __fdiv_rn(bf16_bits_to_f32(group_amax_bits(g0)), 6.0f);
+  const float q1 = __fdiv_rn(bf16_bits_to_f32(group_amax_bits(g1)), 6.0f);
+  uint16_t pair;  // byte 0 = group 2*part, byte 1 = group 2*part+1
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(q1), "f"(q0));
+  uint32_t sw = e4m3x2_to_f16x2(pair);
+  const __half2 s2 = *reinterpret_cast<const __half2*>(&sw);
+  const float s0 = __low2float(s2), s1 = __high2float(s2);
+
+  uint4 out;
+  quantise_group(g0, out.x, out.y, s0);
+  quantise_group(g1, out.z, out.w, s1);
+
+  const int64_t page = slot / kPage, pos = slot % kPage;
+  const int64_t rec = (page * H + h) * kPage + pos;
+  *reinterpret_cast<uint4*>(codes + rec * kCodeBytes + part * 16) = out;
+
+  const int lane = threadIdx.x & 31;
+  const unsigned mask = 0xFu << (lane & 28);
+  const uint32_t mine = pair;
+  const uint32_t p1 = __shfl_sync(mask, mine, (lane & 28) + 1);
+  const uint32_t p2 = __shfl_sync(mask, mine, (lane & 28) + 2);
+  const uint32_t p3 = __shfl_sync(mask, mine, (lane & 28) + 3);
+  if (part == 0) {
+    *reinterpret_cast<uint2*>(scales + rec * kScaleBytes) = make_uint2(mine | (p1 << 16), p2 | (p3 << 16));
+  }
+}
+
+__global__ void decode_rows_kernel(const int32_t* __restrict__ cu_q,
+                                   const int32_t* __restrict__ seq_len, int32_t B, int32_t R,
+                                   int32_t* __restrict__ row_req, int32_t* __restrict__ row_len) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  int32_t req = -1, len = 0;
+  if (B > 0 && r < cu_q[B]) {
+    int lo = 0, hi = B;  // cu_q[lo] <= r < cu_q[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu_q[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int qb = cu_q[lo + 1] - cu_q[lo];
+    req = lo;
+    len = seq_len[lo] - qb + (r - cu_q[lo]) + 1;
+  }
+  row_req[r] = req;
+  row_len[r] = len;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace m3s
+
+extern "C" int m3s_nvfp4_store(const uint16_t* src, int64_t src_row_stride, int32_t T, int32_t H,
+                               const int64_t* slot_mapping, m3s_nvfp4_plane dst, int32_t* err,
+                               void* stream) {
+  using namespace m3s;
+  if (T < 0 || H <= 0 || dst.num_pages < 0 || dst.num_heads != H) return M3S_ERR_INVALID;
+  if (T == 0) return M3S_OK;
+  if (!src || !slot_mapping || !dst.codes || !dst.scales) return M3S_ERR_INVALID;
+  if (!aligned16(src) || !aligned16(dst.codes) || !aligned16(dst.scales)) return M3S_ERR_INVALID;
+  if (src_row_stride < static_cast<int64_t>(H) * kHeadDim || (src_row_stride & 7)) return M3S_ERR_INVALID;
+  const int64_t total = static_cast<int64_t>(T) * H * 4;
+  const int64_t blocks = (total + 255) / 256;
+  if (blocks > 0x7FFFFFFF) return M3S_ERR_UNSUPPORTED;
+  nvfp4_store_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      src, src_row_stride, total, H, slot_mapping, dst.codes, dst.scales,
+      static_cast<int64_t>(dst.num_pages) * kPage, err);
+  return cudaGetLastError() == cudaSuccess ? M3S_OK : M3S_ERR_LAUNCH;
+}
+
+extern "C" int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int32_t R,
+                               int32_t* row_req, int32_t* row_len, void* stream) {
+  if (B < 0 || R < 0) return M3S_ERR_INVALID;
+  if (R == 0) return M3S_OK;
+  if (!cu_q || !row_req || !row_len || (B > 0 && !seq_len)) return M3S_ERR_INVALID;
+  m3s::decode_rows_kernel<<<(R + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      cu_q, seq_len, B, R, row_req, row_len);
+  return cudaGetLastError() == cudaSuccess ? M3S_OK : M3S_ERR_LAUNCH;
+}

@@ -70,11 +70,17 @@ def uniform(seed: int, name: str, start: int, count: int) -> np.ndarray:
     return (b.astype(np.float64) + 0.5) * (2.0 ** -53)
 
 
-def _normal_chunk(seed: int, name: str, start_pair: int, npairs: int) -> np.ndarray:
-    u = uniform(seed, name, 2 * start_pair, 2 * npairs)
+def normal_slice(seed: int, name: str, start: int, count: int) -> np.ndarray:
+    """Elements [start, start+count) of the named standard-normal stream (start, count even).
+
+    Variates 2i and 2i+1 are the cosine and sine outputs of the Box-Muller
+    transform of uniforms 2i and 2i+1 of the stream.
+    """
+    assert start % 2 == 0 and count % 2 == 0
+    u = uniform(seed, name, start, count)
     r = np.sqrt(-2.0 * np.log(u[0::2]))
     th = (2.0 * np.pi) * u[1::2]
-    out = np.empty(2 * npairs, dtype=np.float64)
+    out = np.empty(count, dtype=np.float64)
     out[0::2] = r * np.cos(th)
     out[1::2] = r * np.sin(th)
     return out
@@ -86,19 +92,7 @@ def _threads() -> int:
 
 def normal(seed: int, name: str, count: int) -> np.ndarray:
     """``count`` standard normal float64 variates of the named stream."""
-    npairs = (count + 1) // 2
-    chunk = 1 << 21
-    if npairs <= chunk:
-        return _normal_chunk(seed, name, 0, npairs)[:count]
-    out = np.empty(2 * npairs, dtype=np.float64)
-
-    def work(p0: int) -> None:
-        n = min(chunk, npairs - p0)
-        out[2 * p0: 2 * (p0 + n)] = _normal_chunk(seed, name, p0, n)
-
-    with ThreadPoolExecutor(_threads()) as ex:
-        list(ex.map(work, range(0, npairs, chunk)))
-    return out[:count]
+    return normal_slice(seed, name, 0, count + (count & 1))[:count]
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -127,14 +121,34 @@ def outlier_channels(seed: int, name: str, n_out: int) -> np.ndarray:
 
 
 def bf16_tensor(seed: int, name: str, shape: tuple, n_out: int = 0, factor: float = 1.0,
-                ) -> np.ndarray:
-    """BF16 bits of N(0,1) values; ``n_out`` channels of the last axis scaled by ``factor``."""
-    count = int(np.prod(shape))
-    x = normal(seed, name, count).reshape(shape)
-    if n_out:
-        ch = outlier_channels(seed, name, n_out)
-        x[..., ch] *= factor
-    return f32_to_bf16_bits(x.astype(np.float32))
+                rows: tuple | None = None) -> np.ndarray:
+    """BF16 bits of N(0,1) values; ``n_out`` channels of the last axis scaled by ``factor``.
+
+    ``rows=(r0, r1)`` draws only rows r0..r1-1 of the first axis; they are
+    bit-identical to the same rows of the full draw. Large draws run in threads.
+    """
+    per_row = int(np.prod(shape[1:]))
+    r0, r1 = rows if rows is not None else (0, shape[0])
+    out = np.empty((r1 - r0,) + tuple(shape[1:]), dtype=np.uint16)
+    ch = outlier_channels(seed, name, n_out) if n_out else None
+    pad = per_row & 1            # keep every row on a Box-Muller pair boundary
+
+    def work(a: int, b: int) -> None:
+        x = normal_slice(seed, name, a * (per_row + pad), (b - a) * (per_row + pad))
+        x = x.reshape(b - a, per_row + pad)[:, :per_row].reshape((b - a,) + tuple(shape[1:]))
+        if ch is not None:
+            x[..., ch] *= factor
+        out[a - r0: b - r0] = f32_to_bf16_bits(x.astype(np.float32))
+
+    step = max(1, (1 << 20) // max(per_row, 1))
+    spans = [(a, min(r1, a + step)) for a in range(r0, r1, step)]
+    if len(spans) <= 1:
+        for a, b in spans:
+            work(a, b)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(lambda ab: work(*ab), spans))
+    return out
 
 
 @dataclasses.dataclass(frozen=True)

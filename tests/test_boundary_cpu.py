@@ -1,0 +1,78 @@
+"""CPU checks of the C-ABI boundary: the library builds and loads, exports every
+function include/m3s.h declares, and rejects bad arguments on the host before
+any launch (these calls never reach the GPU)."""
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "m3s.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(m3s_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available to build the library")
+    from nvfp4_block_sparse_m3s_gb300 import binding
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("m3s_nvfp4_store", "m3s_decode_rows", "m3s_index_score_topk",
+              "m3s_verify_score_topk", "m3s_sparse_attention", "m3s_workspace_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert lib.m3s_version().startswith(b"m3s")
+
+
+def test_workspace_sizes(lib):
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600) == 8 * 3600 * 4
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 0, 8, 3600) == 0
+    # decode batch: one block per split -> 16 splits of (o[128], lse) per (row, head)
+    assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == \
+        8 * 16 * 16 * 129 * 4
+    # many rows: no split, no workspace
+    assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8192, 1, 2112, 16, 1, 16, 16) == 0
+    assert M.m3s_workspace_bytes(99, 8, 8, 8) == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    P = M.Plane(None, None, 4, 1)
+    # null source
+    assert lib.m3s_nvfp4_store(None, 128, 4, 1, None, P, None, None) == M.ERR_INVALID
+    # head count mismatch with the plane
+    assert lib.m3s_nvfp4_store(None, 128, 4, 2, None, P, None, None) == M.ERR_INVALID
+    # nothing to do
+    assert lib.m3s_nvfp4_store(None, 128, 0, 1, None, P, None, None) == M.OK
+    assert lib.m3s_decode_rows(None, None, 1, 0, None, None, None) == M.OK
+    assert lib.m3s_decode_rows(None, None, -1, 4, None, None, None) == M.ERR_INVALID
+    # too many index heads / top-k beyond the build
+    assert lib.m3s_index_score_topk(None, None, 17, P, None, 1, None, None, 1, 1, 8, None, None,
+                                    None, 0, None, None) == M.ERR_UNSUPPORTED
+    assert lib.m3s_index_score_topk(None, None, 16, P, None, 1, None, None, 1, 1, 65, None, None,
+                                    None, 0, None, None) == M.ERR_UNSUPPORTED
+    # attention: q heads not a multiple of KV heads, GQA beyond 16
+    P2 = M.Plane(None, None, 4, 1)
+    assert lib.m3s_sparse_attention(None, 6, 4, P2, P2, None, 1, 1, None, None, None, 16, 1,
+                                    ctypes.c_float(0.1), None, None, None, 0, None,
+                                    None) == M.ERR_INVALID
+    assert lib.m3s_sparse_attention(None, 32, 1, P2, P2, None, 1, 1, None, None, None, 16, 1,
+                                    ctypes.c_float(0.1), None, None, None, 0, None,
+                                    None) == M.ERR_UNSUPPORTED
