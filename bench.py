@@ -112,7 +112,7 @@ def oracle_sample(spec_name: str, reps: int):
     cu = np.array([0, qb], dtype=np.int32)
     seq = np.array([L], dtype=np.int32)
     bt = wl.block_table[b: b + 1]
-    new = np.arange(L - qb, L)
+    new = wl.new_tok[(wl.new_tok >= t0) & (wl.new_tok < t1)] - t0    # this step's rows of b
     times = []
     for _ in range(reps):
         t = time.perf_counter()
@@ -183,53 +183,79 @@ def run_reference(args):
 # --------------------------------------------------------------------------
 
 class Clocks:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and clock-event reasons sampled through NVML (ctypes) in a thread
+    every 2 ms while the timed region runs; nvidia-smi is the fallback."""
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.threading = threading
+        self.samples = []
+        self.max_mhz = None
+        self.h = None
+        self.err = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            import torch
+            props = torch.cuda.get_device_properties(torch_device)
+            ok = False
+            uuid = getattr(props, "uuid", None)
+            if uuid is not None:
+                ok = lib.nvmlDeviceGetHandleByUUID(f"GPU-{uuid}".encode(), ctypes.byref(h)) == 0
+            if not ok and hasattr(props, "pci_bus_id"):
+                bus = f"{getattr(props, 'pci_domain_id', 0):08X}:{props.pci_bus_id:02X}:" \
+                      f"{getattr(props, 'pci_device_id', 0):02X}.0"
+                ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            if not ok:
+                ok = lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) == 0
+            if not ok:
+                raise RuntimeError("no NVML handle")
+            self.lib, self.h = lib, h
+            m = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = float(m.value)
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception as e:  # no NVML on this machine
+            self.err = str(e)
+
+    def _run(self):
+        ct = self.ct
+        c = ct.c_uint()
+        r = ct.c_ulonglong()
+        while not self.stop_flag:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(c)) == 0:
+                rv = r.value if self.reasons_fn(self.h, ct.byref(r)) == 0 else 0
+                self.samples.append((float(c.value), int(rv)))
+            time.sleep(0.002)
 
     def start(self):
-        try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
-                stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+        self.stop_flag = False
+        if self.h is not None:
+            self.t = self.threading.Thread(target=self._run, daemon=True)
+            self.t.start()
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.f.close()
-        sm, smax, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
-                continue
-            try:
-                sm.append(float(p[1]))
-                smax = float(p[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, p[5:9]):
-                if v.lower().startswith("active"):
+        self.stop_flag = True
+        if self.h is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [f"NVML unavailable: {self.err}"]}
+        self.t.join()
+        sm = sorted(v for v, _ in self.samples)
+        reasons = set()
+        for _, bits in self.samples:
+            for b, n in self.REASONS.items():
+                if bits & b:
                     reasons.add(n)
-        sm.sort()
-        med = sm[len(sm) // 2] if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "source": "NVML, 2 ms sampling during the timed region"}
 
 
 def run_ours(args):
@@ -295,28 +321,59 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     ev_s0, ev_s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    def step(score_events=None):
-        M.m3s_nvfp4_store(d["k_new"], d["slots"], kc, ks, err)
-        M.m3s_nvfp4_store(d["v_new"], d["slots"], vc, vs, err)
-        M.m3s_nvfp4_store(d["ik_new"], d["slots"], ic, is_, err)
-        M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
-        if score_events:
-            score_events[0].record(stream)
+    side = torch.cuda.Stream(device=dev)
+
+    def pre():
+        # the row map runs on a parallel branch beside the batched store
+        cur = torch.cuda.current_stream()
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
+        M.m3s_nvfp4_store_batch([(d["k_new"], kc, ks), (d["v_new"], vc, vs), (d["ik_new"], ic, is_)],
+                                d["slots"], err)
+        cur.wait_stream(side)
+
+    def score():
         if fused:
             M.m3s_verify_score_topk(d["q_idx"], d["w"], ic, is_, bt, d["cu_q"], row_len,
                                     max(s.q_rows), s.topk, ids, ws_v, err)
-            if score_events:
-                score_events[1].record(stream)
         else:
             M.m3s_index_block_scores(d["q_idx"], d["w"], ic, is_, bt, row_req, row_len, bscores, err)
-            if score_events:
-                score_events[1].record(stream)
+
+    def topk():
+        if not fused:
             M.m3s_block_topk(bscores, row_req, row_len, B, bt_stride, s.topk, ids)
+
+    def attn():
         M.m3s_sparse_attention(d["q"], s.hkv, kc, ks, vc, vs, bt, row_req, row_len, ids, SM_SCALE,
                                out, lse, ws_a, err)
 
-    nsplit_ws = ws_a.numel() > 16
-    launches_per_step = 3 + 1 + 2 + 1 + (1 if nsplit_ws else 0)
+    # eager warm-up (sets kernel attributes), then one CUDA graph per phase; the
+    # scorer's graph sits alone between two events so its duration is measured live
+    phases = [pre, score, topk, attn] if not fused else [pre, score, attn]
+    for _ in range(2):
+        for fn in phases:
+            fn()
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream(device=dev)
+    for fn in phases:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def step(phase_events=None):
+        # phase_events: len(phases)+1 events bracketing each phase's graph
+        for i, g in enumerate(graphs):
+            if phase_events:
+                phase_events[i].record(stream)
+            g.replay()
+        if phase_events:
+            phase_events[-1].record(stream)
+
+    launches_per_step = 5   # batched store, row map, scorer, top-k, attention
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -345,26 +402,24 @@ def run_ours(args):
     step_bytes = score_bytes + attn_bytes + store_bytes + R * 8
 
     # ---- timed region (device time, per step, L2 flushed between steps) ----
-    clocks = Clocks(local)
+    clocks = Clocks(dev)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
            for _ in range(args.steps)]
-    sevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
     for i in range(args.steps):
         flush()
-        evs[i][0].record(stream)
-        step(sevs[i])
-        evs[i][1].record(stream)
+        step(pev[i])
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
-    score_ms = sum(a.elapsed_time(b) for a, b in sevs) / args.steps
+    ms = sum(e[0].elapsed_time(e[-1]) for e in pev) / args.steps
+    phase_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in pev) / args.steps
+                for j in range(len(phases))]
+    score_ms = phase_ms[1]
     if world > 1:
         t = torch.tensor([ms, score_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -431,6 +486,7 @@ def run_ours(args):
         "e2e": {"value": world * R / (e2e_ms * 1e-3), "unit": "rows/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "phases_ms": {fn.__name__: round(v, 5) for fn, v in zip(phases, phase_ms)},
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

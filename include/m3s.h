@@ -94,7 +94,8 @@ typedef struct {
  *   q and KV heads, Hi index heads, topk, max_q = the largest rows-per-request
  *   the verify call will see (the cu_q differences).
  * Index / verify: R * max_blocks fp32 block scores (index: 0 when the caller
- * passes its own block_scores). Attention: the split-K partials.
+ * passes its own block_scores). Attention: 0 (its split-K partials are merged
+ * on chip); its ws arguments are accepted and ignored.
  */
 size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int32_t Hq,
                            int32_t Hkv, int32_t Hi, int32_t topk, int32_t max_q);
@@ -118,6 +119,23 @@ size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int
 int m3s_nvfp4_store(const uint16_t* src, int64_t src_row_stride, int32_t T, int32_t H,
                     const int64_t* slot_mapping, m3s_nvfp4_plane dst, int32_t* err,
                     void* stream);
+
+/*
+ * Batched quantise-store: up to M3S_MAX_STORE_JOBS tensors whose rows share
+ * one slot mapping (a step's new K, V and index-K rows), in one launch. Each
+ * job is quantised exactly as m3s_nvfp4_store would. `jobs` is a HOST array
+ * (read during the call); each job's src row r holds job.H heads.
+ */
+#define M3S_MAX_STORE_JOBS 4
+typedef struct {
+  const uint16_t* src;    /* BF16 [T][H][128] device rows */
+  int64_t src_row_stride; /* elements between rows (>= H*128, multiple of 8) */
+  int32_t H;              /* heads per row; must equal dst.num_heads */
+  m3s_nvfp4_plane dst;
+} m3s_store_job;
+
+int m3s_nvfp4_store_batch(const m3s_store_job* jobs, int32_t njobs, int32_t T,
+                          const int64_t* slot_mapping, int32_t* err, void* stream);
 
 /*
  * Row map. #2744, Design / Attention: one launch maps each row to its request

@@ -38,11 +38,19 @@ class Plane(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("num_heads", ctypes.c_int32)]
 
 
+class StoreJob(ctypes.Structure):
+    """m3s_store_job: one tensor of a batched store."""
+
+    _fields_ = [("src", ctypes.c_void_p), ("src_row_stride", ctypes.c_int64),
+                ("H", ctypes.c_int32), ("dst", Plane)]
+
+
 _P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                              ctypes.c_size_t)
 _SIGS = {
     "m3s_workspace_bytes": (_SZ, [ctypes.c_int, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32]),
     "m3s_nvfp4_store": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, Plane, _P, _P]),
+    "m3s_nvfp4_store_batch": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "m3s_decode_rows": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
     "m3s_index_score_topk": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
                                             _I32, _P, _P, _P, _SZ, _P, _P]),
@@ -120,6 +128,21 @@ def m3s_nvfp4_store(src: torch.Tensor, slot_mapping: torch.Tensor, codes: torch.
     rc = load().m3s_nvfp4_store(_ptr(src), src.stride(0), T, H, _ptr(slot_mapping),
                                 plane(codes, scales), _ptr(err), _stream(stream))
     _check(rc, "m3s_nvfp4_store")
+
+
+def m3s_nvfp4_store_batch(jobs, slot_mapping: torch.Tensor, err: torch.Tensor | None = None,
+                          stream=None) -> None:
+    """jobs: sequence of (src bf16 [T, H, 128], codes, scales) sharing ``slot_mapping``."""
+    assert slot_mapping.dtype == torch.int64
+    arr = (StoreJob * max(1, len(jobs)))()
+    T = slot_mapping.shape[0]
+    for i, (src, codes, scales) in enumerate(jobs):
+        assert src.dtype == torch.bfloat16 and src.dim() == 3 and src.shape[0] == T
+        assert src.stride(2) == 1 and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
+        arr[i] = StoreJob(src.data_ptr(), src.stride(0), src.shape[1], plane(codes, scales))
+    rc = load().m3s_nvfp4_store_batch(arr, len(jobs), T, _ptr(slot_mapping), _ptr(err),
+                                      _stream(stream))
+    _check(rc, "m3s_nvfp4_store_batch")
 
 
 def m3s_decode_rows(cu_q: torch.Tensor, seq_len: torch.Tensor, R: int,

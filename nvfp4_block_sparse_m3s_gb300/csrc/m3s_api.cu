@@ -3,10 +3,6 @@
 
 #include "../../include/m3s.h"
 
-namespace m3s {
-int attention_splits(int R, int Hkv, int topk, int* ips);
-}
-
 namespace {
 size_t round16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
 }  // namespace
@@ -23,13 +19,9 @@ extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_
       const size_t stride = max_blocks > 0 ? static_cast<size_t>(max_blocks) : 1;
       return round16(static_cast<size_t>(R) * stride * sizeof(float));
     }
-    case M3S_OP_SPARSE_ATTENTION: {
-      if (Hq <= 0 || Hkv <= 0) return 0;
-      int ips = 0;
-      const int nsplit = m3s::attention_splits(R, Hkv, topk, &ips);
-      if (nsplit <= 1) return 0;
-      return round16(static_cast<size_t>(R) * Hq * nsplit * (128 + 1) * sizeof(float));
-    }
+    case M3S_OP_SPARSE_ATTENTION:
+      // split-K partials are combined inside a thread-block cluster: no workspace
+      return 0;
     default:
       return 0;
   }

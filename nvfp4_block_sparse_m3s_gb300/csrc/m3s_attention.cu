@@ -6,16 +6,19 @@
 // table, against the dequantised K/V. Bad ids are reported, never wrapped
 // (review of #2744: a modulo silently mapped an invalid id onto a valid page).
 //
-// Split-K: CTA (split, kv head, row) runs an online softmax over its share of
-// the row's blocks and, when the row has several splits, leaves (o, lse) for a
-// combine pass. Inside a CTA the four warps take 32 tokens each of every
-// 128-token block: S = Q K^T with the q heads of the KV head as M (m16), then
-// P V with P re-used from the S accumulators as the A operand. K and V are
-// dequantised from the shared-memory copy of the page straight into mma
-// fragments: K in a permuted head-dim order (each thread reads one 16-byte
-// chunk of a token, the q fragments follow the same order), V two tokens at a
-// time with the nibbles of the same byte interleaved (each n8 tile covers
-// every other dimension).
+// Split-K inside a thread-block cluster: the CTAs (split, kv head, row) of one
+// (kv head, row) form a cluster; each runs an online softmax over its share of
+// the row's blocks, leaves (m, l, o) in its shared memory, and cluster rank 0
+// combines the partials through distributed shared memory and writes the
+// output, so there is no second launch and no workspace round trip. Inside a
+// CTA the four warps take 32 tokens each of every 128-token block: S = Q K^T
+// with the q heads of the KV head as M (m16), then P V with P re-used from the
+// S accumulators as the A operand. K and V are dequantised from the
+// shared-memory copy of the page straight into mma fragments: K in a permuted
+// head-dim order (each thread reads one 16-byte chunk of a token, the q
+// fragments follow the same order), V two tokens at a time with the nibbles of
+// the same byte interleaved (each n8 tile covers every other dimension).
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include "m3s_device.cuh"
@@ -24,9 +27,8 @@ namespace m3s {
 namespace {
 
 constexpr int kAttWarps = 4;
-constexpr int kAttThreads = kAttWarps * 32;
+constexpr int kAttThreads = kAttWarps * 32;  // == head_dim: one thread per output dim
 constexpr int kBlockBytes = 2 * (kPageCodeBytes + kPageScaleBytes);  // K and V: 18432
-constexpr int kPartStride = kHeadDim + 1;                            // o[128], lse
 
 struct AttnArgs {
   const uint16_t* q;
@@ -43,7 +45,6 @@ struct AttnArgs {
   int nsplit, ips;
   uint16_t* out;
   float* lse;
-  float* part;  // [R][Hq][nsplit][129]
   int32_t* err;
 };
 
@@ -56,6 +57,9 @@ struct __align__(16) AttnSmem {
       float l[kAttWarps][16];
     } merge;
   };
+  float cta_o[16][kHeadDim];  // this CTA's partial: sum p v, relative to cta_m (log2 units)
+  float cta_m[16];
+  float cta_l[16];
   uint64_t bar[2];
   int page[M3S_MAX_TOPK];
   int ntok[M3S_MAX_TOPK];
@@ -73,38 +77,75 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
-  const int len = a.row_len[r];
-  const int req = a.row_req[r];
-  const bool row_ok = req >= 0 && len > 0;
-  if (tid == 0) {
-    int n = 0;
-    if (row_ok && (req >= a.B || len > a.bt_stride * kPage)) {
-      if (split == 0 && kvh == 0) raise(a.err, M3S_DEVERR_ROW);
-    } else if (row_ok) {
-      const int nb = (len + kPage - 1) / kPage;
-      const int i0 = split * a.ips, i1 = min(a.topk, i0 + a.ips);
-      for (int i = i0; i < i1; ++i) {
-        const int id = a.ids[static_cast<size_t>(r) * a.topk + i];
-        if (id < 0) continue;
-        if (id >= nb || id >= a.bt_stride) {
-          if (kvh == 0) raise(a.err, M3S_DEVERR_BLOCK_ID);
-          continue;
-        }
-        const int page = a.block_table[static_cast<size_t>(req) * a.bt_stride + id];
-        if (page < 0 || page >= a.num_pages) {
-          if (kvh == 0) raise(a.err, M3S_DEVERR_PAGE);
-          continue;
-        }
-        sm.page[n] = page;
-        sm.ntok[n] = min(kPage, len - id * kPage);
-        ++n;
-      }
+  pdl_trigger();
+  pdl_wait();
+  // q fragments (A operand, heads as rows) in the permuted head-dim order:
+  // k-step j covers dims 32t+4j .. 32t+4j+3 for thread t. Loaded first: they do
+  // not depend on the block list.
+  uint32_t qa[8][4];
+  bool qbad = false;
+  {
+    const int h0 = g, h1 = g + 8;
+    const uint16_t* q0 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h0) * kHeadDim + 32 * t;
+    const uint16_t* q1 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h1) * kHeadDim + 32 * t;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint2 v0 = make_uint2(0u, 0u), v1 = make_uint2(0u, 0u);
+      if (h0 < a.G) v0 = *reinterpret_cast<const uint2*>(q0 + 4 * j);
+      if (h1 < a.G) v1 = *reinterpret_cast<const uint2*>(q1 + 4 * j);
+      qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
+      qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
+      qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
+      qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
     }
-    sm.nblocks = n;
-    mbar_init(&sm.bar[0], 1);
-    mbar_init(&sm.bar[1], 1);
-    mbar_fence_init();
   }
+
+  // The block list of this split: warp 0 reads the ids, checks them, looks the
+  // pages up in parallel and compacts the valid ones.
+  if (warp == 0) {
+    const int len = a.row_len[r];
+    const int req = a.row_req[r];
+    const bool row_ok = req >= 0 && len > 0;
+    const bool row_bad = row_ok && (req >= a.B || len > a.bt_stride * kPage);
+    if (row_bad && lane == 0 && split == 0 && kvh == 0) raise(a.err, M3S_DEVERR_ROW);
+    const int nb = (len + kPage - 1) / kPage;
+    const int i0 = split * a.ips, i1 = min(a.topk, i0 + a.ips);
+    int n = 0;
+    for (int base = i0; base < i1; base += 32) {
+      const int i = base + lane;
+      int page = -1, ntok = 0;
+      if (row_ok && !row_bad && i < i1) {
+        const int id = a.ids[static_cast<size_t>(r) * a.topk + i];
+        if (id >= 0) {
+          if (id >= nb || id >= a.bt_stride) {
+            if (kvh == 0) raise(a.err, M3S_DEVERR_BLOCK_ID);
+          } else {
+            page = a.block_table[static_cast<size_t>(req) * a.bt_stride + id];
+            if (page < 0 || page >= a.num_pages) {
+              if (kvh == 0) raise(a.err, M3S_DEVERR_PAGE);
+              page = -1;
+            } else {
+              ntok = min(kPage, len - id * kPage);
+            }
+          }
+        }
+      }
+      const unsigned keep = __ballot_sync(0xffffffffu, page >= 0);
+      if (page >= 0) {
+        const int at = n + __popc(keep & ((1u << lane) - 1u));
+        sm.page[at] = page;
+        sm.ntok[at] = ntok;
+      }
+      n += __popc(keep);
+    }
+    if (lane == 0) {
+      sm.nblocks = n;
+      mbar_init(&sm.bar[0], 1);
+      mbar_init(&sm.bar[1], 1);
+      mbar_fence_init();
+    }
+  }
+  if (qbad) raise(a.err, M3S_DEVERR_QRANGE);
   __syncthreads();
   const int nblocks = sm.nblocks;
 
@@ -125,27 +166,6 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     if (nblocks > 0) issue(0);
     if (nblocks > 1) issue(1);
   }
-
-  // q fragments (A operand, heads as rows) in the permuted head-dim order:
-  // k-step j covers dims 32t+4j .. 32t+4j+3 for thread t.
-  uint32_t qa[8][4];
-  bool qbad = false;
-  {
-    const int h0 = g, h1 = g + 8;
-    const uint16_t* q0 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h0) * kHeadDim + 32 * t;
-    const uint16_t* q1 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h1) * kHeadDim + 32 * t;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint2 v0 = make_uint2(0u, 0u), v1 = make_uint2(0u, 0u);
-      if (h0 < a.G) v0 = *reinterpret_cast<const uint2*>(q0 + 4 * j);
-      if (h1 < a.G) v1 = *reinterpret_cast<const uint2*>(q1 + 4 * j);
-      qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
-      qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
-      qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
-      qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
-    }
-  }
-  if (qbad) raise(a.err, M3S_DEVERR_QRANGE);
 
   float o[16][4];
 #pragma unroll
@@ -302,8 +322,9 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       }
   __syncthreads();
 
+  // this CTA's partial over its blocks: (M, L, O) per head, O relative to 2^M
   const int G = a.G;
-  for (int e = tid; e < G * kHeadDim; e += kAttThreads) {
+  for (int e = tid; e < 16 * kHeadDim; e += kAttThreads) {
     const int head = e / kHeadDim, dim = e % kHeadDim;
     float M = -INFINITY;
 #pragma unroll
@@ -317,59 +338,70 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
         O += f * sm.merge.o[wv][head][dim];
       }
     }
-    const float val = L > 0.f ? O / L : 0.f;
-    const float lse_nat = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-    const int qh = kvh * G + head;
-    if (a.nsplit == 1) {
-      a.out[(static_cast<size_t>(r) * a.Hq + qh) * kHeadDim + dim] = f32_to_bf16_bits(val);
-      if (a.lse && dim == 0) a.lse[static_cast<size_t>(r) * a.Hq + qh] = lse_nat;
-    } else {
-      float* p = a.part + ((static_cast<size_t>(r) * a.Hq + qh) * a.nsplit + split) * kPartStride;
-      p[dim] = val;
-      if (dim == 0) p[kHeadDim] = lse_nat;
+    sm.cta_o[head][dim] = O;
+    if (dim == 0) {
+      sm.cta_m[head] = M;
+      sm.cta_l[head] = L;
     }
   }
-}
-
-// One warp per (row, q head): merge the splits' (o, lse).
-__global__ void combine_kernel(const float* __restrict__ part, int nsplit, int rows_heads,
-                               uint16_t* __restrict__ out, float* __restrict__ lse) {
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= rows_heads) return;
-  const float* p = part + static_cast<size_t>(wid) * nsplit * kPartStride;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, p[s * kPartStride + kHeadDim]);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float ls = p[s * kPartStride + kHeadDim];
-      if (ls == -INFINITY) continue;
-      const float f = __expf(ls - M);
-      L += f;
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int nrank = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  if (nrank > 1) cluster.sync(); else __syncthreads();
+  // rank k merges heads k, k + nrank, ...: thread = dim, every partial read
+  // once through distributed shared memory, all loads independent
+  const AttnSmem* peer[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[e] += f * p[s * kPartStride + 4 * lane + e];
+  for (int rk = 0; rk < 8; ++rk) peer[rk] = rk < nrank ? cluster.map_shared_rank(&sm, rk) : &sm;
+  for (int head = rank; head < G; head += nrank) {
+    const int dim = tid;  // kAttThreads == kHeadDim
+    float mr[8], lr[8], orr[8];
+#pragma unroll
+    for (int rk = 0; rk < 8; ++rk) {
+      if (rk < nrank) {
+        mr[rk] = peer[rk]->cta_m[head];
+        lr[rk] = peer[rk]->cta_l[head];
+        orr[rk] = peer[rk]->cta_o[head][dim];
+      } else {
+        mr[rk] = -INFINITY;
+        lr[rk] = 0.f;
+        orr[rk] = 0.f;
+      }
     }
+    float M = -INFINITY;
+#pragma unroll
+    for (int rk = 0; rk < 8; ++rk) M = fmaxf(M, mr[rk]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int rk = 0; rk < 8; ++rk) {
+        const float f = mr[rk] == -INFINITY ? 0.f : exp2f(mr[rk] - M);
+        L += f * lr[rk];
+        O += f * orr[rk];
+      }
+    }
+    const int qh = kvh * G + head;
+    a.out[(static_cast<size_t>(r) * a.Hq + qh) * kHeadDim + dim] = f32_to_bf16_bits(L > 0.f ? O / L : 0.f);
+    if (a.lse && dim == 0)
+      a.lse[static_cast<size_t>(r) * a.Hq + qh] =
+          L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
-  uint16_t* o = out + static_cast<size_t>(wid) * kHeadDim + 4 * lane;
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const uint32_t lo = f32_to_bf16_bits(acc[0] * inv) | (static_cast<uint32_t>(f32_to_bf16_bits(acc[1] * inv)) << 16);
-  const uint32_t hi = f32_to_bf16_bits(acc[2] * inv) | (static_cast<uint32_t>(f32_to_bf16_bits(acc[3] * inv)) << 16);
-  *reinterpret_cast<uint2*>(o) = make_uint2(lo, hi);
-  if (lse && lane == 0) lse[wid] = L > 0.f ? M + __logf(L) : -INFINITY;
+  if (nrank > 1) cluster.sync();  // keep every rank's shared memory alive until rank 0 is done
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
-// Split count: enough CTAs to cover the GPU twice, at most one block per split.
+// Split count: enough CTAs to cover the GPU twice, at most one block per split
+// and at most 8 splits (one portable thread-block cluster per (kv head, row)).
 int attention_splits(int R, int Hkv, int topk, int* ips) {
   if (topk <= 0) { *ips = 0; return 1; }
   const long long ctas = static_cast<long long>(R) * Hkv;
   long long want = ctas > 0 ? (2 * 152 + ctas - 1) / ctas : 1;
   if (want < 1) want = 1;
+  if (want > 8) want = 8;
   if (want > topk) want = topk;
   const int per = static_cast<int>((topk + want - 1) / want);
   *ips = per;
@@ -400,21 +432,13 @@ extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, 
   if (B > 0 && (bt_stride < 1 || !block_table)) return M3S_ERR_INVALID;
   int ips = 0;
   const int nsplit = attention_splits(R, Hkv, topk, &ips);
-  if (nsplit > 1) {
-    if (ws_bytes < m3s_workspace_bytes(M3S_OP_SPARSE_ATTENTION, R, 0, bt_stride, Hq, Hkv, 0, topk, 1))
-      return M3S_ERR_WORKSPACE;
-    if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
-  }
+  (void)ws;
+  (void)ws_bytes;
   AttnArgs a{q, Hq, Hkv, Hq / Hkv, k.codes, k.scales, v.codes, v.scales, k.num_pages, block_table,
              bt_stride, row_req, row_len, topk_ids, topk, R, B,
-             sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, static_cast<float*>(ws), err};
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  attention_kernel<<<dim3(nsplit, Hkv, R), kAttThreads, 0, st>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return M3S_ERR_LAUNCH;
-  if (nsplit > 1) {
-    const int rh = R * Hq;
-    combine_kernel<<<(rh * 32 + 255) / 256, 256, 0, st>>>(static_cast<float*>(ws), nsplit, rh, out, lse);
-    if (cudaGetLastError() != cudaSuccess) return M3S_ERR_LAUNCH;
-  }
+             sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err};
+  if (launch_kernel(attention_kernel, dim3(nsplit, Hkv, R), dim3(kAttThreads), 0,
+                    static_cast<cudaStream_t>(stream), nsplit, a) != cudaSuccess)
+    return M3S_ERR_LAUNCH;
   return M3S_OK;
 }

@@ -1,7 +1,7 @@
 // Lightning-indexer scoring over paged NVFP4 index keys with block top-k.
 //
 // "[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache" (ROCm/ATOM
-// #2744): Design / Index (FP4 index keys decoded to fp16 in registers),
+// #2744): Design / Index (FP4 index keys decoded to 16-bit in registers),
 // Design / Decode score grid (a long request must not serialise the kernel)
 // and Design / Fused verify top-k (rows of one request scored together, ids
 // only). Token score = sum_h w_h * ReLU(q_h . k_t); block score = max over the
@@ -14,13 +14,13 @@
 // into equal contiguous ranges, one per CTA, so a 450K-token request is spread
 // over every SM exactly like the short ones.
 //
-// Inner loop. Each warp streams whole blocks (9216 B: 8192 B of codes + 1024 B
-// of scales) into its own double-buffered shared-memory stages with 1-D bulk
-// copies (TMA) and an mbarrier, dequantises e2m1 x E4M3 to fp16 in registers
-// (exact) and feeds mma.sync m16n8k16 with the 16 keys of an m-tile as M and
-// (row, head) pairs as N. The head dimension is walked in a permuted order so
-// that every thread's key bytes are one contiguous 16-byte chunk; the query
-// fragments use the same permutation, which leaves every dot product unchanged.
+// Inner loop (tcgen05). A warpgroup owns a block of 128 keys at a time: its
+// 128 threads each dequantise one key (e2m1 x E4M3 -> f16, exact) straight from
+// the bulk-copied (TMA) page in shared memory into tensor memory, which is the
+// A operand (M = 128 keys) of tcgen05.mma kind::f16; B is the tile's queries
+// (N = 16 heads x rows) in shared memory; the f32 scores accumulate in tensor
+// memory and come back with tcgen05.ld, one key per thread, for the
+// ReLU-weighted head sum and the block maximum.
 #include <cuda_runtime.h>
 
 #include "m3s_device.cuh"
@@ -28,11 +28,22 @@
 namespace m3s {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 2;
-constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;  // 9216
+constexpr int kStages = 3;                                      // per warpgroup
+constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;   // one block: 9216
 constexpr int kMaxTiles = 8192;
+
+// Warpgroups per CTA and the tensor-memory plan: per warpgroup 64 columns of
+// A (128 keys x 128 dims of f16) and N = 16 * QT columns of f32 scores.
+template <int QT>
+struct Cfg {
+  static constexpr int kWG = QT == 1 ? 4 : 2;
+  static constexpr int kThreads = kWG * 128;
+  static constexpr int kN = 16 * QT;
+  static constexpr int kACols = kHeadDim / 2;
+  static constexpr int kWGCols = kACols + kN;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kQBytes = kN * kHeadDim * 2;
+};
 
 struct ScoreArgs {
   const uint16_t* q_idx;
@@ -87,43 +98,71 @@ __device__ TileInfo<QT> tile_info(const ScoreArgs& a, int t, bool report) {
   return ti;
 }
 
-struct __align__(16) ScoreSmem {
-  uint8_t stage[kWarps][kStages][kStageBytes];
-  uint64_t bar[kWarps][kStages];
-};
-
-// Shared-memory layout: ScoreSmem | q fragments (8 k-steps x NT n-tiles x 32 lanes
-// x 8 B) | w (QT x 16 floats) | row lengths (QT ints) | tile prefix (ntiles+1 ints).
 template <int QT>
-__host__ __device__ constexpr int qfrag_bytes() { return 8 * (2 * QT) * 32 * 8; }
+struct __align__(128) ScoreSmem {
+  uint8_t stage[Cfg<QT>::kWG][kStages][kStageBytes];
+  uint8_t bq[Cfg<QT>::kQBytes];  // B operand: queries, f16, K-major, no swizzle
+  uint64_t sbar[Cfg<QT>::kWG][kStages];
+  uint64_t mbar[Cfg<QT>::kWG];
+  float blkmax[Cfg<QT>::kWG][4][QT];
+  float wsm[QT * 16];
+  int lensm[QT];
+  int svalid[Cfg<QT>::kWG][kStages];
+  int abort_wg[Cfg<QT>::kWG];
+  uint32_t tmem_base;
+  int qbad;
+};
 
 template <int QT>
 size_t score_smem_bytes(int ntiles) {
-  return sizeof(ScoreSmem) + qfrag_bytes<QT>() + QT * 16 * 4 + QT * 4 + (ntiles + 1) * 4 + 16;
+  return sizeof(ScoreSmem<QT>) + (ntiles + 1) * 4 + 128;
+}
+
+// B layout: core matrix (8 rows x 8 f16 = 128 B) for K-chunk kc (dims 8kc ..
+// 8kc+7) and row group rg sits at (kc * N/8 + rg) * 128 B: the K-direction
+// stride (LBO) is 16 N bytes, the row-group stride (SBO) 128 bytes.
+template <int QT>
+__device__ __forceinline__ uint32_t bq_offset(int n, int kc) {
+  return (kc * (Cfg<QT>::kN / 8) + (n >> 3)) * 128 + (n & 7) * 16;
 }
 
 template <int QT>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(const ScoreArgs a) {
-  constexpr int NT = 2 * QT;  // n8 tiles of (row, head) columns
+__global__ void __launch_bounds__(Cfg<QT>::kThreads, 1) score_kernel(const ScoreArgs a) {
+  using C = Cfg<QT>;
+  constexpr uint32_t kIdesc = idesc_f16(128, C::kN);
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  ScoreSmem& sm = *reinterpret_cast<ScoreSmem*>(smem_raw);
-  uint2* qfrag = reinterpret_cast<uint2*>(smem_raw + sizeof(ScoreSmem));
-  float* wsm = reinterpret_cast<float*>(smem_raw + sizeof(ScoreSmem) + qfrag_bytes<QT>());
-  int* lensm = reinterpret_cast<int*>(wsm + QT * 16);
-  int* pre = lensm + QT;
-  __shared__ int red[kWarps];
-  __shared__ int qbad;
+  ScoreSmem<QT>& sm = *reinterpret_cast<ScoreSmem<QT>*>(smem_raw);
+  int* pre = reinterpret_cast<int*>(smem_raw + sizeof(ScoreSmem<QT>));
+  __shared__ int red[C::kThreads / 32];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, t = lane & 3;
+  const int wg = warp >> 2, wq = warp & 3;  // warpgroup; quarter = TMEM lanes 32wq .. 32wq+31
+  const int wtid = tid & 127;               // = key index within the block
+  const bool issuer = wtid == 0;
+  const int bar_id = 1 + wg;
 
-  if (tid < kWarps * kStages) mbar_init(&sm.bar[tid / kStages][tid % kStages], 1);
-  if (tid == 0) qbad = 0;
+  // ---- prologue: barriers and tensor memory (touches no input) ----
+  if (tid < C::kWG * kStages) mbar_init(&sm.sbar[tid / kStages][tid % kStages], 1);
+  if (tid < C::kWG) {
+    mbar_init(&sm.mbar[tid], 1);
+    sm.abort_wg[tid] = 0;
+  }
+  if (tid == 0) sm.qbad = 0;
+  if (warp == 0) tmem_alloc(&sm.tmem_base, C::kTmemCols);
   mbar_fence_init();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const uint32_t a_tm = tmem + wg * C::kWGCols;  // lane 0, first A column of this warpgroup
+  const uint32_t d_tm = a_tm + C::kACols;        // lane 0, first score column
+  const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
+  pdl_trigger();
+  pdl_wait();
 
   // ---- exclusive prefix of block counts over tiles (block-wide scan) ----
   const int ntiles = a.ntiles;
-  const int per = (ntiles + kThreads - 1) / kThreads;
+  const int per = (ntiles + C::kThreads - 1) / C::kThreads;
   const int i0 = min(ntiles, tid * per), i1 = min(ntiles, i0 + per);
   int local = 0;
   for (int i = i0; i < i1; ++i) {
@@ -152,9 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const ScoreArgs a) {
   const long long N = pre[ntiles];
   const int lo = static_cast<int>(N * blockIdx.x / gridDim.x);
   const int hi = static_cast<int>(N * (blockIdx.x + 1) / gridDim.x);
-  if (lo >= hi) return;
-
-  // first tile with pre[t+1] > lo
   int tile = 0;
   {
     int l = 0, h = ntiles;  // pre[l] <= lo < pre[h]
@@ -165,10 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const ScoreArgs a) {
     tile = l;
   }
 
-  uint32_t phase_bits = 0;  // per-stage mbarrier parity of this warp
-  bool aborted = false;
-  uint32_t qa[8][NT == 2 ? 2 : 1][2];  // decode path: q fragments kept in registers
-  (void)qa;
+  uint32_t sphase = 0;    // expected parity per stage of this warpgroup
+  uint32_t mphase = 0;    // expected parity of the MMA barrier
+  uint32_t pending = 0;   // issuer: stages with a copy not yet waited for
+  bool mma_pending = false;
+  float wreg[16];
 
   int pos = lo;
   while (pos < hi) {
@@ -177,238 +214,317 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const ScoreArgs a) {
     const int seg_hi = min(hi, pre[tile + 1]) - pre[tile];
     const TileInfo<QT> ti = tile_info<QT>(a, tile, false);
 
-    // ---- stage the tile's queries (fp16, fragment order) and weights ----
+    // ---- stage the tile's queries (the B operand), weights and lengths ----
     __syncthreads();
-    for (int e = tid; e < 8 * NT * 32; e += kThreads) {
-      const int ln = e & 31, c = (e >> 5) % NT, j = (e >> 5) / NT;
-      const int col = 8 * c + (ln >> 2), tt = ln & 3;
-      const int rho = col >> 4, h = col & 15;
-      uint2 v = make_uint2(0u, 0u);
+    for (int e = tid; e < C::kN * 16; e += C::kThreads) {
+      const int n = e >> 4, kc = e & 15;
+      const int rho = n >> 4, h = n & 15;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (rho < ti.nrows && h < a.Hi) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(
-            a.q_idx + (static_cast<size_t>(ti.row0 + rho) * a.Hi + h) * kHeadDim + 32 * tt + 4 * j);
+        const uint4 raw = *reinterpret_cast<const uint4*>(
+            a.q_idx + (static_cast<size_t>(ti.row0 + rho) * a.Hi + h) * kHeadDim + 8 * kc);
         bool bad = false;
         v.x = bf16x2_to_f16x2(raw.x, bad);
         v.y = bf16x2_to_f16x2(raw.y, bad);
-        if (bad) qbad = 1;
+        v.z = bf16x2_to_f16x2(raw.z, bad);
+        v.w = bf16x2_to_f16x2(raw.w, bad);
+        if (bad) sm.qbad = 1;
       }
-      qfrag[e] = v;
+      *reinterpret_cast<uint4*>(sm.bq + bq_offset<QT>(n, kc)) = v;
     }
-    for (int e = tid; e < QT * 16; e += kThreads) {
+    for (int e = tid; e < QT * 16; e += C::kThreads) {
       const int rho = e >> 4, h = e & 15;
-      wsm[e] = (rho < ti.nrows && h < a.Hi) ? a.w[static_cast<size_t>(ti.row0 + rho) * a.Hi + h] : 0.f;
+      sm.wsm[e] = (rho < ti.nrows && h < a.Hi) ? a.w[static_cast<size_t>(ti.row0 + rho) * a.Hi + h] : 0.f;
     }
-    if (tid < QT) lensm[tid] = tid < ti.nrows ? a.row_len[ti.row0 + tid] : 0;
+    if (tid < QT) sm.lensm[tid] = tid < ti.nrows ? a.row_len[ti.row0 + tid] : 0;
+    fence_proxy_async();  // the queries are read by the tensor core (async proxy)
     __syncthreads();
-
-    float wreg[QT][4];
     int rlen[QT];
 #pragma unroll
-    for (int rho = 0; rho < QT; ++rho) {
-      wreg[rho][0] = wsm[rho * 16 + 2 * t];
-      wreg[rho][1] = wsm[rho * 16 + 2 * t + 1];
-      wreg[rho][2] = wsm[rho * 16 + 8 + 2 * t];
-      wreg[rho][3] = wsm[rho * 16 + 9 + 2 * t];
-      rlen[rho] = lensm[rho];
-    }
-    if constexpr (NT == 2) {
+    for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
+    if constexpr (QT == 1) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint2 v = qfrag[(j * NT + c) * 32 + lane];
-          qa[j][c][0] = v.x;
-          qa[j][c][1] = v.y;
-        }
+      for (int h = 0; h < 16; ++h) wreg[h] = sm.wsm[h];
     }
 
-    // ---- this warp's blocks of the segment: seg_lo + warp + k * kWarps ----
-    const int first = seg_lo + warp;
-    const int count = first < seg_hi ? (seg_hi - first + kWarps - 1) / kWarps : 0;
+    // ---- this warpgroup's blocks: seg_lo + wg + k * kWG ----
+    const int first = seg_lo + wg;
+    const int count = first < seg_hi ? (seg_hi - first + C::kWG - 1) / C::kWG : 0;
     const int32_t* bt_row = a.block_table + static_cast<size_t>(ti.req) * a.bt_stride;
-    uint32_t valid_bits = 0;
 
-    auto issue = [&](int k) {
-      const int s = k & 1;
-      const int blk = first + k * kWarps;
+    auto issue = [&](int k) {  // issuer thread only
+      const int s = k % kStages;
+      const int page = bt_row[first + k * C::kWG];
       int ok = 0;
-      if (lane == 0 && !aborted) {
-        const int page = bt_row[blk];
-        if (page < 0 || page >= a.num_pages) {
-          raise(a.err, M3S_DEVERR_PAGE);
-        } else {
-          fence_proxy_async();
-          mbar_expect_tx(&sm.bar[warp][s], kStageBytes);
-          bulk_g2s(sm.stage[warp][s], a.codes + static_cast<size_t>(page) * kPageCodeBytes,
-                   kPageCodeBytes, &sm.bar[warp][s]);
-          bulk_g2s(sm.stage[warp][s] + kPageCodeBytes,
-                   a.scales + static_cast<size_t>(page) * kPageScaleBytes, kPageScaleBytes,
-                   &sm.bar[warp][s]);
-          ok = 1;
-        }
+      if (page < 0 || page >= a.num_pages) {
+        raise(a.err, M3S_DEVERR_PAGE);
+      } else if (!sm.abort_wg[wg]) {
+        fence_proxy_async();
+        mbar_expect_tx(&sm.sbar[wg][s], kStageBytes);
+        bulk_g2s(sm.stage[wg][s], a.codes + static_cast<size_t>(page) * kPageCodeBytes,
+                 kPageCodeBytes, &sm.sbar[wg][s]);
+        bulk_g2s(sm.stage[wg][s] + kPageCodeBytes,
+                 a.scales + static_cast<size_t>(page) * kPageScaleBytes, kPageScaleBytes,
+                 &sm.sbar[wg][s]);
+        pending |= 1u << s;
+        ok = 1;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      valid_bits = (valid_bits & ~(1u << s)) | (static_cast<uint32_t>(ok) << s);
+      sm.svalid[wg][s] = ok;
     };
+    if (issuer)
+      for (int k = 0; k < count && k < kStages; ++k) issue(k);
+    named_bar_sync(bar_id, 128);
 
-    if (count > 0) issue(0);
-    if (count > 1) issue(1);
     for (int k = 0; k < count; ++k) {
-      const int s = k & 1;
-      const int blk = first + k * kWarps;
-      bool have = (valid_bits >> s) & 1u;
-      if (have) {
-        const bool done = mbar_wait(&sm.bar[warp][s], (phase_bits >> s) & 1u);
-        phase_bits ^= 1u << s;
-        if (!done) {
-          if (lane == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
-          aborted = true;
-          have = false;
-          // give the copies still in flight one more bounded wait before leaving
-          mbar_wait(&sm.bar[warp][s], (phase_bits >> s) & 1u ^ 1u);
-          if (k + 1 < count && ((valid_bits >> (s ^ 1)) & 1u))
-            mbar_wait(&sm.bar[warp][s ^ 1], (phase_bits >> (s ^ 1)) & 1u);
-          valid_bits = 0;
+      const int s = k % kStages;
+      const int blk = first + k * C::kWG;
+      const bool issued = sm.svalid[wg][s] != 0;
+      const bool valid = issued && !sm.abort_wg[wg];
+      if (valid) {
+        if (!mbar_wait(&sm.sbar[wg][s], (sphase >> s) & 1u)) {
+          sm.abort_wg[wg] = 1;
+          raise(a.err, M3S_DEVERR_TIMEOUT);
+        } else if (issuer) {
+          pending &= ~(1u << s);
+        }
+        // dequantise key wtid into A (TMEM lane = key, column i = dims 2i, 2i+1)
+        const uint8_t* cs = sm.stage[wg][s];
+        const uint8_t* ss = cs + kPageCodeBytes;
+        const uint4* kp = reinterpret_cast<const uint4*>(cs + wtid * kCodeBytes);
+        const uint2 sc = *reinterpret_cast<const uint2*>(ss + wtid * kScaleBytes);
+        const uint32_t s01 = e4m3x2_to_f16x2(sc.x & 0xFFFFu), s23 = e4m3x2_to_f16x2(sc.x >> 16);
+        const uint32_t s45 = e4m3x2_to_f16x2(sc.y & 0xFFFFu), s67 = e4m3x2_to_f16x2(sc.y >> 16);
+        const uint32_t spair[4] = {s01, s23, s45, s67};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {  // chunk c = dims 32c .. 32c+31 = scale groups 2c, 2c+1
+          const uint4 wv = kp[c];
+          const uint32_t g0 = bcast_lo(spair[c]), g1 = bcast_hi(spair[c]);
+          uint32_t v[16];
+          e2m1x8_to_f16x2(wv.x, v[0], v[1], v[2], v[3]);
+          e2m1x8_to_f16x2(wv.y, v[4], v[5], v[6], v[7]);
+          e2m1x8_to_f16x2(wv.z, v[8], v[9], v[10], v[11]);
+          e2m1x8_to_f16x2(wv.w, v[12], v[13], v[14], v[15]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = hmul2(v[i], g0);
+#pragma unroll
+          for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], g1);
+          tmem_st16(lane_base + a_tm + 16 * c, v);
+        }
+        tmem_wait_st();
+      }
+      if (issued) sphase ^= 1u << s;
+      tc_fence_before();
+      named_bar_sync(bar_id, 128);
+      const bool go = valid && !sm.abort_wg[wg];
+      if (issuer) {
+        if (k + kStages < count) issue(k + kStages);  // stage s has been read by all
+        if (go) {
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint64_t bdesc = smem_desc_noswizzle(sm.bq + ks * 32 * C::kN, 16 * C::kN, 128);
+            tc_mma_ts(d_tm, a_tm + 8 * ks, bdesc, kIdesc, ks > 0 ? 1u : 0u);
+          }
+          tc_commit(&sm.mbar[wg]);
+          mma_pending = true;
         }
       }
-      float best[QT];
+      if (go) {
+        if (!mbar_wait(&sm.mbar[wg], mphase & 1u)) {
+          sm.abort_wg[wg] = 1;
+          raise(a.err, M3S_DEVERR_TIMEOUT);
+        } else if (issuer) {
+          mma_pending = false;
+        }
+        mphase ^= 1u;
+        tc_fence_after();
+        const int tok = blk * kPage + wtid;
 #pragma unroll
-      for (int rho = 0; rho < QT; ++rho) best[rho] = -INFINITY;
-
-      if (have) {
-        const uint8_t* cs = sm.stage[warp][s];
-        const uint8_t* ss = cs + kPageCodeBytes;
-#pragma unroll 1
-        for (int mt = 0; mt < 8; ++mt) {
-          const int key0 = mt * 16 + g;
-          const uint4 ca = *reinterpret_cast<const uint4*>(cs + key0 * kCodeBytes + 16 * t);
-          const uint4 cb = *reinterpret_cast<const uint4*>(cs + (key0 + 8) * kCodeBytes + 16 * t);
-          const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + key0 * kScaleBytes + 2 * t));
-          const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + (key0 + 8) * kScaleBytes + 2 * t));
-          const uint32_t sa0 = bcast_lo(sa), sa1 = bcast_hi(sa);
-          const uint32_t sb0 = bcast_lo(sb), sb1 = bcast_hi(sb);
-          const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
-          const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
-          float acc[NT][4];
+        for (int rho = 0; rho < QT; ++rho) {
+          float d[16];
+          tmem_ld16(lane_base + d_tm + 16 * rho, d);
+          tmem_wait_ld();
+          float sc = 0.f;
+          if constexpr (QT == 1) {
 #pragma unroll
-          for (int c = 0; c < NT; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+            for (int h = 0; h < 16; ++h) sc = fmaf(wreg[h], fmaxf(d[h], 0.f), sc);
+          } else {
+            const float4* w4 = reinterpret_cast<const float4*>(sm.wsm + 16 * rho);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            // bytes 2j, 2j+1 of the thread's chunk = dims 32t+4j .. 32t+4j+3,
-            // scale group 2t + (j >= 4)
-            const uint32_t xa = wa[j >> 1] >> (16 * (j & 1));
-            const uint32_t xb = wb[j >> 1] >> (16 * (j & 1));
-            const uint32_t scA = j < 4 ? sa0 : sa1, scB = j < 4 ? sb0 : sb1;
-            const uint32_t a0 = hmul2(e2m1x2_to_f16x2(xa & 0xFFu), scA);
-            const uint32_t a2 = hmul2(e2m1x2_to_f16x2((xa >> 8) & 0xFFu), scA);
-            const uint32_t a1 = hmul2(e2m1x2_to_f16x2(xb & 0xFFu), scB);
-            const uint32_t a3 = hmul2(e2m1x2_to_f16x2((xb >> 8) & 0xFFu), scB);
-#pragma unroll
-            for (int c = 0; c < NT; ++c) {
-              uint32_t b0, b1;
-              if constexpr (NT == 2) {
-                b0 = qa[j][c][0];
-                b1 = qa[j][c][1];
-              } else {
-                const uint2 v = qfrag[(j * NT + c) * 32 + lane];
-                b0 = v.x;
-                b1 = v.y;
-              }
-              mma16816(acc[c], a0, a1, a2, a3, b0, b1);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const float4 wv = w4[q4];
+              sc = fmaf(wv.x, fmaxf(d[4 * q4 + 0], 0.f), sc);
+              sc = fmaf(wv.y, fmaxf(d[4 * q4 + 1], 0.f), sc);
+              sc = fmaf(wv.z, fmaxf(d[4 * q4 + 2], 0.f), sc);
+              sc = fmaf(wv.w, fmaxf(d[4 * q4 + 3], 0.f), sc);
             }
           }
-          // token scores of keys key0 and key0 + 8 for each row of the tile
-          const int tok0 = blk * kPage + key0;
+          float m = tok < rlen[rho] ? sc : -INFINITY;
 #pragma unroll
-          for (int rho = 0; rho < QT; ++rho) {
-            const float* w4 = wreg[rho];
-            float p0 = w4[0] * fmaxf(acc[2 * rho][0], 0.f) + w4[1] * fmaxf(acc[2 * rho][1], 0.f) +
-                       w4[2] * fmaxf(acc[2 * rho + 1][0], 0.f) + w4[3] * fmaxf(acc[2 * rho + 1][1], 0.f);
-            float p1 = w4[0] * fmaxf(acc[2 * rho][2], 0.f) + w4[1] * fmaxf(acc[2 * rho][3], 0.f) +
-                       w4[2] * fmaxf(acc[2 * rho + 1][2], 0.f) + w4[3] * fmaxf(acc[2 * rho + 1][3], 0.f);
-            p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-            p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-            p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
-            p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
-            if (tok0 < rlen[rho]) best[rho] = fmaxf(best[rho], p0);
-            if (tok0 + 8 < rlen[rho]) best[rho] = fmaxf(best[rho], p1);
-          }
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) sm.blkmax[wg][wq][rho] = m;
         }
       }
+      tc_fence_before();
+      named_bar_sync(bar_id, 128);
+      if (wtid < QT) {
+        const int rho = wtid;
+        if (rho < ti.nrows && blk * kPage < rlen[rho]) {
+          float m = -INFINITY;
+          if (go) {
 #pragma unroll
-      for (int rho = 0; rho < QT; ++rho) {
-        float m = best[rho];
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        if (lane == 0 && rho < ti.nrows && blk * kPage < rlen[rho])
+            for (int q = 0; q < 4; ++q) m = fmaxf(m, sm.blkmax[wg][q][rho]);
+          }
           a.bscores[static_cast<size_t>(ti.row0 + rho) * a.bs_stride + blk] = m;
+        }
       }
-      __syncwarp();
-      if (k + 2 < count) issue(k + 2);
     }
     pos = pre[tile] + seg_hi;
     ++tile;
   }
+
+  // ---- leave: drain anything still in flight after a timeout, free TMEM ----
+  if (issuer) {
+    for (int s = 0; s < kStages; ++s)
+      if (pending & (1u << s)) mbar_wait(&sm.sbar[wg][s], (sphase >> s) & 1u);
+    if (mma_pending) mbar_wait(&sm.mbar[wg], mphase & 1u);
+  }
+  tc_fence_before();
   __syncthreads();
-  if (tid == 0 && qbad) raise(a.err, M3S_DEVERR_QRANGE);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (tid == 0 && sm.qbad) raise(a.err, M3S_DEVERR_QRANGE);
 }
 
-// ---- top-k over block scores: one CTA per row ----
-// Round i picks the largest key below the previous pick (keys are distinct:
-// the block id sits in the low half), so nothing has to be removed.
-constexpr int kTopkThreads = 256;
+// ---- top-k over block scores: one CTA per row, exact radix select ----
+// Keys are 64-bit (ordered score bits, then the complemented block id), all
+// distinct. The leading bytes every key shares are skipped; then one byte per
+// pass from the top: a histogram of the byte over the keys that still match
+// the chosen prefix locates the bin holding the k-th largest key; keys in
+// higher bins are in, lower bins out. The loop stops as soon as the bin's keys
+// are exactly the ones still needed (at the latest on the last byte).
+constexpr int kTopkThreads = 1024;
+
+__device__ __forceinline__ unsigned long long topk_key_at(const float* row, const unsigned long long* keys,
+                                                        bool in_smem, int i) {
+  return in_smem ? keys[i] : topk_key(row[i], i);
+}
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float* __restrict__ bscores, int bs_stride, const int32_t* __restrict__ row_req,
     const int32_t* __restrict__ row_len, int B, int bt_stride, int topk, int smem_keys,
     int32_t* __restrict__ ids) {
   extern __shared__ unsigned long long keys[];
-  __shared__ unsigned long long wbest[kTopkThreads / 32];
+  __shared__ unsigned int hist[256];
+  __shared__ unsigned long long wmax[kTopkThreads / 32], wmin[kTopkThreads / 32];
+  __shared__ unsigned long long sh_prefix, sh_mask;
+  __shared__ int sh_krem, sh_done, sh_shift, nsel;
   __shared__ int sel[M3S_MAX_TOPK];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int len = row_len[r];
   const int req = row_req ? row_req[r] : 0;
   const bool ok = len > 0 && req >= 0 && req < B && len <= bt_stride * kPage;
   const int nb = ok ? (len + kPage - 1) / kPage : 0;
+  const int cnt = min(topk, nb);
+  int32_t* out = ids + static_cast<size_t>(r) * topk;
+  for (int i = cnt + tid; i < topk; i += kTopkThreads) out[i] = -1;
+  if (cnt == 0) return;
+  if (cnt == nb) {  // every block is selected: ids 0 .. nb-1
+    for (int i = tid; i < nb; i += kTopkThreads) out[i] = i;
+    return;
+  }
   const float* row = bscores + static_cast<size_t>(r) * bs_stride;
   const bool in_smem = nb <= smem_keys;
-  if (in_smem)
-    for (int i = tid; i < nb; i += kTopkThreads) keys[i] = topk_key(row[i], i);
-  __syncthreads();
-  const int cnt = min(topk, nb);
-  unsigned long long prev = ~0ull;
-  for (int k = 0; k < cnt; ++k) {
-    unsigned long long best = 0;
-    for (int i = tid; i < nb; i += kTopkThreads) {
-      const unsigned long long key = in_smem ? keys[i] : topk_key(row[i], i);
-      if (key < prev && key > best) best = key;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long v = __shfl_xor_sync(0xffffffffu, best, o);
-      best = v > best ? v : best;
-    }
-    if (lane == 0) wbest[warp] = best;
-    __syncthreads();
-    best = wbest[0];
-#pragma unroll
-    for (int wv = 1; wv < kTopkThreads / 32; ++wv) best = wbest[wv] > best ? wbest[wv] : best;
-    if (tid == 0) sel[k] = key_id(best);
-    prev = best;
-    __syncthreads();
+  unsigned long long kmax = 0, kmin = ~0ull;
+  for (int i = tid; i < nb; i += kTopkThreads) {
+    const unsigned long long key = topk_key(row[i], i);
+    if (in_smem) keys[i] = key;
+    kmax = key > kmax ? key : kmax;
+    kmin = key < kmin ? key : kmin;
   }
-  // write ascending ids, then -1 padding
-  if (tid < topk) {
-    int out = -1;
-    if (tid < cnt) {
-      const int mine = sel[tid];
-      int rank = 0;
-      for (int j = 0; j < cnt; ++j) rank += sel[j] < mine;
-      ids[static_cast<size_t>(r) * topk + rank] = mine;
-    } else {
-      ids[static_cast<size_t>(r) * topk + tid] = out;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long x = __shfl_xor_sync(0xffffffffu, kmax, o);
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, kmin, o);
+    kmax = x > kmax ? x : kmax;
+    kmin = y < kmin ? y : kmin;
+  }
+  if (lane == 0) {
+    wmax[warp] = kmax;
+    wmin[warp] = kmin;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 0; w < kTopkThreads / 32; ++w) {
+      kmax = wmax[w] > kmax ? wmax[w] : kmax;
+      kmin = wmin[w] < kmin ? wmin[w] : kmin;
     }
+    const int common = (__clzll(static_cast<long long>(kmax ^ kmin)) / 8) * 8;  // shared leading bits
+    const unsigned long long mask = common ? ~0ull << (64 - common) : 0ull;
+    sh_prefix = kmax & mask;
+    sh_mask = mask;
+    sh_shift = 56 - common;
+    sh_krem = cnt;
+    sh_done = 0;
+    nsel = 0;
+  }
+  __syncthreads();
+
+  for (int shift = sh_shift; shift >= 0; shift -= 8) {
+    for (int b = tid; b < 256; b += kTopkThreads) hist[b] = 0;
+    const unsigned long long prefix = sh_prefix, mask = sh_mask;
+    const int krem = sh_krem;
+    __syncthreads();
+    for (int i = tid; i < nb; i += kTopkThreads) {
+      const unsigned long long key = topk_key_at(row, keys, in_smem, i);
+      if ((key & mask) == prefix) atomicAdd(&hist[static_cast<unsigned>(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      int loc = 0;
+#pragma unroll
+      for (int d = 0; d < 8; ++d) loc += hist[8 * tid + d];
+      int suf = loc;  // sum over lanes >= this one
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_down_sync(0xffffffffu, suf, o);
+        if (tid + o < 32) suf += u;
+      }
+      int above = suf - loc;
+#pragma unroll
+      for (int d = 7; d >= 0; --d) {
+        const int bin = 8 * tid + d;
+        const int h = hist[bin];
+        if (above < krem && above + h >= krem) {
+          sh_prefix = prefix | (static_cast<unsigned long long>(bin) << shift);
+          sh_mask = mask | (255ull << shift);
+          sh_krem = krem - above;
+          sh_done = (h == krem - above);
+        }
+        above += h;
+      }
+    }
+    __syncthreads();
+    if (sh_done) break;
+  }
+  const unsigned long long prefix = sh_prefix, mask = sh_mask;
+  for (int i = tid; i < nb; i += kTopkThreads) {
+    const unsigned long long key = topk_key_at(row, keys, in_smem, i);
+    if ((key & mask) >= prefix) {
+      const int slot = atomicAdd(&nsel, 1);
+      if (slot < M3S_MAX_TOPK) sel[slot] = i;
+    }
+  }
+  __syncthreads();
+  if (tid < cnt) {
+    const int mine = sel[tid];
+    int rank = 0;
+    for (int j = 0; j < cnt; ++j) rank += sel[j] < mine;
+    out[rank] = mine;
   }
 }
 
@@ -434,8 +550,10 @@ int launch_score(const ScoreArgs& a, cudaStream_t st) {
   if (cudaFuncSetAttribute(score_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
-  score_kernel<QT><<<sm_count(), kThreads, smem, st>>>(a);
-  return cudaGetLastError() == cudaSuccess ? M3S_OK : M3S_ERR_LAUNCH;
+  return launch_kernel(score_kernel<QT>, dim3(sm_count()), dim3(Cfg<QT>::kThreads), smem, st, 0, a) ==
+                 cudaSuccess
+             ? M3S_OK
+             : M3S_ERR_LAUNCH;
 }
 
 int launch_topk(const float* bscores, int bs_stride, const int32_t* row_req, const int32_t* row_len,
@@ -445,9 +563,10 @@ int launch_topk(const float* bscores, int bs_stride, const int32_t* row_req, con
   if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
-  topk_kernel<<<R, kTopkThreads, smem, st>>>(bscores, bs_stride, row_req, row_len, B, bt_stride,
-                                             topk, keys, ids);
-  return cudaGetLastError() == cudaSuccess ? M3S_OK : M3S_ERR_LAUNCH;
+  return launch_kernel(topk_kernel, dim3(R), dim3(kTopkThreads), smem, st, 0, bscores, bs_stride,
+                       row_req, row_len, B, bt_stride, topk, keys, ids) == cudaSuccess
+             ? M3S_OK
+             : M3S_ERR_LAUNCH;
 }
 
 int check_common(const uint16_t* q_idx, const float* w, int Hi, const m3s_nvfp4_plane& idx_k,

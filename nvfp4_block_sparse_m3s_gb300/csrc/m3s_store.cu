@@ -56,12 +56,34 @@ __device__ __forceinline__ uint32_t group_amax_bits(const uint32_t (&x)[8]) {
 // reads 64 B, writes 16 B of codes with one 128-bit store, and the four
 // threads of a (row, head) gather their scale pairs so one of them writes the
 // 8 scale bytes with one 64-bit store.
-__global__ void __launch_bounds__(256) nvfp4_store_kernel(
-    const uint16_t* __restrict__ src, int64_t stride, int64_t total_threads, int32_t H,
-    const int64_t* __restrict__ slots, uint8_t* __restrict__ codes,
-    uint8_t* __restrict__ scales, int64_t capacity, int32_t* err) {
+struct StoreJob {
+  const uint16_t* src;
+  int64_t stride;
+  int64_t total_threads;  // T * H * 4
+  int32_t H;
+  uint8_t* codes;
+  uint8_t* scales;
+  int64_t capacity;       // num_pages * 128
+};
+
+struct StoreBatch {
+  StoreJob job[M3S_MAX_STORE_JOBS];
+};
+
+__global__ void __launch_bounds__(256) nvfp4_store_kernel(const StoreBatch batch,
+                                                         const int64_t* __restrict__ slots,
+                                                         int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
+  const StoreJob& jb = batch.job[blockIdx.y];
+  const uint16_t* __restrict__ src = jb.src;
+  const int64_t stride = jb.stride;
+  const int32_t H = jb.H;
+  uint8_t* __restrict__ codes = jb.codes;
+  uint8_t* __restrict__ scales = jb.scales;
+  const int64_t capacity = jb.capacity;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= total_threads) return;
+  if (idx >= jb.total_threads) return;
   const int part = static_cast<int>(idx & 3);
   const int64_t rh = idx >> 2;
   const int h = static_cast<int>(rh % H);
@@ -111,6 +133,8 @@ __global__ void __launch_bounds__(256) nvfp4_store_kernel(
 __global__ void decode_rows_kernel(const int32_t* __restrict__ cu_q,
                                    const int32_t* __restrict__ seq_len, int32_t B, int32_t R,
                                    int32_t* __restrict__ row_req, int32_t* __restrict__ row_len) {
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
   int32_t req = -1, len = 0;
@@ -133,22 +157,60 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 }  // namespace
 }  // namespace m3s
 
+namespace m3s {
+namespace {
+int check_job(const uint16_t* src, int64_t stride, int32_t H, const m3s_nvfp4_plane& dst) {
+  if (H <= 0 || dst.num_pages < 0 || dst.num_heads != H) return M3S_ERR_INVALID;
+  if (!src || !dst.codes || !dst.scales) return M3S_ERR_INVALID;
+  if (!aligned16(src) || !aligned16(dst.codes) || !aligned16(dst.scales)) return M3S_ERR_INVALID;
+  if (stride < static_cast<int64_t>(H) * kHeadDim || (stride & 7)) return M3S_ERR_INVALID;
+  return M3S_OK;
+}
+
+int launch_store(const m3s_store_job* jobs, int32_t njobs, int32_t T, const int64_t* slots,
+                 int32_t* err, cudaStream_t st) {
+  StoreBatch b{};
+  int64_t most = 0;
+  for (int i = 0; i < njobs; ++i) {
+    const m3s_store_job& j = jobs[i];
+    b.job[i] = StoreJob{j.src, j.src_row_stride, static_cast<int64_t>(T) * j.H * 4, j.H,
+                        j.dst.codes, j.dst.scales, static_cast<int64_t>(j.dst.num_pages) * kPage};
+    most = b.job[i].total_threads > most ? b.job[i].total_threads : most;
+  }
+  const int64_t blocks = (most + 255) / 256;
+  if (blocks > 0x7FFFFFFF) return M3S_ERR_UNSUPPORTED;
+  return launch_kernel(nvfp4_store_kernel, dim3(static_cast<unsigned>(blocks), njobs), dim3(256), 0,
+                       st, 0, b, slots, err) == cudaSuccess
+             ? M3S_OK
+             : M3S_ERR_LAUNCH;
+}
+}  // namespace
+}  // namespace m3s
+
 extern "C" int m3s_nvfp4_store(const uint16_t* src, int64_t src_row_stride, int32_t T, int32_t H,
                                const int64_t* slot_mapping, m3s_nvfp4_plane dst, int32_t* err,
                                void* stream) {
   using namespace m3s;
   if (T < 0 || H <= 0 || dst.num_pages < 0 || dst.num_heads != H) return M3S_ERR_INVALID;
   if (T == 0) return M3S_OK;
-  if (!src || !slot_mapping || !dst.codes || !dst.scales) return M3S_ERR_INVALID;
-  if (!aligned16(src) || !aligned16(dst.codes) || !aligned16(dst.scales)) return M3S_ERR_INVALID;
-  if (src_row_stride < static_cast<int64_t>(H) * kHeadDim || (src_row_stride & 7)) return M3S_ERR_INVALID;
-  const int64_t total = static_cast<int64_t>(T) * H * 4;
-  const int64_t blocks = (total + 255) / 256;
-  if (blocks > 0x7FFFFFFF) return M3S_ERR_UNSUPPORTED;
-  nvfp4_store_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      src, src_row_stride, total, H, slot_mapping, dst.codes, dst.scales,
-      static_cast<int64_t>(dst.num_pages) * kPage, err);
-  return cudaGetLastError() == cudaSuccess ? M3S_OK : M3S_ERR_LAUNCH;
+  if (!slot_mapping) return M3S_ERR_INVALID;
+  const int rc = check_job(src, src_row_stride, H, dst);
+  if (rc != M3S_OK) return rc;
+  const m3s_store_job job{src, src_row_stride, H, dst};
+  return launch_store(&job, 1, T, slot_mapping, err, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int m3s_nvfp4_store_batch(const m3s_store_job* jobs, int32_t njobs, int32_t T,
+                                     const int64_t* slot_mapping, int32_t* err, void* stream) {
+  using namespace m3s;
+  if (T < 0 || njobs < 0 || njobs > M3S_MAX_STORE_JOBS || (njobs > 0 && !jobs)) return M3S_ERR_INVALID;
+  if (T == 0 || njobs == 0) return M3S_OK;
+  if (!slot_mapping) return M3S_ERR_INVALID;
+  for (int i = 0; i < njobs; ++i) {
+    const int rc = check_job(jobs[i].src, jobs[i].src_row_stride, jobs[i].H, jobs[i].dst);
+    if (rc != M3S_OK) return rc;
+  }
+  return launch_store(jobs, njobs, T, slot_mapping, err, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int32_t R,
@@ -156,7 +218,9 @@ extern "C" int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int3
   if (B < 0 || R < 0) return M3S_ERR_INVALID;
   if (R == 0) return M3S_OK;
   if (!cu_q || !row_req || !row_len || (B > 0 && !seq_len)) return M3S_ERR_INVALID;
-  m3s::decode_rows_kernel<<<(R + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      cu_q, seq_len, B, R, row_req, row_len);
-  return cudaGetLastError() == cudaSuccess ? M3S_OK : M3S_ERR_LAUNCH;
+  return m3s::launch_kernel(m3s::decode_rows_kernel, dim3((R + 255) / 256), dim3(256), 0,
+                            static_cast<cudaStream_t>(stream), 0, cu_q, seq_len, B, R, row_req,
+                            row_len) == cudaSuccess
+             ? M3S_OK
+             : M3S_ERR_LAUNCH;
 }

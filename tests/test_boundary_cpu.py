@@ -44,10 +44,8 @@ def test_workspace_sizes(lib):
     from nvfp4_block_sparse_m3s_gb300 import binding as M
     assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600) == 8 * 3600 * 4
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 0, 8, 3600) == 0
-    # decode batch: one block per split -> 16 splits of (o[128], lse) per (row, head)
-    assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == \
-        8 * 16 * 16 * 129 * 4
-    # many rows: no split, no workspace
+    # attention merges its split-K partials on chip (thread-block cluster): no workspace
+    assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == 0
     assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8192, 1, 2112, 16, 1, 16, 16) == 0
     assert M.m3s_workspace_bytes(99, 8, 8, 8) == 0
 

@@ -252,3 +252,55 @@ def test_pad_rows_and_empty_inputs(lib):
     # zero-sized calls are no-ops
     M.m3s_nvfp4_store(torch.zeros((0, 1, 128), dtype=torch.bfloat16, device="cuda"),
                       torch.zeros(0, dtype=torch.int64, device="cuda"), dev.ic, dev.is_)
+
+
+def test_store_batch_equals_single_stores(lib):
+    T, P = 300, 4
+    srcs = [W.bf16_tensor(9, n, (T, h, 128), 3, 10.0) for n, h in (("bk", 2), ("bv", 2), ("bi", 1))]
+    slots = W.permutation(9, "bslots", P * 128)[:T].astype(np.int64)
+    slots[7] = -1
+    sl = i64(slots)
+    single, batch = [], []
+    for src in srcs:
+        c1, s1 = M.new_plane(P, src.shape[1])
+        M.m3s_nvfp4_store(bf16_dev(src), sl, c1, s1)
+        single.append((c1, s1))
+        batch.append((bf16_dev(src),) + M.new_plane(P, src.shape[1]))
+    M.m3s_nvfp4_store_batch(batch, sl)
+    torch.cuda.synchronize()
+    for (c1, s1), (_, c2, s2) in zip(single, batch):
+        assert torch.equal(c1, c2) and torch.equal(s1, s2)
+
+
+def test_block_topk_direct_against_oracle(lib):
+    """m3s_block_topk on given fp32 block scores == the oracle's selection exactly:
+    ties (lower id wins), +-0, negatives, rows narrower than k, and rows wider
+    than the shared-memory key cache."""
+    rng = np.random.default_rng(11)
+    widths = [1, 5, 16, 17, 300, 3600, 20000]
+    bt_stride = max(widths)
+    R = len(widths) * 4
+    scores = np.zeros((R, bt_stride), dtype=np.float32)
+    lens = np.zeros(R, dtype=np.int32)
+    for i, nb in enumerate(widths):
+        for v in range(4):
+            r = 4 * i + v
+            lens[r] = nb * 128 - int(rng.integers(0, 128))
+            x = rng.standard_normal(nb).astype(np.float32)
+            if v == 1:
+                x = np.round(x * 2).astype(np.float32)          # many exact ties
+            if v == 2:
+                x[:] = 0.0
+                x[rng.integers(0, nb, size=max(1, nb // 3))] = -0.0
+            if v == 3:
+                x = -np.abs(x)                                  # all negative
+            scores[r, :nb] = x
+            scores[r, nb:] = np.nan                             # never read
+    for topk in (1, 8, 16, 64):
+        ids = M.m3s_block_topk(torch.from_numpy(scores).cuda(), None, i32(lens), 1, bt_stride, topk)
+        torch.cuda.synchronize()
+        got = ids.cpu().numpy()
+        for r in range(R):
+            nb = (int(lens[r]) + 127) // 128
+            exp = O.topk_ids(scores[r, :nb].astype(np.float64), topk)
+            assert np.array_equal(got[r], exp), (topk, r, got[r], exp)
