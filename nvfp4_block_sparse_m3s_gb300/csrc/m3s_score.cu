@@ -14,108 +14,72 @@
 // into equal contiguous ranges, one per CTA, so a 450K-token request is spread
 // over every SM exactly like the short ones.
 //
-// Inner loop (tcgen05). A warpgroup owns a block of 128 keys at a time: its
-// 128 threads each dequantise one key (e2m1 x E4M3 -> f16, exact) straight from
-// the bulk-copied (TMA) page in shared memory into tensor memory, which is the
-// A operand (M = 128 keys) of tcgen05.mma kind::f16; B is the tile's queries
-// (N = 16 heads x rows) in shared memory; the f32 scores accumulate in tensor
-// memory and come back with tcgen05.ld, one key per thread, for the
-// ReLU-weighted head sum and the block maximum.
-#include <cuda_runtime.h>
+// Inner loop (tcgen05, warp-specialised). A producer warp streams whole
+// blocks (8 KB of codes through a 2-D tensor map with 64-byte swizzle, so the
+// per-key reads below are free of bank conflicts, plus 1 KB of scales) into a
+// ring of shared-memory stages. Dequantising warpgroups turn a block into the
+// A operand: each of their 128 threads decodes one key (e2m1 x E4M3 -> f16,
+// exact) straight into its lane of a tensor-memory slot (M = 128 keys). One
+// thread issues tcgen05.mma kind::f16 against the tile's queries in shared
+// memory (B: N = 16 heads x rows) into a ring of tensor-memory accumulators,
+// and an epilogue warpgroup reads the f32 scores back one key per thread for
+// the ReLU-weighted head sum and the block maximum. mbarriers hand stages,
+// A slots and accumulators from one role to the next, so no role waits on a
+// round trip of another.
+#include <cstring>
 
-#include "m3s_device.cuh"
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "m3s_score_common.cuh"
 
 namespace m3s {
 namespace {
 
-constexpr int kStages = 3;                                      // per warpgroup
-constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;   // one block: 9216
-constexpr int kMaxTiles = 8192;
+constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;  // one block: 9216 = 9 x 1024
 
-// Warpgroups per CTA and the tensor-memory plan: per warpgroup 64 columns of
-// A (128 keys x 128 dims of f16) and N = 16 * QT columns of f32 scores.
+// Roles and resources. Warp 0: producer (bulk copies); warp 1: MMA issuer;
+// warps 2-5: epilogue warpgroup; warps 6 ...: kNDQ dequantising warpgroups.
+// Tensor memory: kNA A slots of 64 columns (128 keys x 128 f16) and kND
+// accumulator slots of N = 16 * QT f32 columns.
 template <int QT>
 struct Cfg {
-  static constexpr int kWG = QT == 1 ? 4 : 2;
-  static constexpr int kThreads = kWG * 128;
   static constexpr int kN = 16 * QT;
+  static constexpr int kNDQ = QT == 1 ? 3 : 2;
+  static constexpr int kWarps = 2 + 4 + 4 * kNDQ;
+  static constexpr int kThreads = 32 * kWarps;
+  // Stages and A slots are multiples of kNDQ: block g goes to warpgroup g % kNDQ,
+  // stage g % kNS and slot g % kNA, so each stage and each slot is only ever used
+  // by one warpgroup, in order, and a parity wait can never see a phase two back.
+  static constexpr int kNS = (QT == 1 ? 5 : 4) * kNDQ;
+  static constexpr int kNA = 2 * kNDQ;
+  static constexpr int kND = QT == 1 ? 4 : 2;
   static constexpr int kACols = kHeadDim / 2;
-  static constexpr int kWGCols = kACols + kN;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kQBytes = kN * kHeadDim * 2;
-};
-
-struct ScoreArgs {
-  const uint16_t* q_idx;
-  const float* w;
-  int Hi;
-  const uint8_t* codes;
-  const uint8_t* scales;
-  int num_pages;
-  const int32_t* block_table;
-  int bt_stride;
-  const int32_t* row_req;  // index path (QT == 1)
-  const int32_t* cu_q;     // verify path (QT == 8)
-  const int32_t* row_len;
-  int R, B, ntiles, cpr;   // cpr: row chunks per request (verify path)
-  float* bscores;
-  int bs_stride;
-  int32_t* err;
+  static_assert(kNA * kACols + kND * kN <= 512, "tensor memory plan exceeds 512 columns");
+  static_assert(kNS % kNDQ == 0 && kNA % kNDQ == 0, "stages and slots must partition by warpgroup");
 };
 
 template <int QT>
-struct TileInfo {
-  int row0, nrows, req, len;
-};
-
-// Rows, request and key count of tile t. Invalid tiles (pad rows, bad request,
-// a length beyond the block table) come back with nrows == 0.
-template <int QT>
-__device__ TileInfo<QT> tile_info(const ScoreArgs& a, int t, bool report) {
-  TileInfo<QT> ti{0, 0, -1, 0};
-  if (QT == 1) {
-    ti.row0 = t;
-    ti.req = a.row_req[t];
-    ti.len = a.row_len[t];
-    if (ti.req < 0 || ti.len <= 0) { ti.len = 0; return ti; }
-    ti.nrows = 1;
-  } else {
-    const int b = t / a.cpr, j = t % a.cpr;
-    const int c0 = a.cu_q[b], qb = a.cu_q[b + 1] - c0;
-    const int n = min(QT, qb - j * QT);
-    if (n <= 0) return ti;
-    ti.row0 = c0 + j * QT;
-    ti.req = b;
-    ti.nrows = n;
-    for (int i = 0; i < n; ++i) ti.len = max(ti.len, a.row_len[ti.row0 + i]);
-    if (ti.len <= 0) { ti.nrows = 0; ti.len = 0; return ti; }
-  }
-  if (ti.req >= a.B || ti.len > a.bt_stride * kPage) {
-    if (report) raise(a.err, M3S_DEVERR_ROW);
-    ti.nrows = 0;
-    ti.len = 0;
-  }
-  return ti;
-}
-
-template <int QT>
-struct __align__(128) ScoreSmem {
-  uint8_t stage[Cfg<QT>::kWG][kStages][kStageBytes];
-  uint8_t bq[Cfg<QT>::kQBytes];  // B operand: queries, f16, K-major, no swizzle
-  uint64_t sbar[Cfg<QT>::kWG][kStages];
-  uint64_t mbar[Cfg<QT>::kWG];
-  float blkmax[Cfg<QT>::kWG][4][QT];
+struct __align__(1024) ScoreSmem {
+  uint8_t stage[Cfg<QT>::kNS][kStageBytes];  // codes (swizzled, 1024-aligned) then scales
+  uint8_t bq[Cfg<QT>::kQBytes];              // B operand: queries, f16, K-major, no swizzle
+  uint64_t full[Cfg<QT>::kNS], empty[Cfg<QT>::kNS];
+  uint64_t afull[Cfg<QT>::kNA], aempty[Cfg<QT>::kNA];
+  uint64_t dfull[Cfg<QT>::kND], dempty[Cfg<QT>::kND];
+  float blkmax[Cfg<QT>::kND][4][QT];
   float wsm[QT * 16];
   int lensm[QT];
-  int svalid[Cfg<QT>::kWG][kStages];
-  int abort_wg[Cfg<QT>::kWG];
   uint32_t tmem_base;
   int qbad;
+  int abort;
 };
 
 template <int QT>
 size_t score_smem_bytes(int ntiles) {
-  return sizeof(ScoreSmem<QT>) + (ntiles + 1) * 4 + 128;
+  return sizeof(ScoreSmem<QT>) + (ntiles + 1) * 4 + 1024;  // + alignment slack
 }
 
 // B layout: core matrix (8 rows x 8 f16 = 128 B) for K-chunk kc (dims 8kc ..
@@ -126,96 +90,90 @@ __device__ __forceinline__ uint32_t bq_offset(int n, int kc) {
   return (kc * (Cfg<QT>::kN / 8) + (n >> 3)) * 128 + (n & 7) * 16;
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// 2-D tiled bulk tensor copy: box at (x, y) of the tensor map into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Bounded wait that gives up at once when the CTA has aborted; raises on timeout.
 template <int QT>
-__global__ void __launch_bounds__(Cfg<QT>::kThreads, 1) score_kernel(const ScoreArgs a) {
+__device__ __forceinline__ bool role_wait(ScoreSmem<QT>& sm, uint64_t* bar, uint32_t parity, int32_t* err) {
+  if (*reinterpret_cast<volatile int*>(&sm.abort)) return false;
+  if (mbar_wait(bar, parity)) return true;
+  raise(err, M3S_DEVERR_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+  return false;
+}
+
+template <int QT>
+__global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
+    score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap codes_map) {
   using C = Cfg<QT>;
   constexpr uint32_t kIdesc = idesc_f16(128, C::kN);
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  ScoreSmem<QT>& sm = *reinterpret_cast<ScoreSmem<QT>*>(smem_raw);
-  int* pre = reinterpret_cast<int*>(smem_raw + sizeof(ScoreSmem<QT>));
-  __shared__ int red[C::kThreads / 32];
+  extern __shared__ uint8_t smem_raw[];
+  ScoreSmem<QT>& sm = *reinterpret_cast<ScoreSmem<QT>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  int* pre = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(ScoreSmem<QT>));
+  __shared__ int red[C::kWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int wg = warp >> 2, wq = warp & 3;  // warpgroup; quarter = TMEM lanes 32wq .. 32wq+31
-  const int wtid = tid & 127;               // = key index within the block
-  const bool issuer = wtid == 0;
-  const int bar_id = 1 + wg;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;  // TMEM lane quarter
 
   // ---- prologue: barriers and tensor memory (touches no input) ----
-  if (tid < C::kWG * kStages) mbar_init(&sm.sbar[tid / kStages][tid % kStages], 1);
-  if (tid < C::kWG) {
-    mbar_init(&sm.mbar[tid], 1);
-    sm.abort_wg[tid] = 0;
+  if (tid < C::kNS) {
+    mbar_init(&sm.full[tid], 1);
+    mbar_init(&sm.empty[tid], 128);
   }
-  if (tid == 0) sm.qbad = 0;
+  if (tid < C::kNA) {
+    mbar_init(&sm.afull[tid], 128);
+    mbar_init(&sm.aempty[tid], 1);
+  }
+  if (tid < C::kND) {
+    mbar_init(&sm.dfull[tid], 1);
+    mbar_init(&sm.dempty[tid], 128);
+  }
+  if (tid == 0) {
+    sm.qbad = 0;
+    sm.abort = 0;
+  }
   if (warp == 0) tmem_alloc(&sm.tmem_base, C::kTmemCols);
   mbar_fence_init();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t a_tm = tmem + wg * C::kWGCols;  // lane 0, first A column of this warpgroup
-  const uint32_t d_tm = a_tm + C::kACols;        // lane 0, first score column
-  const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
   pdl_trigger();
   pdl_wait();
 
-  // ---- exclusive prefix of block counts over tiles (block-wide scan) ----
+  // ---- exclusive prefix of block counts over tiles, then this CTA's range ----
+  tile_prefix<QT>(a, pre, red, C::kThreads);
   const int ntiles = a.ntiles;
-  const int per = (ntiles + C::kThreads - 1) / C::kThreads;
-  const int i0 = min(ntiles, tid * per), i1 = min(ntiles, i0 + per);
-  int local = 0;
-  for (int i = i0; i < i1; ++i) {
-    const TileInfo<QT> ti = tile_info<QT>(a, i, blockIdx.x == 0);
-    local += ti.nrows ? (ti.len + kPage - 1) / kPage : 0;
-  }
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
-  }
-  if (lane == 31) red[warp] = incl;
-  __syncthreads();
-  int base = 0;
-  for (int wv = 0; wv < warp; ++wv) base += red[wv];
-  int run = base + incl - local;
-  if (tid == 0) pre[0] = 0;
-  for (int i = i0; i < i1; ++i) {
-    const TileInfo<QT> ti = tile_info<QT>(a, i, false);
-    run += ti.nrows ? (ti.len + kPage - 1) / kPage : 0;
-    pre[i + 1] = run;
-  }
-  __syncthreads();
-
   const long long N = pre[ntiles];
   const int lo = static_cast<int>(N * blockIdx.x / gridDim.x);
   const int hi = static_cast<int>(N * (blockIdx.x + 1) / gridDim.x);
-  int tile = 0;
-  {
-    int l = 0, h = ntiles;  // pre[l] <= lo < pre[h]
-    while (h - l > 1) {
-      const int m = (l + h) >> 1;
-      if (pre[m] <= lo) l = m; else h = m;
-    }
-    tile = l;
-  }
+  int tile = tile_at(pre, ntiles, lo);
 
-  uint32_t sphase = 0;    // expected parity per stage of this warpgroup
-  uint32_t mphase = 0;    // expected parity of the MMA barrier
-  uint32_t pending = 0;   // issuer: stages with a copy not yet waited for
-  bool mma_pending = false;
-  float wreg[16];
-
+  int g0 = 0;               // sequence number of the segment's first block in this CTA
+  bool mma_issued = false;  // MMA thread: a commit may still be outstanding
+  uint32_t last_d = 0, last_ud = 0;
   int pos = lo;
   while (pos < hi) {
     while (pre[tile + 1] <= pos) ++tile;
     const int seg_lo = pos - pre[tile];
     const int seg_hi = min(hi, pre[tile + 1]) - pre[tile];
+    const int nseg = seg_hi - seg_lo;
     const TileInfo<QT> ti = tile_info<QT>(a, tile, false);
+    const int32_t* bt_row = a.block_table + static_cast<size_t>(ti.req) * a.bt_stride;
 
     // ---- stage the tile's queries (the B operand), weights and lengths ----
-    __syncthreads();
     for (int e = tid; e < C::kN * 16; e += C::kThreads) {
       const int n = e >> 4, kc = e & 15;
       const int rho = n >> 4, h = n & 15;
@@ -239,106 +197,75 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1) score_kernel(const Score
     if (tid < QT) sm.lensm[tid] = tid < ti.nrows ? a.row_len[ti.row0 + tid] : 0;
     fence_proxy_async();  // the queries are read by the tensor core (async proxy)
     __syncthreads();
-    int rlen[QT];
-#pragma unroll
-    for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
-    if constexpr (QT == 1) {
-#pragma unroll
-      for (int h = 0; h < 16; ++h) wreg[h] = sm.wsm[h];
-    }
 
-    // ---- this warpgroup's blocks: seg_lo + wg + k * kWG ----
-    const int first = seg_lo + wg;
-    const int count = first < seg_hi ? (seg_hi - first + C::kWG - 1) / C::kWG : 0;
-    const int32_t* bt_row = a.block_table + static_cast<size_t>(ti.req) * a.bt_stride;
-
-    auto issue = [&](int k) {  // issuer thread only
-      const int s = k % kStages;
-      const int page = bt_row[first + k * C::kWG];
-      int ok = 0;
-      if (page < 0 || page >= a.num_pages) {
-        raise(a.err, M3S_DEVERR_PAGE);
-      } else if (!sm.abort_wg[wg]) {
-        fence_proxy_async();
-        mbar_expect_tx(&sm.sbar[wg][s], kStageBytes);
-        bulk_g2s(sm.stage[wg][s], a.codes + static_cast<size_t>(page) * kPageCodeBytes,
-                 kPageCodeBytes, &sm.sbar[wg][s]);
-        bulk_g2s(sm.stage[wg][s] + kPageCodeBytes,
-                 a.scales + static_cast<size_t>(page) * kPageScaleBytes, kPageScaleBytes,
-                 &sm.sbar[wg][s]);
-        pending |= 1u << s;
-        ok = 1;
-      }
-      sm.svalid[wg][s] = ok;
-    };
-    if (issuer)
-      for (int k = 0; k < count && k < kStages; ++k) issue(k);
-    named_bar_sync(bar_id, 128);
-
-    for (int k = 0; k < count; ++k) {
-      const int s = k % kStages;
-      const int blk = first + k * C::kWG;
-      const bool issued = sm.svalid[wg][s] != 0;
-      const bool valid = issued && !sm.abort_wg[wg];
-      if (valid) {
-        if (!mbar_wait(&sm.sbar[wg][s], (sphase >> s) & 1u)) {
-          sm.abort_wg[wg] = 1;
-          raise(a.err, M3S_DEVERR_TIMEOUT);
-        } else if (issuer) {
-          pending &= ~(1u << s);
+    if (warp == 0) {
+      // ================= producer =================
+      PageWindow pw;
+      for (int j = 0; j < nseg; ++j) {
+        const int g = g0 + j, s = g % C::kNS, u = g / C::kNS;
+        const int page = pw.get(bt_row + seg_lo, j, 1, nseg, lane);
+        int ok = 1;
+        if (lane == 0) {
+          if (!role_wait(sm, &sm.empty[s], (u & 1) ^ 1, a.err)) {
+            ok = 0;
+          } else if (page < 0 || page >= a.num_pages) {
+            raise(a.err, M3S_DEVERR_PAGE);
+            mbar_arrive(&sm.full[s]);  // nothing to copy: complete the phase empty
+          } else {
+            mbar_expect_tx(&sm.full[s], kStageBytes);
+            tma_load_2d(sm.stage[s], &codes_map, 0, page * kPage, &sm.full[s]);
+            bulk_g2s(sm.stage[s] + kPageCodeBytes,
+                     a.scales + static_cast<size_t>(page) * kPageScaleBytes, kPageScaleBytes,
+                     &sm.full[s]);
+          }
         }
-        // dequantise key wtid into A (TMEM lane = key, column i = dims 2i, 2i+1)
-        const uint8_t* cs = sm.stage[wg][s];
-        const uint8_t* ss = cs + kPageCodeBytes;
-        const uint4* kp = reinterpret_cast<const uint4*>(cs + wtid * kCodeBytes);
-        const uint2 sc = *reinterpret_cast<const uint2*>(ss + wtid * kScaleBytes);
-        const uint32_t s01 = e4m3x2_to_f16x2(sc.x & 0xFFFFu), s23 = e4m3x2_to_f16x2(sc.x >> 16);
-        const uint32_t s45 = e4m3x2_to_f16x2(sc.y & 0xFFFFu), s67 = e4m3x2_to_f16x2(sc.y >> 16);
-        const uint32_t spair[4] = {s01, s23, s45, s67};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {  // chunk c = dims 32c .. 32c+31 = scale groups 2c, 2c+1
-          const uint4 wv = kp[c];
-          const uint32_t g0 = bcast_lo(spair[c]), g1 = bcast_hi(spair[c]);
-          uint32_t v[16];
-          e2m1x8_to_f16x2(wv.x, v[0], v[1], v[2], v[3]);
-          e2m1x8_to_f16x2(wv.y, v[4], v[5], v[6], v[7]);
-          e2m1x8_to_f16x2(wv.z, v[8], v[9], v[10], v[11]);
-          e2m1x8_to_f16x2(wv.w, v[12], v[13], v[14], v[15]);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = hmul2(v[i], g0);
-#pragma unroll
-          for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], g1);
-          tmem_st16(lane_base + a_tm + 16 * c, v);
-        }
-        tmem_wait_st();
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-      if (issued) sphase ^= 1u << s;
-      tc_fence_before();
-      named_bar_sync(bar_id, 128);
-      const bool go = valid && !sm.abort_wg[wg];
-      if (issuer) {
-        if (k + kStages < count) issue(k + kStages);  // stage s has been read by all
-        if (go) {
+    } else if (warp == 1) {
+      // ================= MMA issuer =================
+      if (lane == 0) {
+        for (int j = 0; j < nseg; ++j) {
+          const int g = g0 + j;
+          const int as = g % C::kNA, ua = g / C::kNA, ds = g % C::kND, ud = g / C::kND;
+          if (!role_wait(sm, &sm.afull[as], ua & 1, a.err)) break;
+          if (!role_wait(sm, &sm.dempty[ds], (ud & 1) ^ 1, a.err)) break;
           tc_fence_after();
+          const uint32_t a_tm = tmem + as * C::kACols;
+          const uint32_t d_tm = tmem + C::kNA * C::kACols + ds * C::kN;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint64_t bdesc = smem_desc_noswizzle(sm.bq + ks * 32 * C::kN, 16 * C::kN, 128);
             tc_mma_ts(d_tm, a_tm + 8 * ks, bdesc, kIdesc, ks > 0 ? 1u : 0u);
           }
-          tc_commit(&sm.mbar[wg]);
-          mma_pending = true;
+          tc_commit(&sm.dfull[ds]);
+          tc_commit(&sm.aempty[as]);
+          mma_issued = true;
+          last_d = ds;
+          last_ud = ud;
         }
       }
-      if (go) {
-        if (!mbar_wait(&sm.mbar[wg], mphase & 1u)) {
-          sm.abort_wg[wg] = 1;
-          raise(a.err, M3S_DEVERR_TIMEOUT);
-        } else if (issuer) {
-          mma_pending = false;
-        }
-        mphase ^= 1u;
+    } else if (warp < 6) {
+      // ================= epilogue warpgroup =================
+      const int etid = tid - 64;         // 0 .. 127 = key within the block (TMEM lane)
+      const int wq = warp & 3;
+      int rlen[QT];
+#pragma unroll
+      for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
+      float wreg[QT == 1 ? 16 : 1];
+      if constexpr (QT == 1) {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) wreg[h] = sm.wsm[h];
+      }
+      (void)wreg;
+      PageWindow pw;
+      for (int j = 0; j < nseg; ++j) {
+        const int g = g0 + j, ds = g % C::kND, ud = g / C::kND;
+        const int blk = seg_lo + j;
+        const int page = pw.get(bt_row + seg_lo, j, 1, nseg, lane);
+        if (!role_wait(sm, &sm.dfull[ds], ud & 1, a.err)) break;
         tc_fence_after();
-        const int tok = blk * kPage + wtid;
+        const int tok = blk * kPage + (32 * wq + lane);
+        const uint32_t d_tm = tmem + C::kNA * C::kACols + ds * C::kN;
 #pragma unroll
         for (int rho = 0; rho < QT; ++rho) {
           float d[16];
@@ -362,33 +289,72 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1) score_kernel(const Score
           float m = tok < rlen[rho] ? sc : -INFINITY;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == 0) sm.blkmax[wg][wq][rho] = m;
+          if (lane == 0) sm.blkmax[ds][wq][rho] = m;
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.dempty[ds]);
+        named_bar_sync(1, 128);
+        if (etid < QT) {
+          const int rho = etid;
+          if (rho < ti.nrows && blk * kPage < rlen[rho]) {
+            float m = -INFINITY;
+            if (page >= 0 && page < a.num_pages) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) m = fmaxf(m, sm.blkmax[ds][q][rho]);
+            }
+            a.bscores[static_cast<size_t>(ti.row0 + rho) * a.bs_stride + blk] = m;
+          }
         }
       }
-      tc_fence_before();
-      named_bar_sync(bar_id, 128);
-      if (wtid < QT) {
-        const int rho = wtid;
-        if (rho < ti.nrows && blk * kPage < rlen[rho]) {
-          float m = -INFINITY;
-          if (go) {
+    } else {
+      // ================= dequantising warpgroups =================
+      const int dq = (warp - 6) >> 2;    // which warpgroup
+      const int key = tid & 127;         // TMEM lane = key within the block
+      const int sw = (key >> 1) & 3;     // 64-byte swizzle of this key's row
+      PageWindow pw;
+      for (int j = dq; j < nseg; j += C::kNDQ) {
+        const int g = g0 + j, s = g % C::kNS, us = g / C::kNS;
+        const int as = g % C::kNA, ua = g / C::kNA;
+        const int page = pw.get(bt_row + seg_lo, j, C::kNDQ, nseg, lane);
+        if (!role_wait(sm, &sm.full[s], us & 1, a.err)) break;
+        if (!role_wait(sm, &sm.aempty[as], (ua & 1) ^ 1, a.err)) break;
+        if (page >= 0 && page < a.num_pages) {
+          const uint8_t* cs = sm.stage[s];
+          const uint8_t* ss = cs + kPageCodeBytes;
+          const uint2 sc = *reinterpret_cast<const uint2*>(ss + key * kScaleBytes);
+          const uint32_t spair[4] = {e4m3x2_to_f16x2(sc.x & 0xFFFFu), e4m3x2_to_f16x2(sc.x >> 16),
+                                     e4m3x2_to_f16x2(sc.y & 0xFFFFu), e4m3x2_to_f16x2(sc.y >> 16)};
+          const uint32_t a_tm = tmem + as * C::kACols;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) m = fmaxf(m, sm.blkmax[wg][q][rho]);
+          for (int c = 0; c < 4; ++c) {  // chunk c = dims 32c .. 32c+31 = scale groups 2c, 2c+1
+            const uint4 wv = *reinterpret_cast<const uint4*>(cs + key * kCodeBytes + 16 * (c ^ sw));
+            const uint32_t g0s = bcast_lo(spair[c]), g1s = bcast_hi(spair[c]);
+            uint32_t v[16];
+            e2m1x8_to_f16x2(wv.x, v[0], v[1], v[2], v[3]);
+            e2m1x8_to_f16x2(wv.y, v[4], v[5], v[6], v[7]);
+            e2m1x8_to_f16x2(wv.z, v[8], v[9], v[10], v[11]);
+            e2m1x8_to_f16x2(wv.w, v[12], v[13], v[14], v[15]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = hmul2(v[i], g0s);
+#pragma unroll
+            for (int i = 8; i < 16; ++i) v[i] = hmul2(v[i], g1s);
+            tmem_st16(lane_base + a_tm + 16 * c, v);
           }
-          a.bscores[static_cast<size_t>(ti.row0 + rho) * a.bs_stride + blk] = m;
+          tmem_wait_st();
         }
+        tc_fence_before();
+        mbar_arrive(&sm.afull[as]);
+        mbar_arrive(&sm.empty[s]);
       }
     }
+    __syncthreads();  // every role is done with this segment (and its queries)
+    g0 += nseg;
     pos = pre[tile] + seg_hi;
     ++tile;
   }
 
-  // ---- leave: drain anything still in flight after a timeout, free TMEM ----
-  if (issuer) {
-    for (int s = 0; s < kStages; ++s)
-      if (pending & (1u << s)) mbar_wait(&sm.sbar[wg][s], (sphase >> s) & 1u);
-    if (mma_pending) mbar_wait(&sm.mbar[wg], mphase & 1u);
-  }
+  // ---- leave: after a timeout, give the last MMA one more bounded wait; free TMEM ----
+  if (warp == 1 && lane == 0 && mma_issued && sm.abort) mbar_wait(&sm.dfull[last_d], last_ud & 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -528,12 +494,16 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   }
 }
 
+}  // namespace
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
   return n;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -543,15 +513,41 @@ size_t topk_smem(int bt_stride, int* keys_out) {
   return static_cast<size_t>(k) * 8;
 }
 
+// Tensor map over a one-head index code plane viewed as [num_pages * 128 rows]
+// x [64 bytes], boxes of one page (128 rows), 64-byte swizzle.
+bool make_codes_map(CUtensorMap* map, const uint8_t* codes, int num_pages) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kCodeBytes),
+                              static_cast<cuuint64_t>(num_pages > 0 ? num_pages : 1) * kPage};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kCodeBytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kCodeBytes), static_cast<cuuint32_t>(kPage)};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int QT>
 int launch_score(const ScoreArgs& a, cudaStream_t st) {
   const size_t smem = score_smem_bytes<QT>(a.ntiles);
   if (smem > 227 * 1024) return M3S_ERR_UNSUPPORTED;
+  CUtensorMap map;
+  if (a.num_pages > 0 && !make_codes_map(&map, a.codes, a.num_pages)) return M3S_ERR_LAUNCH;
+  if (a.num_pages <= 0) memset(&map, 0, sizeof(map));
   if (cudaFuncSetAttribute(score_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
-  return launch_kernel(score_kernel<QT>, dim3(sm_count()), dim3(Cfg<QT>::kThreads), smem, st, 0, a) ==
-                 cudaSuccess
+  return launch_kernel(score_kernel<QT>, dim3(sm_count()), dim3(Cfg<QT>::kThreads), smem, st, 0, a,
+                       map) == cudaSuccess
              ? M3S_OK
              : M3S_ERR_LAUNCH;
 }
@@ -602,7 +598,7 @@ extern "C" int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int
   if (B == 0) return M3S_OK;
   ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
               row_req, nullptr, row_len, R, B, R, 1, block_scores, bs_stride, err};
-  return launch_score<1>(a, static_cast<cudaStream_t>(stream));
+  return launch_score_decode(a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* row_req,
@@ -641,7 +637,7 @@ extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32
   if (B > 0) {
     ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
                 row_req, nullptr, row_len, R, B, R, 1, bs, stride, err};
-    rc = launch_score<1>(a, st);
+    rc = launch_score_decode(a, st);
     if (rc != M3S_OK) return rc;
   }
   return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, topk_ids, st);

@@ -1,0 +1,253 @@
+// Index scorer for single-row tiles (decode rows), on mma.sync tensor cores.
+//
+// "[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache" (ROCm/ATOM
+// #2744), Design / Index and Decode score grid: score[t] = sum_h w_h *
+// ReLU(q_h . k_t) over NVFP4 index keys decoded to 16-bit, block score = max
+// over the block's causal tokens, work spread so a long request cannot
+// serialise the kernel.
+//
+// With one query row per tile the product has only 16 columns (the index
+// heads), which is far too narrow for tcgen05.mma (every M128 x K16
+// instruction costs about the same time up to N = 128). The warp-level
+// m16n8k16 instruction fits this shape: the 16 keys of an m-tile are M, the
+// 16 heads two n8 tiles, and K walks the head dimension in a permuted order so
+// every thread's key bytes are one contiguous 16-byte chunk (the query
+// fragments use the same order, which leaves every dot product unchanged).
+//
+// Each of the 16 warps streams whole blocks of its share (every 16th block of
+// the CTA's contiguous range) as two halves of 64 keys through its own
+// double-buffered shared-memory stages, filled by 1-D bulk copies (TMA) that
+// complete on an mbarrier. Block-table entries are fetched 32 at a time.
+#include <cuda_runtime.h>
+
+#include "m3s_score_common.cuh"
+
+namespace m3s {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 2;                                    // per warp
+constexpr int kHalfKeys = 64;                                 // keys per stage
+constexpr int kHalfCodeBytes = kHalfKeys * kCodeBytes;        // 4096
+constexpr int kHalfScaleBytes = kHalfKeys * kScaleBytes;      // 512
+constexpr int kStageBytes = kHalfCodeBytes + kHalfScaleBytes; // 4608
+constexpr int kQFragWords = 8 * 2 * 32;                       // k-steps x n-tiles x lanes (uint2)
+
+struct __align__(16) DecodeSmem {
+  uint8_t stage[kWarps][kStages][kStageBytes];
+  uint64_t bar[kWarps][kStages];
+  uint2 qfrag[kQFragWords];
+  float w[16];
+  int len;
+  int qbad;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  int* pre = reinterpret_cast<int*>(smem_raw + sizeof(DecodeSmem));
+  __shared__ int red[kWarps];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  if (tid < kWarps * kStages) mbar_init(&sm.bar[tid / kStages][tid % kStages], 1);
+  if (tid == 0) sm.qbad = 0;
+  mbar_fence_init();
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+
+  tile_prefix<1>(a, pre, red, kThreads);
+  const int ntiles = a.ntiles;
+  const long long N = pre[ntiles];
+  const int lo = static_cast<int>(N * blockIdx.x / gridDim.x);
+  const int hi = static_cast<int>(N * (blockIdx.x + 1) / gridDim.x);
+  int tile = tile_at(pre, ntiles, lo);
+
+  uint32_t phase_bits = 0;  // per-stage mbarrier parity of this warp
+  bool aborted = false;
+
+  int pos = lo;
+  while (pos < hi) {
+    while (pre[tile + 1] <= pos) ++tile;
+    const int seg_lo = pos - pre[tile];
+    const int seg_hi = min(hi, pre[tile + 1]) - pre[tile];
+    const TileInfo<1> ti = tile_info<1>(a, tile, false);
+
+    // ---- the row's queries (fp16, fragment order), weights and length ----
+    __syncthreads();
+    for (int e = tid; e < kQFragWords; e += kThreads) {
+      const int ln = e & 31, c = (e >> 5) & 1, j = e >> 6;
+      const int h = 8 * c + (ln >> 2), tt = ln & 3;
+      uint2 v = make_uint2(0u, 0u);
+      if (ti.nrows && h < a.Hi) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(
+            a.q_idx + (static_cast<size_t>(ti.row0) * a.Hi + h) * kHeadDim + 32 * tt + 4 * j);
+        bool bad = false;
+        v.x = bf16x2_to_f16x2(raw.x, bad);
+        v.y = bf16x2_to_f16x2(raw.y, bad);
+        if (bad) sm.qbad = 1;
+      }
+      sm.qfrag[e] = v;
+    }
+    if (tid < 16) sm.w[tid] = (ti.nrows && tid < a.Hi) ? a.w[static_cast<size_t>(ti.row0) * a.Hi + tid] : 0.f;
+    if (tid == 0) sm.len = ti.nrows ? a.row_len[ti.row0] : 0;
+    __syncthreads();
+
+    const float w0 = sm.w[2 * t], w1 = sm.w[2 * t + 1], w2 = sm.w[8 + 2 * t], w3 = sm.w[9 + 2 * t];
+    const int rlen = sm.len;
+    uint32_t qa[8][2][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint2 v = sm.qfrag[(j * 2 + c) * 32 + lane];
+        qa[j][c][0] = v.x;
+        qa[j][c][1] = v.y;
+      }
+
+    // ---- this warp's blocks: seg_lo + warp + k * kWarps, two halves each ----
+    const int first = seg_lo + warp;
+    const int count = first < seg_hi ? (seg_hi - first + kWarps - 1) / kWarps : 0;
+    const int nhalf = 2 * count;
+    const int32_t* bt_row = a.block_table + static_cast<size_t>(ti.req) * a.bt_stride;
+    PageWindow pw;
+    uint32_t valid_bits = 0;
+
+    auto issue = [&](int hh) {  // all lanes (the page window is warp-wide)
+      const int s = hh & 1;
+      const int blk = first + (hh >> 1) * kWarps;
+      const int half = hh & 1;
+      const int page = pw.get(bt_row, blk, kWarps, seg_hi, lane);
+      int ok = 0;
+      if (lane == 0 && !aborted) {
+        if (page < 0 || page >= a.num_pages) {
+          if (half == 0) raise(a.err, M3S_DEVERR_PAGE);
+        } else {
+          fence_proxy_async();
+          mbar_expect_tx(&sm.bar[warp][s], kStageBytes);
+          bulk_g2s(sm.stage[warp][s],
+                   a.codes + static_cast<size_t>(page) * kPageCodeBytes + half * kHalfCodeBytes,
+                   kHalfCodeBytes, &sm.bar[warp][s]);
+          bulk_g2s(sm.stage[warp][s] + kHalfCodeBytes,
+                   a.scales + static_cast<size_t>(page) * kPageScaleBytes + half * kHalfScaleBytes,
+                   kHalfScaleBytes, &sm.bar[warp][s]);
+          ok = 1;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      valid_bits = (valid_bits & ~(1u << s)) | (static_cast<uint32_t>(ok) << s);
+    };
+
+    if (nhalf > 0) issue(0);
+    if (nhalf > 1) issue(1);
+    float best = -INFINITY;
+    for (int hh = 0; hh < nhalf; ++hh) {
+      const int s = hh & 1;
+      const int blk = first + (hh >> 1) * kWarps;
+      const int half = hh & 1;
+      if (half == 0) best = -INFINITY;
+      bool have = (valid_bits >> s) & 1u;
+      if (have) {
+        const bool done = mbar_wait(&sm.bar[warp][s], (phase_bits >> s) & 1u);
+        phase_bits ^= 1u << s;
+        if (!done) {
+          if (lane == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
+          aborted = true;
+          have = false;
+          // give the copies still in flight one more bounded wait before leaving
+          mbar_wait(&sm.bar[warp][s], ((phase_bits >> s) & 1u) ^ 1u);
+          if (hh + 1 < nhalf && ((valid_bits >> (s ^ 1)) & 1u))
+            mbar_wait(&sm.bar[warp][s ^ 1], (phase_bits >> (s ^ 1)) & 1u);
+          valid_bits = 0;
+        }
+      }
+      if (have) {
+        const uint8_t* cs = sm.stage[warp][s];
+        const uint8_t* ss = cs + kHalfCodeBytes;
+#pragma unroll 1
+        for (int mt = 0; mt < kHalfKeys / 16; ++mt) {
+          const int key0 = mt * 16 + g;
+          const uint4 ca = *reinterpret_cast<const uint4*>(cs + key0 * kCodeBytes + 16 * t);
+          const uint4 cb = *reinterpret_cast<const uint4*>(cs + (key0 + 8) * kCodeBytes + 16 * t);
+          const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + key0 * kScaleBytes + 2 * t));
+          const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + (key0 + 8) * kScaleBytes + 2 * t));
+          const uint32_t sa0 = bcast_lo(sa), sa1 = bcast_hi(sa);
+          const uint32_t sb0 = bcast_lo(sb), sb1 = bcast_hi(sb);
+          const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
+          const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
+          float acc[2][4];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+#pragma unroll
+          for (int jw = 0; jw < 4; ++jw) {
+            // word jw of the thread's chunk = bytes 4jw .. 4jw+3 = k-steps 2jw
+            // (bytes 4jw, 4jw+1) and 2jw+1 (bytes 4jw+2, 4jw+3); the chunk holds
+            // dims 32t .. 32t+31, scale group 2t for words 0-1, 2t+1 for 2-3
+            uint32_t xa[4], xb[4];
+            e2m1x8_to_f16x2(wa[jw], xa[0], xa[1], xa[2], xa[3]);
+            e2m1x8_to_f16x2(wb[jw], xb[0], xb[1], xb[2], xb[3]);
+            const uint32_t scA = jw < 2 ? sa0 : sa1, scB = jw < 2 ? sb0 : sb1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              xa[e] = hmul2(xa[e], scA);
+              xb[e] = hmul2(xb[e], scB);
+            }
+#pragma unroll
+            for (int js = 0; js < 2; ++js) {
+              const int j = 2 * jw + js;
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                mma16816(acc[c], xa[2 * js], xb[2 * js], xa[2 * js + 1], xb[2 * js + 1], qa[j][c][0],
+                         qa[j][c][1]);
+            }
+          }
+          // token scores of keys key0 and key0 + 8
+          float p0 = w0 * fmaxf(acc[0][0], 0.f) + w1 * fmaxf(acc[0][1], 0.f) +
+                     w2 * fmaxf(acc[1][0], 0.f) + w3 * fmaxf(acc[1][1], 0.f);
+          float p1 = w0 * fmaxf(acc[0][2], 0.f) + w1 * fmaxf(acc[0][3], 0.f) +
+                     w2 * fmaxf(acc[1][2], 0.f) + w3 * fmaxf(acc[1][3], 0.f);
+          p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+          p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+          p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
+          p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+          const int tok0 = blk * kPage + half * kHalfKeys + key0;
+          if (tok0 < rlen) best = fmaxf(best, p0);
+          if (tok0 + 8 < rlen) best = fmaxf(best, p1);
+        }
+      }
+      if (half == 1) {
+        float m = best;
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+        if (lane == 0 && ti.nrows && blk * kPage < rlen)
+          a.bscores[static_cast<size_t>(ti.row0) * a.bs_stride + blk] = m;
+      }
+      __syncwarp();
+      if (hh + 2 < nhalf) issue(hh + 2);
+    }
+    pos = pre[tile] + seg_hi;
+    ++tile;
+  }
+  __syncthreads();
+  if (tid == 0 && sm.qbad) raise(a.err, M3S_DEVERR_QRANGE);
+}
+
+}  // namespace
+
+int launch_score_decode(const ScoreArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(DecodeSmem) + (a.ntiles + 1) * 4 + 16;
+  if (smem > 227 * 1024) return M3S_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(score_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return M3S_ERR_LAUNCH;
+  return launch_kernel(score_decode_kernel, dim3(sm_count()), dim3(kThreads), smem, st, 0, a) ==
+                 cudaSuccess
+             ? M3S_OK
+             : M3S_ERR_LAUNCH;
+}
+
+}  // namespace m3s
