@@ -176,7 +176,9 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
 
   for (int i = 0; i < nblocks; ++i) {
     const int s = i & 1;
-    if (!aborted && !mbar_wait(&sm.bar[s], (i >> 1) & 1)) {
+    const bool fail = !aborted && !mbar_wait(&sm.bar[s], (i >> 1) & 1);
+    // one decision for the whole CTA before any warp-collective work
+    if (__syncthreads_or(fail) && !aborted) {
       aborted = true;
       if (tid == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
       // give the copies still in flight one more bounded wait before leaving

@@ -69,7 +69,7 @@ struct __align__(1024) ScoreSmem {
   uint64_t full[Cfg<QT>::kNS], empty[Cfg<QT>::kNS];
   uint64_t afull[Cfg<QT>::kNA], aempty[Cfg<QT>::kNA];
   uint64_t dfull[Cfg<QT>::kND], dempty[Cfg<QT>::kND];
-  float blkmax[Cfg<QT>::kND][4][QT];
+  uint32_t blkmax[Cfg<QT>::kND][4][QT];  // order-preserving bits of per-warp maxima
   float wsm[QT * 16];
   int lensm[QT];
   uint32_t tmem_base;
@@ -262,45 +262,61 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
         const int g = g0 + j, ds = g % C::kND, ud = g / C::kND;
         const int blk = seg_lo + j;
         const int page = pw.get(bt_row + seg_lo, j, 1, nseg, lane);
-        if (!role_wait(sm, &sm.dfull[ds], ud & 1, a.err)) break;
+        const bool ok = __all_sync(0xffffffffu, role_wait(sm, &sm.dfull[ds], ud & 1, a.err));
         tc_fence_after();
         const int tok = blk * kPage + (32 * wq + lane);
         const uint32_t d_tm = tmem + C::kNA * C::kACols + ds * C::kN;
+        // two rows of 16 head scores per tensor-memory load; the block maximum over
+        // the warp's 32 keys is one redux on order-preserving integer keys
 #pragma unroll
-        for (int rho = 0; rho < QT; ++rho) {
-          float d[16];
-          tmem_ld16(lane_base + d_tm + 16 * rho, d);
-          tmem_wait_ld();
-          float sc = 0.f;
+        for (int rp = 0; rp < QT; rp += 2) {
+          if (!ok) break;
+          float d[32];
           if constexpr (QT == 1) {
+            float h16[16];
+            tmem_ld16(lane_base + d_tm, h16);
 #pragma unroll
-            for (int h = 0; h < 16; ++h) sc = fmaf(wreg[h], fmaxf(d[h], 0.f), sc);
+            for (int i = 0; i < 16; ++i) d[i] = h16[i];
           } else {
-            const float4* w4 = reinterpret_cast<const float4*>(sm.wsm + 16 * rho);
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const float4 wv = w4[q4];
-              sc = fmaf(wv.x, fmaxf(d[4 * q4 + 0], 0.f), sc);
-              sc = fmaf(wv.y, fmaxf(d[4 * q4 + 1], 0.f), sc);
-              sc = fmaf(wv.z, fmaxf(d[4 * q4 + 2], 0.f), sc);
-              sc = fmaf(wv.w, fmaxf(d[4 * q4 + 3], 0.f), sc);
-            }
+            tmem_ld32(lane_base + d_tm + 16 * rp, d);
           }
-          float m = tok < rlen[rho] ? sc : -INFINITY;
+          tmem_wait_ld();
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == 0) sm.blkmax[ds][wq][rho] = m;
+          for (int r = 0; r < 2 && rp + r < QT; ++r) {
+            const int rho = rp + r;
+            float sc = 0.f;
+            if constexpr (QT == 1) {
+#pragma unroll
+              for (int h = 0; h < 16; ++h) sc = fmaf(wreg[h], fmaxf(d[h], 0.f), sc);
+            } else {
+              const float4* w4 = reinterpret_cast<const float4*>(sm.wsm + 16 * rho);
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 wv = w4[q4];
+                sc = fmaf(wv.x, fmaxf(d[16 * r + 4 * q4 + 0], 0.f), sc);
+                sc = fmaf(wv.y, fmaxf(d[16 * r + 4 * q4 + 1], 0.f), sc);
+                sc = fmaf(wv.z, fmaxf(d[16 * r + 4 * q4 + 2], 0.f), sc);
+                sc = fmaf(wv.w, fmaxf(d[16 * r + 4 * q4 + 3], 0.f), sc);
+              }
+            }
+            const uint32_t key = ordered_bits(tok < rlen[rho] ? sc : -INFINITY);
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+            if (lane == 0) sm.blkmax[ds][wq][rho] = mx;
+          }
         }
         tc_fence_before();
         mbar_arrive(&sm.dempty[ds]);
         named_bar_sync(1, 128);
+        if (*reinterpret_cast<volatile int*>(&sm.abort)) break;  // uniform: read after the barrier
         if (etid < QT) {
           const int rho = etid;
           if (rho < ti.nrows && blk * kPage < rlen[rho]) {
             float m = -INFINITY;
             if (page >= 0 && page < a.num_pages) {
+              uint32_t mk = 0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) m = fmaxf(m, sm.blkmax[ds][q][rho]);
+              for (int q = 0; q < 4; ++q) mk = max(mk, sm.blkmax[ds][q][rho]);
+              m = from_ordered_bits(mk);
             }
             a.bscores[static_cast<size_t>(ti.row0 + rho) * a.bs_stride + blk] = m;
           }
@@ -312,12 +328,15 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
       const int key = tid & 127;         // TMEM lane = key within the block
       const int sw = (key >> 1) & 3;     // 64-byte swizzle of this key's row
       PageWindow pw;
-      for (int j = dq; j < nseg; j += C::kNDQ) {
+      // block g = g0 + j belongs to warpgroup g % kNDQ, whatever g0 the segment
+      // starts at: each stage and A slot is then used by one warpgroup only
+      for (int j = ((dq - g0) % C::kNDQ + C::kNDQ) % C::kNDQ; j < nseg; j += C::kNDQ) {
         const int g = g0 + j, s = g % C::kNS, us = g / C::kNS;
         const int as = g % C::kNA, ua = g / C::kNA;
         const int page = pw.get(bt_row + seg_lo, j, C::kNDQ, nseg, lane);
-        if (!role_wait(sm, &sm.full[s], us & 1, a.err)) break;
-        if (!role_wait(sm, &sm.aempty[as], (ua & 1) ^ 1, a.err)) break;
+        // failed (timed-out) waits are made warp-uniform before any warp-collective op
+        if (!__all_sync(0xffffffffu, role_wait(sm, &sm.full[s], us & 1, a.err))) break;
+        if (!__all_sync(0xffffffffu, role_wait(sm, &sm.aempty[as], (ua & 1) ^ 1, a.err))) break;
         if (page >= 0 && page < a.num_pages) {
           const uint8_t* cs = sm.stage[s];
           const uint8_t* ss = cs + kPageCodeBytes;

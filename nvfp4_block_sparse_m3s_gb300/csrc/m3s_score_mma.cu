@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
       if (half == 0) best = -INFINITY;
       bool have = (valid_bits >> s) & 1u;
       if (have) {
-        const bool done = mbar_wait(&sm.bar[warp][s], (phase_bits >> s) & 1u);
+        // every lane waits; the warp takes one decision (the loop below is warp-collective)
+        const bool done = __all_sync(0xffffffffu, mbar_wait(&sm.bar[warp][s], (phase_bits >> s) & 1u));
         phase_bits ^= 1u << s;
         if (!done) {
           if (lane == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
