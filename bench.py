@@ -56,6 +56,36 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel, from one ncu capture of this bench's workload (summary under
+# profiles/). It is reported only while the kernel's sources hash to what was
+# captured; after any change it is null until the counters are taken again.
+NCU_TRAFFIC = {
+    ("skewed", "score_decode_kernel"): {
+        "bytes": 110_721_792 + 3_161_600,
+        "sources": {"m3s_score_mma.cu": "b3851cde1e369617",
+                    "m3s_score_common.cuh": "8c1bedc424ca4235"},
+    },
+}
+
+
+def ncu_traffic(workload, kernel):
+    import hashlib
+    rec = NCU_TRAFFIC.get((workload, kernel))
+    if rec is None:
+        return None
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "nvfp4_block_sparse_m3s_gb300",
+                        "csrc")
+    for name, digest in rec["sources"].items():
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest()[:16] != digest:
+                    return None
+        except OSError:
+            return None
+    return rec["bytes"]
+
+
 def workload_config(spec, ntok):
     return {
         "workload": spec.description,
@@ -78,13 +108,15 @@ def workload_config(spec, ntok):
 # --------------------------------------------------------------------------
 
 def oracle_sample(spec_name: str, reps: int):
-    """Time the oracle's step for one request of the workload.
+    """Time the oracle's step for a bounded sample of the workload.
 
-    The sample is the step of one request (its new K / V / index-K rows
-    stored, row map, score + top-k over its causal keys, attention over its
-    selected blocks). The step of the whole batch is extrapolated from it by
-    the ratio of causal keys scored (scoring dominates the oracle's time).
-    Returns (seconds per sample step, description, rows in the sample, scale).
+    The sample is the last request's step restricted to at most 8 of its
+    rows, evenly spaced and always including its last row: the new K / V /
+    index-K rows of those positions stored, the request's row map, score +
+    top-k over each sampled row's causal keys and attention over its selected
+    blocks. The whole batch's step is extrapolated from it by the ratio of
+    causal keys scored (scoring dominates the oracle's time).
+    Returns (seconds per sample step, description, rows in the batch, scale).
     """
     import numpy as np
 
@@ -93,42 +125,45 @@ def oracle_sample(spec_name: str, reps: int):
 
     wl = W.make(spec_name, with_cache_src=False)
     s = wl.spec
-    # the sampled request: the last one (a 150K-token request for the skewed batch)
     b = s.batch - 1
     L = int(wl.seq_len[b])
     t0, t1 = int(wl.tok_off[b]), int(wl.tok_off[b + 1])
     nb = (L + 127) // 128
-    pages = wl.block_table[b, :nb].astype(np.int64)
+    qb = int(wl.cu_q[b + 1] - wl.cu_q[b])
+    r0 = int(wl.cu_q[b])
+    nsamp = min(qb, 8)
+    sample = sorted({int(round(i * (qb - 1) / max(1, nsamp - 1))) for i in range(nsamp)} | {qb - 1})
     kc, ks = O.new_planes(wl.num_pages, s.hkv)
     vc, vs = O.new_planes(wl.num_pages, s.hkv)
     ic, is_ = O.new_planes(wl.num_pages, 1)
-    ntok = wl.ntok
     srcs = {}
     for name, h, c, sc in (("k", s.hkv, kc, ks), ("v", s.hkv, vc, vs), ("ik", 1, ic, is_)):
-        src = W.bf16_tensor(s.seed, name, (ntok, h, 128), s.n_out, s.out_factor, rows=(t0, t1))
+        src = W.bf16_tensor(s.seed, name, (wl.ntok, h, 128), s.n_out, s.out_factor, rows=(t0, t1))
         srcs[name] = src
         O.nvfp4_store(src, wl.slot_all[t0:t1], c, sc)          # the resident cache (setup)
-    qb = int(wl.cu_q[b + 1] - wl.cu_q[b])
-    r0 = int(wl.cu_q[b])
     cu = np.array([0, qb], dtype=np.int32)
     seq = np.array([L], dtype=np.int32)
     bt = wl.block_table[b: b + 1]
     new = wl.new_tok[(wl.new_tok >= t0) & (wl.new_tok < t1)] - t0    # this step's rows of b
+    new = new[np.array(sample)] if len(new) == qb else new
+    q_idx, wgt, q = wl.q_idx[r0: r0 + qb], wl.w[r0: r0 + qb], wl.q[r0: r0 + qb]
     times = []
     for _ in range(reps):
         t = time.perf_counter()
         for name, c, sc in (("k", kc, ks), ("v", vc, vs), ("ik", ic, is_)):
             O.nvfp4_store(srcs[name][new], wl.slot_all[t0 + new], c, sc)
         rr, rl = O.decode_rows(cu, seq, qb)
-        ids, _, _ = O.index_score_topk(wl.q_idx[r0: r0 + qb], wl.w[r0: r0 + qb], ic, is_, bt, rr,
-                                       rl, s.topk)
-        O.sparse_attention(wl.q[r0: r0 + qb], s.hkv, kc, ks, vc, vs, bt, rr, rl, ids, SM_SCALE)
+        ids, _, _ = O.index_score_topk(q_idx, wgt, ic, is_, bt, rr, rl, s.topk, rows=sample)
+        O.sparse_attention(q, s.hkv, kc, ks, vc, vs, bt, rr, rl, ids, SM_SCALE, rows=sample)
         times.append(time.perf_counter() - t)
     t_sample = min(times)
-    keys_all = float(np.sum(wl.seq_len.astype(np.float64)))
-    scale = keys_all / L
-    desc = (f"oracle step of request {b} ({L} cached tokens, {qb} row(s)) timed {reps}x (best),"
-            f" scaled by causal keys x{scale:.2f} to the batch of {s.rows} rows")
+    _, rl_all = O.decode_rows(wl.cu_q, wl.seq_len, s.rows)
+    keys_all = float(np.sum(rl_all.astype(np.float64)))
+    keys_sample = float(sum(int(rl[r]) for r in sample))
+    scale = keys_all / keys_sample
+    desc = (f"oracle step of {len(sample)} of the {qb} row(s) of request {b} ({L} cached tokens),"
+            f" timed {reps}x (best), scaled by causal keys x{scale:.2f} to the batch of"
+            f" {s.rows} rows")
     return t_sample, desc, s.rows, scale
 
 
@@ -481,7 +516,8 @@ def run_ours(args):
         "achieved_gbs_step": world * step_bytes / (ms * 1e-3) / 1e9,
         "algorithmic_bytes_per_step": step_bytes,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": ncu_traffic(s.name, "score_kernel" if fused else "score_decode_kernel"),
                      "kernel": ("score_kernel<8> + topk (m3s_verify_score_topk)" if fused
                                 else "score_decode_kernel (m3s_index_block_scores)"),
                      "kernel_ms": score_ms, "bytes_per_launch": score_bytes,
