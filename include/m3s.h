@@ -192,6 +192,30 @@ int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* 
                    int32_t* topk_ids, void* stream);
 
 /*
+ * m3s_index_score_topk without a caller workspace. The pages have no
+ * counterpart to this call; it is an integration variant of
+ * m3s_index_score_topk (same arguments minus block_scores / ws / ws_bytes,
+ * same result) for callers that cannot allocate device memory at call time:
+ * a C host that links only this library and owns no device allocator, or an
+ * engine plugin whose device memory is budgeted once at start-up.
+ * The block-score scratch is a file-scope device array of
+ * M3S_STATIC_SCRATCH_BYTES (4 MiB), one per device; the call allocates
+ * nothing. R * max(bt_stride, 1) * 4 bytes above that size returns
+ * M3S_ERR_WORKSPACE before any launch. The first call on a device looks the
+ * array up (cudaGetSymbolAddress, which also loads the library's device
+ * module) and should come before any stream capture; later calls reuse the
+ * cached address. Nothing in the scratch needs to start at zero. Every call
+ * on a device shares the one scratch: calls that overlap on the GPU (e.g. on
+ * two unordered streams) race and may return wrong ids.
+ */
+#define M3S_STATIC_SCRATCH_BYTES (4u << 20)
+int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t Hi,
+                                m3s_nvfp4_plane idx_k, const int32_t* block_table,
+                                int32_t bt_stride, const int32_t* row_req, const int32_t* row_len,
+                                int32_t R, int32_t B, int32_t topk, int32_t* topk_ids,
+                                int32_t* err, void* stream);
+
+/*
  * Fused verify score + top-k. #2744, Design / Fused verify top-k: for
  * speculative-verify rows, index scoring and top-k in one pass over each
  * request's keys, emitting top-k ids only (all the sparse attention reads).

@@ -54,6 +54,8 @@ _SIGS = {
     "m3s_decode_rows": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
     "m3s_index_score_topk": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
                                             _I32, _P, _P, _P, _SZ, _P, _P]),
+    "m3s_index_score_topk_static": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32,
+                                                   _I32, _I32, _P, _P, _P]),
     "m3s_index_block_scores": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
                                               _P, _I32, _P, _P]),
     "m3s_block_topk": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
@@ -174,6 +176,19 @@ def m3s_index_score_topk(q_idx, w, codes, scales, block_table, row_req, row_len,
         _ptr(row_req), _ptr(row_len), R, B, topk, _ptr(topk_ids), _ptr(block_scores), _ptr(ws),
         0 if ws is None else ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
     _check(rc, "m3s_index_score_topk")
+    return topk_ids
+
+
+def m3s_index_score_topk_static(q_idx, w, codes, scales, block_table, row_req, row_len, topk: int,
+                                topk_ids=None, err=None, stream=None):
+    R, Hi = q_idx.shape[0], q_idx.shape[1]
+    B, bt_stride = block_table.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((R, topk), dtype=torch.int32, device=q_idx.device)
+    rc = load().m3s_index_score_topk_static(
+        _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride,
+        _ptr(row_req), _ptr(row_len), R, B, topk, _ptr(topk_ids), _ptr(err), _stream(stream))
+    _check(rc, "m3s_index_score_topk_static")
     return topk_ids
 
 

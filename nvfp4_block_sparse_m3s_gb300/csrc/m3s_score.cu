@@ -27,6 +27,7 @@
 // A slots and accumulators from one role to the next, so no role waits on a
 // round trip of another.
 #include <cstring>
+#include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -693,4 +694,80 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
   rc = launch_score<8>(a, st);
   if (rc != M3S_OK) return rc;
   return launch_topk(bs, bt_stride, nullptr, row_len, R, B, bt_stride, topk, topk_ids, st);
+}
+
+// ---------------------------------------------------------------------------
+// m3s_index_score_topk_static: m3s_index_score_topk with its block-score
+// scratch in a file-scope device array instead of a caller workspace.
+//
+// It serves callers that cannot allocate device memory when they call: a
+// plain C host that links only this library and owns no device allocator,
+// and an engine plugin whose device memory budget is fixed at start-up, so
+// it cannot size a workspace per call. Those callers get a scratch whose
+// size is fixed when the library is built.
+//
+// The host side looks the array's address up once per device
+// (cudaGetSymbolAddress); that first call per device also loads the module
+// that holds the array, so it should come before any stream capture. Later
+// calls only read the cached address. Nothing in the scratch has to start at
+// zero: the scorer writes every block score that the top-k reads (each block
+// below the row's block count, -inf for a skipped page). All calls share one
+// scratch per device, so two calls that overlap on the GPU (different
+// streams, no ordering between them) race on it.
+// ---------------------------------------------------------------------------
+namespace m3s {
+namespace {
+
+constexpr size_t kStaticScratchFloats = M3S_STATIC_SCRATCH_BYTES / sizeof(float);
+static_assert(M3S_STATIC_SCRATCH_BYTES % 256 == 0, "static scratch size");
+
+static __device__ __align__(256) float g_static_block_scores[kStaticScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mutex;
+float* g_static_addr[kMaxDevices] = {};
+
+// The array's address on the current device, looked up on the first call for
+// that device. Returns nullptr when the lookup fails.
+float* static_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_static_mutex);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_block_scores) != cudaSuccess) return nullptr;
+    g_static_addr[dev] = static_cast<float*>(p);
+  }
+  return g_static_addr[dev];
+}
+
+}  // namespace
+}  // namespace m3s
+
+extern "C" int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t Hi,
+                                           m3s_nvfp4_plane idx_k, const int32_t* block_table,
+                                           int32_t bt_stride, const int32_t* row_req,
+                                           const int32_t* row_len, int32_t R, int32_t B,
+                                           int32_t topk, int32_t* topk_ids, int32_t* err,
+                                           void* stream) {
+  using namespace m3s;
+  int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk_ids);
+  if (rc != M3S_OK || R == 0) return rc;
+  if (!row_req || !row_len) return M3S_ERR_INVALID;
+  if (R > kMaxTiles) return M3S_ERR_UNSUPPORTED;
+  if (topk == 0) return M3S_OK;
+  const int stride = bt_stride > 0 ? bt_stride : 1;
+  // the block-score matrix [R][stride] must fit the fixed scratch
+  if (static_cast<size_t>(R) * static_cast<size_t>(stride) > kStaticScratchFloats)
+    return M3S_ERR_WORKSPACE;
+  float* bs = static_scratch();
+  if (!bs) return M3S_ERR_LAUNCH;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (B > 0) {
+    ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
+                row_req, nullptr, row_len, R, B, R, 1, bs, stride, err};
+    rc = launch_score_decode(a, st);
+    if (rc != M3S_OK) return rc;
+  }
+  return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, topk_ids, st);
 }
