@@ -91,19 +91,6 @@ __device__ __forceinline__ uint32_t bq_offset(int n, int kc) {
   return (kc * (Cfg<QT>::kN / 8) + (n >> 3)) * 128 + (n & 7) * 16;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// 2-D tiled bulk tensor copy: box at (x, y) of the tensor map into shared memory.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3}], [%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // Bounded wait that gives up at once when the CTA has aborted; raises on timeout.
 template <int QT>
 __device__ __forceinline__ bool role_wait(ScoreSmem<QT>& sm, uint64_t* bar, uint32_t parity, int32_t* err) {
@@ -516,23 +503,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
 
 }  // namespace
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-  return n;
-}
-
-namespace {
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-size_t topk_smem(int bt_stride, int* keys_out) {
-  const int k = bt_stride < 12288 ? bt_stride : 12288;
-  *keys_out = k;
-  return static_cast<size_t>(k) * 8;
-}
-
 // Tensor map over a one-head index code plane viewed as [num_pages * 128 rows]
 // x [64 bytes], boxes of one page (128 rows), 64-byte swizzle.
 bool make_codes_map(CUtensorMap* map, const uint8_t* codes, int num_pages) {
@@ -554,6 +524,23 @@ bool make_codes_map(CUtensorMap* map, const uint8_t* codes, int num_pages) {
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides,
                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t topk_smem(int bt_stride, int* keys_out) {
+  const int k = bt_stride < 12288 ? bt_stride : 12288;
+  *keys_out = k;
+  return static_cast<size_t>(k) * 8;
 }
 
 template <int QT>

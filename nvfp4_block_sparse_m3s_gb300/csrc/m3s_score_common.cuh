@@ -2,6 +2,8 @@
 // hands out block-table entries to a warp.
 #pragma once
 
+#include <cuda.h>
+
 #include "m3s_device.cuh"
 
 namespace m3s {
@@ -122,6 +124,9 @@ struct PageWindow {
 };
 
 int sm_count();
+// Tensor map over a one-head index code plane viewed as [num_pages * 128 rows]
+// x [64 bytes], boxes of one page (128 rows), 64-byte swizzle.
+bool make_codes_map(CUtensorMap* map, const uint8_t* codes, int num_pages);
 int launch_score_decode(const ScoreArgs& a, cudaStream_t st);
 
 }  // namespace m3s
