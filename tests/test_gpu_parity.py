@@ -283,10 +283,12 @@ def test_store_batch_equals_single_stores(lib):
 
 def test_block_topk_direct_against_oracle(lib):
     """m3s_block_topk on given fp32 block scores == the oracle's selection exactly:
-    ties (lower id wins), +-0, negatives, rows narrower than k, and rows wider
-    than the shared-memory key cache."""
+    ties (lower id wins), +-0, negatives, rows narrower than k, and rows on
+    every path of the selection (keys in registers, in shared memory, re-read)."""
     rng = np.random.default_rng(11)
-    widths = [1, 5, 16, 17, 300, 3600, 20000]
+    # 8192 / 8193: the edge of the keys-in-registers path (8 a thread);
+    # 10000: keys kept in shared memory; 20000: keys read again from memory
+    widths = [1, 5, 16, 17, 300, 3600, 8192, 8193, 10000, 20000]
     bt_stride = max(widths)
     R = len(widths) * 4
     scores = np.zeros((R, bt_stride), dtype=np.float32)
