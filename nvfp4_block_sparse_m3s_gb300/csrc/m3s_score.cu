@@ -41,21 +41,26 @@ namespace {
 constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;  // one block: 9216 = 9 x 1024
 
 // Roles and resources. Warp 0: producer (bulk copies); warp 1: MMA issuer;
-// warps 2-5: epilogue warpgroup; warps 6 ...: kNDQ dequantising warpgroups.
+// warps 2 .. 2 + 4 kNEpi - 1: epilogue warpgroups (block g -> g % kNEpi, which
+// owns accumulator slot g % kND); then kNDQ dequantising warpgroups.
 // Tensor memory: kNA A slots of 64 columns (128 keys x 128 f16) and kND
 // accumulator slots of N = 16 * QT f32 columns.
 template <int QT>
 struct Cfg {
+  static_assert(QT % 2 == 0 && QT <= 8, "rows per tile: an even count up to 8");
   static constexpr int kN = 16 * QT;
-  static constexpr int kNDQ = QT == 1 ? 3 : 2;
-  static constexpr int kWarps = 2 + 4 + 4 * kNDQ;
+  // 14 warps: the register file is split over the four SM sub-partitions, so
+  // at most four warps a partition keeps 128 registers a thread
+  static constexpr int kNDQ = 1;
+  static constexpr int kNEpi = 2;
+  static constexpr int kWarps = 2 + 4 * kNEpi + 4 * kNDQ;
   static constexpr int kThreads = 32 * kWarps;
   // Stages and A slots are multiples of kNDQ: block g goes to warpgroup g % kNDQ,
   // stage g % kNS and slot g % kNA, so each stage and each slot is only ever used
   // by one warpgroup, in order, and a parity wait can never see a phase two back.
-  static constexpr int kNS = (QT == 1 ? 5 : 4) * kNDQ;
-  static constexpr int kNA = 2 * kNDQ;
-  static constexpr int kND = QT == 1 ? 4 : 2;
+  static constexpr int kNS = 8;
+  static constexpr int kNA = 4;
+  static constexpr int kND = kNEpi;
   static constexpr int kACols = kHeadDim / 2;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kQBytes = kN * kHeadDim * 2;
@@ -232,69 +237,73 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
           last_ud = ud;
         }
       }
-    } else if (warp < 6) {
-      // ================= epilogue warpgroup =================
-      const int etid = tid - 64;         // 0 .. 127 = key within the block (TMEM lane)
-      const int wq = warp & 3;
+    } else if (warp < 2 + 4 * C::kNEpi) {
+      // ================= epilogue warpgroups =================
+      // Per block: the accumulator (rows x 16 heads, one key per thread) in two
+      // loads of half the rows each; the slot is released to the MMA as soon as
+      // the second load has landed, before the second half is reduced. Each
+      // row's weighted ReLU head sum runs as two interleaved chains, and the
+      // block maximum over the warp's 32 keys is one redux on order-preserving
+      // integer keys.
+      const int ep = (warp - 2) >> 2;            // warpgroup: blocks g with g % kNEpi == ep
+      const int etid = tid - 64 - 128 * ep;      // 0 .. 127 within the warpgroup
+      const int wq = warp & 3;                   // lane quarter: keys 32 wq .. 32 wq + 31
+      constexpr int kHalfRows = QT / 2;
       int rlen[QT];
 #pragma unroll
       for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
-      float wreg[QT == 1 ? 16 : 1];
-      if constexpr (QT == 1) {
-#pragma unroll
-        for (int h = 0; h < 16; ++h) wreg[h] = sm.wsm[h];
-      }
-      (void)wreg;
       PageWindow pw;
-      for (int j = 0; j < nseg; ++j) {
+      for (int j = ((ep - g0) % C::kNEpi + C::kNEpi) % C::kNEpi; j < nseg; j += C::kNEpi) {
         const int g = g0 + j, ds = g % C::kND, ud = g / C::kND;
         const int blk = seg_lo + j;
-        const int page = pw.get(bt_row + seg_lo, j, 1, nseg, lane);
+        const int page = pw.get(bt_row + seg_lo, j, C::kNEpi, nseg, lane);
         const bool ok = __all_sync(0xffffffffu, role_wait(sm, &sm.dfull[ds], ud & 1, a.err));
         tc_fence_after();
         const int tok = blk * kPage + (32 * wq + lane);
         const uint32_t d_tm = tmem + C::kNA * C::kACols + ds * C::kN;
-        // two rows of 16 head scores per tensor-memory load; the block maximum over
-        // the warp's 32 keys is one redux on order-preserving integer keys
+        float sc[QT];
 #pragma unroll
-        for (int rp = 0; rp < QT; rp += 2) {
-          if (!ok) break;
-          float d[32];
-          if constexpr (QT == 1) {
-            float h16[16];
-            tmem_ld16(lane_base + d_tm, h16);
+        for (int rho = 0; rho < QT; ++rho) sc[rho] = 0.f;
+        if (ok) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) d[i] = h16[i];
-          } else {
-            tmem_ld32(lane_base + d_tm + 16 * rp, d);
-          }
-          tmem_wait_ld();
+          for (int half = 0; half < 2; ++half) {
+            float d[16 * kHalfRows];
 #pragma unroll
-          for (int r = 0; r < 2 && rp + r < QT; ++r) {
-            const int rho = rp + r;
-            float sc = 0.f;
-            if constexpr (QT == 1) {
+            for (int c = 0; c < kHalfRows / 2; ++c)
+              tmem_ld32(lane_base + d_tm + 16 * kHalfRows * half + 32 * c,
+                        *reinterpret_cast<float(*)[32]>(&d[32 * c]));
+            tmem_wait_ld();
+            if (half == 1) {
+              tc_fence_before();
+              mbar_arrive(&sm.dempty[ds]);
+            }
 #pragma unroll
-              for (int h = 0; h < 16; ++h) sc = fmaf(wreg[h], fmaxf(d[h], 0.f), sc);
-            } else {
+            for (int r = 0; r < kHalfRows; ++r) {
+              const int rho = kHalfRows * half + r;
               const float4* w4 = reinterpret_cast<const float4*>(sm.wsm + 16 * rho);
+              float s0 = 0.f, s1 = 0.f;
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
                 const float4 wv = w4[q4];
-                sc = fmaf(wv.x, fmaxf(d[16 * r + 4 * q4 + 0], 0.f), sc);
-                sc = fmaf(wv.y, fmaxf(d[16 * r + 4 * q4 + 1], 0.f), sc);
-                sc = fmaf(wv.z, fmaxf(d[16 * r + 4 * q4 + 2], 0.f), sc);
-                sc = fmaf(wv.w, fmaxf(d[16 * r + 4 * q4 + 3], 0.f), sc);
+                s0 = fmaf(wv.x, fmaxf(d[16 * r + 4 * q4 + 0], 0.f), s0);
+                s1 = fmaf(wv.y, fmaxf(d[16 * r + 4 * q4 + 1], 0.f), s1);
+                s0 = fmaf(wv.z, fmaxf(d[16 * r + 4 * q4 + 2], 0.f), s0);
+                s1 = fmaf(wv.w, fmaxf(d[16 * r + 4 * q4 + 3], 0.f), s1);
               }
+              sc[rho] = s0 + s1;
             }
-            const uint32_t key = ordered_bits(tok < rlen[rho] ? sc : -INFINITY);
-            const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-            if (lane == 0) sm.blkmax[ds][wq][rho] = mx;
           }
+        } else {
+          tc_fence_before();
+          mbar_arrive(&sm.dempty[ds]);
         }
-        tc_fence_before();
-        mbar_arrive(&sm.dempty[ds]);
-        named_bar_sync(1, 128);
+#pragma unroll
+        for (int rho = 0; rho < QT; ++rho) {
+          const uint32_t key = ordered_bits(tok < rlen[rho] ? sc[rho] : -INFINITY);
+          const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+          if (lane == 0) sm.blkmax[ds][wq][rho] = mx;
+        }
+        named_bar_sync(1 + ep, 128);
         if (*reinterpret_cast<volatile int*>(&sm.abort)) break;  // uniform: read after the barrier
         if (etid < QT) {
           const int rho = etid;
@@ -312,7 +321,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
       }
     } else {
       // ================= dequantising warpgroups =================
-      const int dq = (warp - 6) >> 2;    // which warpgroup
+      const int dq = (warp - 2 - 4 * C::kNEpi) >> 2;    // which warpgroup
       const int key = tid & 127;         // TMEM lane = key within the block
       const int sw = (key >> 1) & 3;     // 64-byte swizzle of this key's row
       PageWindow pw;
