@@ -48,13 +48,20 @@ struct AttnArgs {
   int32_t* err;
 };
 
+// Per-warp partial outputs are stored at [head][dim + dim / 32] in rows of
+// kMergeRow floats: the 32 lanes of one store (8 heads x 4 dim groups of 32)
+// then fall in 32 different banks (bank = 4 head + dim / 32 + const).
+constexpr int kMergeRow = kHeadDim + 4;
+__device__ __forceinline__ int merge_at(int head, int dim) { return head * kMergeRow + dim + (dim >> 5); }
+
 struct __align__(16) AttnSmem {
   union {
     uint8_t stage[2][kBlockBytes];
     struct {
-      float o[kAttWarps][16][kHeadDim];
+      float o[kAttWarps][16 * kMergeRow];
       float m[kAttWarps][16];
       float l[kAttWarps][16];
+      float f[kAttWarps][16];   // exp2(m_warp - M) per warp and head
     } merge;
   };
   float cta_o[16][kHeadDim];  // this CTA's partial: sum p v, relative to cta_m (log2 units)
@@ -77,6 +84,11 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
+  if (tid == 0) {
+    mbar_init(&sm.bar[0], 1);
+    mbar_init(&sm.bar[1], 1);
+    mbar_fence_init();
+  }
   pdl_trigger();
   pdl_wait();
   // q fragments (A operand, heads as rows) in the permuted head-dim order:
@@ -100,22 +112,38 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     }
   }
 
-  // The block list of this split: warp 0 reads the ids, checks them, looks the
-  // pages up in parallel and compacts the valid ones.
+  // The block list of this split: warp 0 reads the ids (together with the row's
+  // request and length), checks them, looks the pages up in parallel and
+  // compacts the valid ones; the lane that finds block 0 or 1 starts its copy.
+  auto issue = [&](int i, int page) {
+    const int s = i & 1;
+    const size_t rec = static_cast<size_t>(page) * a.Hkv + kvh;
+    uint8_t* dst = sm.stage[s];
+    fence_proxy_async();
+    mbar_expect_tx(&sm.bar[s], kBlockBytes);
+    bulk_g2s(dst, a.kc + rec * kPageCodeBytes, kPageCodeBytes, &sm.bar[s]);
+    bulk_g2s(dst + kPageCodeBytes, a.ks + rec * kPageScaleBytes, kPageScaleBytes, &sm.bar[s]);
+    bulk_g2s(dst + kPageCodeBytes + kPageScaleBytes, a.vc + rec * kPageCodeBytes, kPageCodeBytes,
+             &sm.bar[s]);
+    bulk_g2s(dst + 2 * kPageCodeBytes + kPageScaleBytes, a.vs + rec * kPageScaleBytes,
+             kPageScaleBytes, &sm.bar[s]);
+  };
   if (warp == 0) {
+    __syncwarp();   // the barriers lane 0 initialised
+    const int i0 = split * a.ips, i1 = min(a.topk, i0 + a.ips);
+    const int id_first = i0 + lane < i1 ? a.ids[static_cast<size_t>(r) * a.topk + i0 + lane] : -1;
     const int len = a.row_len[r];
     const int req = a.row_req[r];
     const bool row_ok = req >= 0 && len > 0;
     const bool row_bad = row_ok && (req >= a.B || len > a.bt_stride * kPage);
     if (row_bad && lane == 0 && split == 0 && kvh == 0) raise(a.err, M3S_DEVERR_ROW);
     const int nb = (len + kPage - 1) / kPage;
-    const int i0 = split * a.ips, i1 = min(a.topk, i0 + a.ips);
     int n = 0;
     for (int base = i0; base < i1; base += 32) {
       const int i = base + lane;
       int page = -1, ntok = 0;
       if (row_ok && !row_bad && i < i1) {
-        const int id = a.ids[static_cast<size_t>(r) * a.topk + i];
+        const int id = base == i0 ? id_first : a.ids[static_cast<size_t>(r) * a.topk + i];
         if (id >= 0) {
           if (id >= nb || id >= a.bt_stride) {
             if (kvh == 0) raise(a.err, M3S_DEVERR_BLOCK_ID);
@@ -135,37 +163,16 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
         const int at = n + __popc(keep & ((1u << lane) - 1u));
         sm.page[at] = page;
         sm.ntok[at] = ntok;
+        if (at < 2) issue(at, page);
       }
       n += __popc(keep);
     }
-    if (lane == 0) {
-      sm.nblocks = n;
-      mbar_init(&sm.bar[0], 1);
-      mbar_init(&sm.bar[1], 1);
-      mbar_fence_init();
-    }
+    if (lane == 0) sm.nblocks = n;
   }
   if (qbad) raise(a.err, M3S_DEVERR_QRANGE);
   __syncthreads();
   const int nblocks = sm.nblocks;
 
-  auto issue = [&](int i) {
-    const int s = i & 1;
-    const size_t rec = static_cast<size_t>(sm.page[i]) * a.Hkv + kvh;
-    uint8_t* dst = sm.stage[s];
-    fence_proxy_async();
-    mbar_expect_tx(&sm.bar[s], kBlockBytes);
-    bulk_g2s(dst, a.kc + rec * kPageCodeBytes, kPageCodeBytes, &sm.bar[s]);
-    bulk_g2s(dst + kPageCodeBytes, a.ks + rec * kPageScaleBytes, kPageScaleBytes, &sm.bar[s]);
-    bulk_g2s(dst + kPageCodeBytes + kPageScaleBytes, a.vc + rec * kPageCodeBytes, kPageCodeBytes,
-             &sm.bar[s]);
-    bulk_g2s(dst + 2 * kPageCodeBytes + kPageScaleBytes, a.vs + rec * kPageScaleBytes,
-             kPageScaleBytes, &sm.bar[s]);
-  };
-  if (tid == 0) {
-    if (nblocks > 0) issue(0);
-    if (nblocks > 1) issue(1);
-  }
 
   float o[16][4];
 #pragma unroll
@@ -296,7 +303,7 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       }
     }
     __syncthreads();  // every warp is done with stage s
-    if (tid == 0 && !aborted && i + 2 < nblocks) issue(i + 2);
+    if (tid == 0 && !aborted && i + 2 < nblocks) issue(i + 2, sm.page[i + 2]);
   }
 
   // ---- merge the four warps ----
@@ -320,31 +327,35 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       for (int e = 0; e < 4; ++e) {
         const int head = e < 2 ? g : g + 8;
         const int dim = 16 * (2 * t + (e & 1)) + 2 * jj + odd;
-        sm.merge.o[warp][head][dim] = o[2 * jj + odd][e];
+        sm.merge.o[warp][merge_at(head, dim)] = o[2 * jj + odd][e];
       }
   __syncthreads();
 
-  // this CTA's partial over its blocks: (M, L, O) per head, O relative to 2^M
+  // this CTA's partial over its blocks: (M, L, O) per head, O relative to 2^M;
+  // each warp's factor 2^(m_warp - M) once per head
   const int G = a.G;
-  for (int e = tid; e < 16 * kHeadDim; e += kAttThreads) {
-    const int head = e / kHeadDim, dim = e % kHeadDim;
+  if (tid < 16) {
+    const int head = tid;
     float M = -INFINITY;
 #pragma unroll
     for (int wv = 0; wv < kAttWarps; ++wv) M = fmaxf(M, sm.merge.m[wv][head]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+    float L = 0.f;
 #pragma unroll
-      for (int wv = 0; wv < kAttWarps; ++wv) {
-        const float f = exp2f(sm.merge.m[wv][head] - M);
-        L += f * sm.merge.l[wv][head];
-        O += f * sm.merge.o[wv][head][dim];
-      }
+    for (int wv = 0; wv < kAttWarps; ++wv) {
+      const float f = M == -INFINITY ? 0.f : exp2f(sm.merge.m[wv][head] - M);
+      sm.merge.f[wv][head] = f;
+      L += f * sm.merge.l[wv][head];
     }
+    sm.cta_m[head] = M;
+    sm.cta_l[head] = L;
+  }
+  __syncthreads();
+  for (int head = 0; head < 16; ++head) {
+    const int dim = tid;   // kAttThreads == kHeadDim
+    float O = 0.f;
+#pragma unroll
+    for (int wv = 0; wv < kAttWarps; ++wv) O += sm.merge.f[wv][head] * sm.merge.o[wv][merge_at(head, dim)];
     sm.cta_o[head][dim] = O;
-    if (dim == 0) {
-      sm.cta_m[head] = M;
-      sm.cta_l[head] = L;
-    }
   }
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();

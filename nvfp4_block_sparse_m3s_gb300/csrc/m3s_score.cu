@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
               tmem_ld32(lane_base + d_tm + 16 * kHalfRows * half + 32 * c,
                         *reinterpret_cast<float(*)[32]>(&d[32 * c]));
             tmem_wait_ld();
+            reg_fence(d);
             if (half == 1) {
               tc_fence_before();
               mbar_arrive(&sm.dempty[ds]);
