@@ -35,6 +35,8 @@ design notes of this repository):
     |x|/s (not x*(1/s)), ties to the even code, sign = IEEE sign bit of x;
   - a block whose scale rounds to 0 stores all-zero code bytes;
   - byte i of the payload holds element 2i in its low nibble, 2i+1 high;
+  - forced blocks (init / local) rank above every scored block, init
+    above local; init blocks lower id first, local blocks most recent first;
   - top-k ties break to the lower block id; the ids are returned sorted
     ascending and padded with -1;
   - sm_scale is an argument (the workloads pass 1/sqrt(128)).
@@ -277,13 +279,28 @@ def block_max(score: np.ndarray, L: int) -> np.ndarray:
     return out
 
 
-def topk_ids(bscore: np.ndarray, k: int) -> np.ndarray:
+def topk_ids(bscore: np.ndarray, k: int, init_blocks: int = 0, local_blocks: int = 0) -> np.ndarray:
     """The k best blocks (higher score first, the lower id on equal scores).
+
+    Forced blocks -- #2744's review of the fused verify top-k and vllm #64198,
+    Design (the init / local sentinels 1e30 and 1e29 written before the
+    top-k): the first ``init_blocks`` blocks and the last ``local_blocks``
+    blocks of the row rank above every scored block, init above local. Init
+    blocks rank lower id first; local blocks rank most recent (higher id)
+    first, so that when init + local exceeds k the row's newest blocks -- its
+    current token's block among them -- are the ones kept (the review's
+    correction of the fused path). A block that is both counts as init.
 
     Returned sorted by ascending id, padded with -1 when there are fewer than k blocks.
     """
     nb = len(bscore)
-    order = np.lexsort((np.arange(nb), -np.asarray(bscore, dtype=np.float64)))
+    ids = np.arange(nb)
+    init = ids < init_blocks
+    local = (ids >= nb - local_blocks) & ~init
+    cls = np.where(init, 2, np.where(local, 1, 0))
+    within = np.where(init, ids.astype(np.float64),
+                      np.where(local, -ids.astype(np.float64), -np.asarray(bscore, dtype=np.float64)))
+    order = np.lexsort((ids, within, -cls))     # class, then the in-class order, then lower id
     sel = np.sort(order[: min(k, nb)])
     out = np.full(k, -1, dtype=np.int32)
     out[: len(sel)] = sel
@@ -292,7 +309,8 @@ def topk_ids(bscore: np.ndarray, k: int) -> np.ndarray:
 
 def index_score_topk(q_idx: np.ndarray, w: np.ndarray, idx_codes: np.ndarray,
                      idx_scales: np.ndarray, block_table: np.ndarray, row_req: np.ndarray,
-                     row_len: np.ndarray, topk: int, rows=None):
+                     row_len: np.ndarray, topk: int, rows=None, init_blocks: int = 0,
+                     local_blocks: int = 0):
     """Per query row: index scores over its causal keys, block maxima, top-k block ids.
 
     Returns (topk_ids int32 [R, topk], block_scores list of float64 arrays
@@ -321,17 +339,17 @@ def index_score_topk(q_idx: np.ndarray, w: np.ndarray, idx_codes: np.ndarray,
         k_hat = cache[key][:L]
         sc = token_scores(q_idx[r], w[r], k_hat)
         bscores[r] = block_max(sc, L)
-        out[r] = topk_ids(bscores[r], topk)
+        out[r] = topk_ids(bscores[r], topk, init_blocks, local_blocks)
     return out, bscores, err
 
 
 def verify_score_topk(q_idx, w, idx_codes, idx_scales, block_table, cu_q, seq_len, R, topk,
-                      rows=None):
+                      rows=None, init_blocks: int = 0, local_blocks: int = 0):
     """Fused verify score + top-k: the same selection as the row map followed by
     score + top-k (the fused kernel only changes how the work is grouped)."""
     row_req, row_len = decode_rows(cu_q, seq_len, R)
     ids, _, err = index_score_topk(q_idx, w, idx_codes, idx_scales, block_table, row_req,
-                                   row_len, topk, rows)
+                                   row_len, topk, rows, init_blocks, local_blocks)
     return ids, err
 
 

@@ -365,3 +365,63 @@ def test_verify_equals_rowmap_plus_score_topk():
     assert err == 0 and np.array_equal(ids_v, ids_u)
     # row j of a request sees one more token than row j-1
     assert list(rl[3:11]) == [1500 - 8 + j + 1 for j in range(8)]
+
+
+# ---------------------------------------------------------------------------
+# Forced init / local blocks in the top-k
+# ---------------------------------------------------------------------------
+
+def _forced_rank_restatement(scores, k, init, local):
+    """Independent restatement: every block gets a tuple whose maximum ranks first."""
+    nb = len(scores)
+    ranked = []
+    for b in range(nb):
+        if b < init:
+            ranked.append(((2, -b, 0.0, 0), b))
+        elif b >= nb - local:
+            ranked.append(((1, b, 0.0, 0), b))
+        else:
+            ranked.append(((0, 0, float(scores[b]), -b), b))
+    ranked.sort(reverse=True)
+    return sorted(b for _, b in ranked[: min(k, nb)])
+
+
+def test_forced_blocks_reviews_worked_example():
+    """#2744 review: topk 16, init 4, local 16 on a long row. The ids kept are the
+    four init blocks and the twelve newest blocks, the current token's block
+    (the last) among them; not the four init blocks plus local n-16 .. n-5."""
+    nb = 100
+    scores = np.linspace(5.0, -5.0, nb)              # scores alone would pick blocks 0 .. 15
+    got = O.topk_ids(scores, 16, init_blocks=4, local_blocks=16)
+    assert got.tolist() == [0, 1, 2, 3] + list(range(88, 100))
+
+
+def test_forced_blocks_special_cases():
+    rng = np.random.default_rng(5)
+    sc = rng.standard_normal(40)
+    # no forced blocks: the plain top-k
+    assert np.array_equal(O.topk_ids(sc, 8, 0, 0), O.topk_ids(sc, 8))
+    # forced blocks that fit are all kept; the rest are the best scored blocks
+    got = set(O.topk_ids(sc, 8, 2, 3).tolist())
+    assert {0, 1, 37, 38, 39} <= got
+    rest = sorted(range(2, 37), key=lambda b: (-sc[b], b))[:3]
+    assert got == {0, 1, 37, 38, 39} | set(rest)
+    # init blocks alone filling k: exactly the first k blocks
+    assert O.topk_ids(sc, 8, 10, 5).tolist() == list(range(8))
+    # a row no longer than k: every block, whatever is forced
+    assert O.topk_ids(sc[:5], 8, 2, 2).tolist() == [0, 1, 2, 3, 4, -1, -1, -1]
+    # init and local overlapping on a short row: the block counts once, as init
+    assert O.topk_ids(sc[:12], 4, 3, 10).tolist() == [0, 1, 2, 11]
+
+
+def test_forced_blocks_against_restatement():
+    rng = np.random.default_rng(6)
+    for _ in range(300):
+        nb = int(rng.integers(1, 60))
+        k = int(rng.integers(1, 20))
+        init, local = int(rng.integers(0, 8)), int(rng.integers(0, 24))
+        sc = np.round(rng.standard_normal(nb), 1)   # ties
+        got = O.topk_ids(sc, k, init, local)
+        exp = _forced_rank_restatement(sc, k, init, local)
+        cnt = min(k, nb)
+        assert got[:cnt].tolist() == exp and (got[cnt:] == -1).all()
