@@ -158,6 +158,13 @@ int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int3
  *   block_score[blk] = max of score over the block's causal tokens,
  *   topk_ids[r] = the topk blocks with the highest block score, the lower id
  *                 on equal scores, sorted ascending, padded with -1.
+ * Forced blocks (#2744's review of the fused verify top-k; "MXFP4 KV cache
+ * for MiniMax-M3.1 on gfx950" (vllm #64198), Design: the init / local
+ * sentinels): the first init_blocks and the last local_blocks blocks of each
+ * row rank above every scored block, init above local; init blocks lower id
+ * first, local blocks most recent first (so init + local > topk keeps the
+ * row's newest blocks, its current token's block among them). 0, 0 = none;
+ * negative counts are M3S_ERR_INVALID.
  *   q_idx BF16 [R][Hi][128], w fp32 [R][Hi], Hi <= 16,
  *   idx_k.num_heads == 1, block_table int32 [B][bt_stride] (logical block ->
  *   physical page), row_req / row_len from m3s_decode_rows,
@@ -170,8 +177,9 @@ int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int3
 int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                          m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
                          const int32_t* row_req, const int32_t* row_len, int32_t R, int32_t B,
-                         int32_t topk, int32_t* topk_ids, float* block_scores, void* ws,
-                         size_t ws_bytes, int32_t* err, void* stream);
+                         int32_t topk, int32_t init_blocks, int32_t local_blocks,
+                         int32_t* topk_ids, float* block_scores, void* ws, size_t ws_bytes,
+                         int32_t* err, void* stream);
 
 /*
  * The two halves of m3s_index_score_topk, for callers that want the block
@@ -180,8 +188,8 @@ int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
  * bt_stride) receives, for every valid row, the block score of each of its
  * ceil(row_len/128) blocks; other entries are left as is.
  * m3s_block_topk: topk_ids [R][topk] from those scores (ties to the lower id,
- * ascending, -1 padded); row_req may be NULL (then rows are taken as valid
- * when 0 < row_len <= bt_stride*128 and B > 0).
+ * ascending, -1 padded, forced blocks as above); row_req may be NULL (then
+ * rows are taken as valid when 0 < row_len <= bt_stride*128 and B > 0).
  */
 int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int32_t Hi,
                            m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
@@ -189,13 +197,14 @@ int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int32_t Hi,
                            float* block_scores, int32_t bs_stride, int32_t* err, void* stream);
 int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* row_req,
                    const int32_t* row_len, int32_t R, int32_t B, int32_t bt_stride, int32_t topk,
-                   int32_t* topk_ids, void* stream);
+                   int32_t init_blocks, int32_t local_blocks, int32_t* topk_ids, void* stream);
 
 /*
  * m3s_index_score_topk without a caller workspace. The pages have no
  * counterpart to this call; it is an integration variant of
- * m3s_index_score_topk (same arguments minus block_scores / ws / ws_bytes,
- * same result) for callers that cannot allocate device memory at call time:
+ * m3s_index_score_topk (same arguments minus block_scores / ws / ws_bytes and
+ * without forced blocks, the same result as that call with init_blocks =
+ * local_blocks = 0) for callers that cannot allocate device memory at call time:
  * a C host that links only this library and owns no device allocator, or an
  * engine plugin whose device memory is budgeted once at start-up.
  * The block-score scratch is a file-scope device array of
@@ -230,8 +239,9 @@ int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t H
 int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                           m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
                           const int32_t* cu_q, const int32_t* row_len, int32_t B, int32_t R,
-                          int32_t max_q, int32_t topk, int32_t* topk_ids, void* ws,
-                          size_t ws_bytes, int32_t* err, void* stream);
+                          int32_t max_q, int32_t topk, int32_t init_blocks, int32_t local_blocks,
+                          int32_t* topk_ids, void* ws, size_t ws_bytes, int32_t* err,
+                          void* stream);
 
 /*
  * Block-sparse attention over the selected NVFP4 pages. "NVFP4 sparse KV",

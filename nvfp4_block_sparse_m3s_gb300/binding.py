@@ -53,14 +53,15 @@ _SIGS = {
     "m3s_nvfp4_store_batch": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "m3s_decode_rows": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
     "m3s_index_score_topk": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
-                                            _I32, _P, _P, _P, _SZ, _P, _P]),
+                                            _I32, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
     "m3s_index_score_topk_static": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32,
                                                    _I32, _I32, _P, _P, _P]),
     "m3s_index_block_scores": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
                                               _P, _I32, _P, _P]),
-    "m3s_block_topk": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _I32, _I32, _P, _P]),
+    "m3s_block_topk": (ctypes.c_int, [_P, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P,
+                                      _P]),
     "m3s_verify_score_topk": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
-                                             _I32, _I32, _P, _P, _SZ, _P, _P]),
+                                             _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "m3s_sparse_attention": (ctypes.c_int, [_P, _I32, _I32, Plane, Plane, _P, _I32, _I32, _P, _P,
                                             _P, _I32, _I32, _F32, _P, _P, _P, _SZ, _P, _P]),
     "m3s_version": (ctypes.c_char_p, []),
@@ -163,7 +164,8 @@ def m3s_decode_rows(cu_q: torch.Tensor, seq_len: torch.Tensor, R: int,
 
 
 def m3s_index_score_topk(q_idx, w, codes, scales, block_table, row_req, row_len, topk: int,
-                         topk_ids=None, block_scores=None, ws=None, err=None, stream=None):
+                         topk_ids=None, block_scores=None, ws=None, err=None, stream=None,
+                         init_blocks: int = 0, local_blocks: int = 0):
     R, Hi = q_idx.shape[0], q_idx.shape[1]
     B, bt_stride = block_table.shape
     if topk_ids is None:
@@ -173,8 +175,9 @@ def m3s_index_score_topk(q_idx, w, codes, scales, block_table, row_req, row_len,
         ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
     rc = load().m3s_index_score_topk(
         _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride,
-        _ptr(row_req), _ptr(row_len), R, B, topk, _ptr(topk_ids), _ptr(block_scores), _ptr(ws),
-        0 if ws is None else ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
+        _ptr(row_req), _ptr(row_len), R, B, topk, init_blocks, local_blocks, _ptr(topk_ids),
+        _ptr(block_scores), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        _ptr(err), _stream(stream))
     _check(rc, "m3s_index_score_topk")
     return topk_ids
 
@@ -205,19 +208,20 @@ def m3s_index_block_scores(q_idx, w, codes, scales, block_table, row_req, row_le
 
 
 def m3s_block_topk(block_scores, row_req, row_len, B: int, bt_stride: int, topk: int,
-                   topk_ids=None, stream=None):
+                   topk_ids=None, stream=None, init_blocks: int = 0, local_blocks: int = 0):
     R = row_len.shape[0]
     if topk_ids is None:
         topk_ids = torch.empty((R, topk), dtype=torch.int32, device=row_len.device)
     rc = load().m3s_block_topk(_ptr(block_scores), block_scores.shape[1], _ptr(row_req),
-                               _ptr(row_len), R, B, bt_stride, topk, _ptr(topk_ids),
-                               _stream(stream))
+                               _ptr(row_len), R, B, bt_stride, topk, init_blocks, local_blocks,
+                               _ptr(topk_ids), _stream(stream))
     _check(rc, "m3s_block_topk")
     return topk_ids
 
 
 def m3s_verify_score_topk(q_idx, w, codes, scales, block_table, cu_q, row_len, max_q: int,
-                          topk: int, topk_ids=None, ws=None, err=None, stream=None):
+                          topk: int, topk_ids=None, ws=None, err=None, stream=None,
+                          init_blocks: int = 0, local_blocks: int = 0):
     R, Hi = q_idx.shape[0], q_idx.shape[1]
     B, bt_stride = block_table.shape
     if topk_ids is None:
@@ -227,8 +231,8 @@ def m3s_verify_score_topk(q_idx, w, codes, scales, block_table, cu_q, row_len, m
         ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
     rc = load().m3s_verify_score_topk(
         _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride, _ptr(cu_q),
-        _ptr(row_len), B, R, max_q, topk, _ptr(topk_ids), _ptr(ws), ws.numel() * ws.element_size(),
-        _ptr(err), _stream(stream))
+        _ptr(row_len), B, R, max_q, topk, init_blocks, local_blocks, _ptr(topk_ids), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
     _check(rc, "m3s_verify_score_topk")
     return topk_ids
 

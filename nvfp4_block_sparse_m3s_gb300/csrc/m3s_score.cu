@@ -390,15 +390,26 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
 // are exactly the ones still needed (at the latest on the last byte).
 constexpr int kTopkThreads = 1024;
 
+// Forced blocks (the first init blocks and the last local blocks of the row)
+// rank above every score: their keys' high words, 0xFFFFFFFF (init) and
+// 0xFFFFFFFE (local), sit above ordered_bits(+inf). Init keys keep the
+// complemented id (lower id first), local keys the id itself (most recent
+// first), so init + local beyond k keeps the row's newest blocks.
+__device__ __forceinline__ unsigned long long block_key(const float* row, int i, int nb, int init, int local) {
+  if (i < init) return (0xFFFFFFFFull << 32) | static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(i));
+  if (i >= nb - local) return (0xFFFFFFFEull << 32) | static_cast<unsigned long long>(static_cast<uint32_t>(i));
+  return topk_key(row[i], i);
+}
+
 __device__ __forceinline__ unsigned long long topk_key_at(const float* row, const unsigned long long* keys,
-                                                        bool in_smem, int i) {
-  return in_smem ? keys[i] : topk_key(row[i], i);
+                                                        bool in_smem, int i, int nb, int init, int local) {
+  return in_smem ? keys[i] : block_key(row, i, nb, init, local);
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const float* __restrict__ bscores, int bs_stride, const int32_t* __restrict__ row_req,
-    const int32_t* __restrict__ row_len, int B, int bt_stride, int topk, int smem_keys,
-    int32_t* __restrict__ ids) {
+    const int32_t* __restrict__ row_len, int B, int bt_stride, int topk, int init_blocks,
+    int local_blocks, int smem_keys, int32_t* __restrict__ ids) {
   extern __shared__ unsigned long long keys[];
   __shared__ unsigned int hist[256];
   __shared__ unsigned long long wmax[kTopkThreads / 32], wmin[kTopkThreads / 32];
@@ -424,7 +435,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   const bool in_smem = nb <= smem_keys;
   unsigned long long kmax = 0, kmin = ~0ull;
   for (int i = tid; i < nb; i += kTopkThreads) {
-    const unsigned long long key = topk_key(row[i], i);
+    const unsigned long long key = block_key(row, i, nb, init_blocks, local_blocks);
     if (in_smem) keys[i] = key;
     kmax = key > kmax ? key : kmax;
     kmin = key < kmin ? key : kmin;
@@ -463,7 +474,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
     const int krem = sh_krem;
     __syncthreads();
     for (int i = tid; i < nb; i += kTopkThreads) {
-      const unsigned long long key = topk_key_at(row, keys, in_smem, i);
+      const unsigned long long key = topk_key_at(row, keys, in_smem, i, nb, init_blocks, local_blocks);
       if ((key & mask) == prefix) atomicAdd(&hist[static_cast<unsigned>(key >> shift) & 255u], 1u);
     }
     __syncthreads();
@@ -496,7 +507,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   }
   const unsigned long long prefix = sh_prefix, mask = sh_mask;
   for (int i = tid; i < nb; i += kTopkThreads) {
-    const unsigned long long key = topk_key_at(row, keys, in_smem, i);
+    const unsigned long long key = topk_key_at(row, keys, in_smem, i, nb, init_blocks, local_blocks);
     if ((key & mask) >= prefix) {
       const int slot = atomicAdd(&nsel, 1);
       if (slot < M3S_MAX_TOPK) sel[slot] = i;
@@ -570,14 +581,16 @@ int launch_score(const ScoreArgs& a, cudaStream_t st) {
 }
 
 int launch_topk(const float* bscores, int bs_stride, const int32_t* row_req, const int32_t* row_len,
-                int R, int B, int bt_stride, int topk, int32_t* ids, cudaStream_t st) {
+                int R, int B, int bt_stride, int topk, int init_blocks, int local_blocks, int32_t* ids,
+                cudaStream_t st) {
   int keys = 0;
   const size_t smem = topk_smem(bt_stride, &keys);
   if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
   return launch_kernel(topk_kernel, dim3(R), dim3(kTopkThreads), smem, st, 0, bscores, bs_stride,
-                       row_req, row_len, B, bt_stride, topk, keys, ids) == cudaSuccess
+                       row_req, row_len, B, bt_stride, topk, init_blocks, local_blocks, keys, ids) ==
+                 cudaSuccess
              ? M3S_OK
              : M3S_ERR_LAUNCH;
 }
@@ -620,26 +633,30 @@ extern "C" int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int
 
 extern "C" int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* row_req,
                               const int32_t* row_len, int32_t R, int32_t B, int32_t bt_stride,
-                              int32_t topk, int32_t* topk_ids, void* stream) {
+                              int32_t topk, int32_t init_blocks, int32_t local_blocks,
+                              int32_t* topk_ids, void* stream) {
   using namespace m3s;
   if (R < 0 || B < 0 || topk < 0 || bt_stride < 0 || bs_stride < bt_stride) return M3S_ERR_INVALID;
+  if (init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
   if (topk > M3S_MAX_TOPK) return M3S_ERR_UNSUPPORTED;
   if (R == 0 || topk == 0) return M3S_OK;
   if (!row_len || !topk_ids || (B > 0 && !block_scores)) return M3S_ERR_INVALID;
   return launch_topk(block_scores, bs_stride > 0 ? bs_stride : 1, row_req, row_len, R, B,
-                     bt_stride, topk, topk_ids, static_cast<cudaStream_t>(stream));
+                     bt_stride, topk, init_blocks, local_blocks, topk_ids,
+                     static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                                     m3s_nvfp4_plane idx_k, const int32_t* block_table,
                                     int32_t bt_stride, const int32_t* row_req,
                                     const int32_t* row_len, int32_t R, int32_t B, int32_t topk,
-                                    int32_t* topk_ids, float* block_scores, void* ws,
-                                    size_t ws_bytes, int32_t* err, void* stream) {
+                                    int32_t init_blocks, int32_t local_blocks, int32_t* topk_ids,
+                                    float* block_scores, void* ws, size_t ws_bytes, int32_t* err,
+                                    void* stream) {
   using namespace m3s;
   int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk_ids);
   if (rc != M3S_OK || R == 0) return rc;
-  if (!row_req || !row_len) return M3S_ERR_INVALID;
+  if (!row_req || !row_len || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
   if (R > kMaxTiles) return M3S_ERR_UNSUPPORTED;
   if (topk == 0) return M3S_OK;
   const int stride = bt_stride > 0 ? bt_stride : 1;
@@ -657,23 +674,25 @@ extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32
     rc = launch_score_decode(a, st);
     if (rc != M3S_OK) return rc;
   }
-  return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, topk_ids, st);
+  return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, init_blocks, local_blocks,
+                     topk_ids, st);
 }
 
 extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                                      m3s_nvfp4_plane idx_k, const int32_t* block_table,
                                      int32_t bt_stride, const int32_t* cu_q,
                                      const int32_t* row_len, int32_t B, int32_t R, int32_t max_q,
-                                     int32_t topk, int32_t* topk_ids, void* ws, size_t ws_bytes,
-                                     int32_t* err, void* stream) {
+                                     int32_t topk, int32_t init_blocks, int32_t local_blocks,
+                                     int32_t* topk_ids, void* ws, size_t ws_bytes, int32_t* err,
+                                     void* stream) {
   using namespace m3s;
   int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk_ids);
   if (rc != M3S_OK || R == 0) return rc;
-  if (!cu_q || !row_len || max_q < 0) return M3S_ERR_INVALID;
+  if (!cu_q || !row_len || max_q < 0 || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
   if (topk == 0 || B == 0) {
     if (topk > 0) {
       // no requests: every row is padding
-      return launch_topk(nullptr, 1, nullptr, row_len, R, 0, bt_stride, topk, topk_ids,
+      return launch_topk(nullptr, 1, nullptr, row_len, R, 0, bt_stride, topk, 0, 0, topk_ids,
                          static_cast<cudaStream_t>(stream));
     }
     return M3S_OK;
@@ -690,7 +709,8 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   rc = launch_score<8>(a, st);
   if (rc != M3S_OK) return rc;
-  return launch_topk(bs, bt_stride, nullptr, row_len, R, B, bt_stride, topk, topk_ids, st);
+  return launch_topk(bs, bt_stride, nullptr, row_len, R, B, bt_stride, topk, init_blocks,
+                     local_blocks, topk_ids, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -766,5 +786,5 @@ extern "C" int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w
     rc = launch_score_decode(a, st);
     if (rc != M3S_OK) return rc;
   }
-  return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, topk_ids, st);
+  return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, 0, 0, topk_ids, st);
 }

@@ -159,3 +159,36 @@ def attention_rel_err(out: np.ndarray, ref: np.ndarray, rows) -> float:
 
 def bf16_np(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
+
+
+def check_topk_forced(gpu_ids: np.ndarray, ref_scores: list, topk: int, rows, init_blocks: int,
+                      local_blocks: int) -> None:
+    """Top-k with forced blocks: the forced part of the selection must be exactly
+    the oracle's; the rest comes from the scored blocks under the tie-band rule."""
+    for r in rows:
+        sc = np.asarray(ref_scores[r], dtype=np.float64)
+        nb = len(sc)
+        cnt = min(topk, nb)
+        ids = gpu_ids[r]
+        assert (ids[cnt:] == -1).all(), (r, ids)
+        sel = ids[:cnt]
+        assert (np.diff(sel) > 0).all(), f"row {r}: ids not strictly ascending {sel}"
+        blocks = np.arange(nb)
+        forced = (blocks < init_blocks) | (blocks >= nb - local_blocks)
+        # which forced blocks are kept does not depend on the scores at all
+        kept_forced = set(O.topk_ids(np.zeros(nb), topk, init_blocks, local_blocks)[:cnt].tolist()) & \
+            set(np.nonzero(forced)[0].tolist())
+        assert set(sel.tolist()) & set(np.nonzero(forced)[0].tolist()) == kept_forced, (r, sel)
+        # the scored remainder: the best of the unforced blocks, ties inside the band
+        free = np.nonzero(~forced)[0]
+        kk = cnt - len(kept_forced)
+        rest = np.array(sorted(set(sel.tolist()) - kept_forced), dtype=np.int64)
+        assert len(rest) == kk, (r, sel)
+        if kk == 0:
+            continue
+        sub = sc[free]
+        pos = {int(b): j for j, b in enumerate(free)}
+        sub_ids = np.array([pos[int(b)] for b in rest], dtype=np.int32)
+        fake = np.full((1, kk), -1, dtype=np.int32)
+        fake[0, :] = np.sort(sub_ids)
+        check_topk(fake, [sub], kk, [0])

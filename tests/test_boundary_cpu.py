@@ -62,10 +62,14 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.m3s_decode_rows(None, None, 1, 0, None, None, None) == M.OK
     assert lib.m3s_decode_rows(None, None, -1, 4, None, None, None) == M.ERR_INVALID
     # too many index heads / top-k beyond the build
-    assert lib.m3s_index_score_topk(None, None, 17, P, None, 1, None, None, 1, 1, 8, None, None,
-                                    None, 0, None, None) == M.ERR_UNSUPPORTED
-    assert lib.m3s_index_score_topk(None, None, 16, P, None, 1, None, None, 1, 1, 65, None, None,
-                                    None, 0, None, None) == M.ERR_UNSUPPORTED
+    assert lib.m3s_index_score_topk(None, None, 17, P, None, 1, None, None, 1, 1, 8, 0, 0, None,
+                                    None, None, 0, None, None) == M.ERR_UNSUPPORTED
+    assert lib.m3s_index_score_topk(None, None, 16, P, None, 1, None, None, 1, 1, 65, 0, 0, None,
+                                    None, None, 0, None, None) == M.ERR_UNSUPPORTED
+    # forced block counts must not be negative
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.m3s_block_topk(fake, 8, fake, fake, 1, 1, 8, 4, -1, 0, fake, None) == M.ERR_INVALID
+    assert lib.m3s_block_topk(fake, 8, fake, fake, 1, 1, 8, 4, 0, -2, fake, None) == M.ERR_INVALID
     # attention: q heads not a multiple of KV heads, GQA beyond 16
     P2 = M.Plane(None, None, 4, 1)
     assert lib.m3s_sparse_attention(None, 6, 4, P2, P2, None, 1, 1, None, None, None, 16, 1,

@@ -342,3 +342,69 @@ def test_many_short_rows_cross_tile_ranges(lib, fused):
         gbs = bscores.cpu().numpy()
         check_block_scores(gbs, ref_bs, range(R))
     check_topk(ids.cpu().numpy(), ref_bs, s.topk, range(R), gbs)
+
+
+def test_block_topk_forced_blocks_direct(lib):
+    """m3s_block_topk with forced init / local blocks == the oracle exactly, on
+    every selection path, including init + local beyond k."""
+    rng = np.random.default_rng(12)
+    widths = [3, 16, 40, 300, 3600, 10000, 20000]
+    bt_stride = max(widths)
+    R = len(widths)
+    scores = np.full((R, bt_stride), np.nan, dtype=np.float32)
+    lens = np.zeros(R, dtype=np.int32)
+    for r, nb in enumerate(widths):
+        lens[r] = nb * 128 - int(rng.integers(0, 128))
+        scores[r, :nb] = np.round(rng.standard_normal(nb), 1)     # ties
+    for topk, init, local in ((16, 0, 0), (16, 2, 3), (16, 4, 16), (8, 10, 2), (64, 1, 64)):
+        ids = M.m3s_block_topk(torch.from_numpy(scores).cuda(), None, i32(lens), 1, bt_stride, topk,
+                               init_blocks=init, local_blocks=local)
+        torch.cuda.synchronize()
+        got = ids.cpu().numpy()
+        for r in range(R):
+            nb = (int(lens[r]) + 127) // 128
+            exp = O.topk_ids(scores[r, :nb].astype(np.float64), topk, init, local)
+            assert np.array_equal(got[r], exp), (topk, init, local, r, got[r], exp)
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["index", "verify"])
+@pytest.mark.parametrize("init,local", [(2, 3), (4, 16)], ids=["fit", "over_k"])
+def test_step_with_forced_blocks(lib, fused, init, local):
+    """Score + top-k with forced blocks through both paths against the oracle:
+    forced blocks exact (with 4 + 16 > k = 16, the row's newest blocks are the
+    ones kept), the rest by score; attention over the selection."""
+    from step_helpers import check_topk_forced
+    wl = W.make("verify", ctx=(6000, 1800, 300, 4500), q_rows=(3, 2, 1, 4) if fused else (1, 1, 1, 1))
+    s = wl.spec
+    dev = DeviceCache(wl)
+    dev.store_all()
+    R = s.rows
+    row_req, row_len = M.m3s_decode_rows(dev.cu_q, dev.seq_len, R)
+    if fused:
+        ids = M.m3s_verify_score_topk(dev.q_idx, dev.w, dev.ic, dev.is_, dev.block_table, dev.cu_q,
+                                      row_len, max(s.q_rows), s.topk, err=dev.err,
+                                      init_blocks=init, local_blocks=local)
+    else:
+        ids = M.m3s_index_score_topk(dev.q_idx, dev.w, dev.ic, dev.is_, dev.block_table, row_req,
+                                     row_len, s.topk, err=dev.err, init_blocks=init,
+                                     local_blocks=local)
+    lse = torch.empty((R, s.hq), dtype=torch.float32, device="cuda")
+    out = M.m3s_sparse_attention(dev.q, s.hkv, dev.kc, dev.ks, dev.vc, dev.vs, dev.block_table,
+                                 row_req, row_len, ids, SM_SCALE, lse=lse, err=dev.err)
+    torch.cuda.synchronize()
+    assert int(dev.err.item()) == 0
+    ref = OracleCache(wl)
+    rr, rl = O.decode_rows(wl.cu_q, wl.seq_len, R)
+    _, ref_bs, _ = O.index_score_topk(wl.q_idx, wl.w, ref.ic, ref.is_, wl.block_table, rr, rl,
+                                      s.topk)
+    gids = ids.cpu().numpy()
+    check_topk_forced(gids, ref_bs, s.topk, range(R), init, local)
+    if (init, local) == (4, 16):
+        for r in range(R):
+            nb = (int(rl[r]) + 127) // 128
+            if nb > s.topk:
+                assert gids[r][-1] == nb - 1      # the current token's block is kept
+    o_ref, _, err = O.sparse_attention(wl.q, s.hkv, ref.kc, ref.ks, ref.vc, ref.vs,
+                                       wl.block_table, rr, rl, gids, SM_SCALE)
+    assert err == 0
+    assert attention_rel_err(bf16_np(out), o_ref, range(R)) <= ATTN_RTOL
