@@ -76,39 +76,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     const int seg_hi = min(hi, pre[tile + 1]) - pre[tile];
     const TileInfo<1> ti = tile_info<1>(a, tile, false);
 
-    // ---- the row's queries (fp16, fragment order), weights and length ----
-    __syncthreads();
-    for (int e = tid; e < kQFragWords; e += kThreads) {
-      const int ln = e & 31, c = (e >> 5) & 1, j = e >> 6;
-      const int h = 8 * c + (ln >> 2), tt = ln & 3;
-      uint2 v = make_uint2(0u, 0u);
-      if (ti.nrows && h < a.Hi) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(
-            a.q_idx + (static_cast<size_t>(ti.row0) * a.Hi + h) * kHeadDim + 32 * tt + 4 * j);
-        bool bad = false;
-        v.x = bf16x2_to_f16x2(raw.x, bad);
-        v.y = bf16x2_to_f16x2(raw.y, bad);
-        if (bad) sm.qbad = 1;
-      }
-      sm.qfrag[e] = v;
-    }
-    if (tid < 16) sm.w[tid] = (ti.nrows && tid < a.Hi) ? a.w[static_cast<size_t>(ti.row0) * a.Hi + tid] : 0.f;
-    if (tid == 0) sm.len = ti.nrows ? a.row_len[ti.row0] : 0;
-    __syncthreads();
-
-    const float w0 = sm.w[2 * t], w1 = sm.w[2 * t + 1], w2 = sm.w[8 + 2 * t], w3 = sm.w[9 + 2 * t];
-    const int rlen = sm.len;
-    uint32_t qa[8][2][2];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint2 v = sm.qfrag[(j * 2 + c) * 32 + lane];
-        qa[j][c][0] = v.x;
-        qa[j][c][1] = v.y;
-      }
-
-    // ---- this warp's blocks: seg_lo + warp + k * kWarps, two halves each ----
+    // ---- this warp's blocks: seg_lo + warp + k * kWarps, two halves each; its
+    // first two copies go out before the queries are staged, so the two global
+    // round trips overlap ----
     const int first = seg_lo + warp;
     const int count = first < seg_hi ? (seg_hi - first + kWarps - 1) / kWarps : 0;
     const int nhalf = 2 * count;
@@ -143,6 +113,39 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
 
     if (nhalf > 0) issue(0);
     if (nhalf > 1) issue(1);
+
+    // ---- the row's queries (fp16, fragment order), weights and length ----
+    __syncthreads();
+    for (int e = tid; e < kQFragWords; e += kThreads) {
+      const int ln = e & 31, c = (e >> 5) & 1, j = e >> 6;
+      const int h = 8 * c + (ln >> 2), tt = ln & 3;
+      uint2 v = make_uint2(0u, 0u);
+      if (ti.nrows && h < a.Hi) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(
+            a.q_idx + (static_cast<size_t>(ti.row0) * a.Hi + h) * kHeadDim + 32 * tt + 4 * j);
+        bool bad = false;
+        v.x = bf16x2_to_f16x2(raw.x, bad);
+        v.y = bf16x2_to_f16x2(raw.y, bad);
+        if (bad) sm.qbad = 1;
+      }
+      sm.qfrag[e] = v;
+    }
+    if (tid < 16) sm.w[tid] = (ti.nrows && tid < a.Hi) ? a.w[static_cast<size_t>(ti.row0) * a.Hi + tid] : 0.f;
+    if (tid == 0) sm.len = ti.nrows ? a.row_len[ti.row0] : 0;
+    __syncthreads();
+
+    const float w0 = sm.w[2 * t], w1 = sm.w[2 * t + 1], w2 = sm.w[8 + 2 * t], w3 = sm.w[9 + 2 * t];
+    const int rlen = sm.len;
+    uint32_t qa[8][2][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint2 v = sm.qfrag[(j * 2 + c) * 32 + lane];
+        qa[j][c][0] = v.x;
+        qa[j][c][1] = v.y;
+      }
+
     float best = -INFINITY;
     for (int hh = 0; hh < nhalf; ++hh) {
       const int s = hh & 1;
