@@ -18,6 +18,11 @@
 // the CTA's contiguous range) as two halves of 64 keys through its own
 // double-buffered shared-memory stages, filled by 1-D bulk copies (TMA) that
 // complete on an mbarrier. Block-table entries are fetched 32 at a time.
+//
+// The CTA ranges are cut in a cost space where every row costs its blocks plus
+// kSegCost: each row segment a CTA takes on pays a fixed set-up (its query row
+// and first block-table entries come from HBM), so a CTA whose range spans two
+// rows is given that many fewer blocks.
 #include <cuda_runtime.h>
 
 #include "m3s_score_common.cuh"
@@ -33,6 +38,8 @@ constexpr int kHalfCodeBytes = kHalfKeys * kCodeBytes;        // 4096
 constexpr int kHalfScaleBytes = kHalfKeys * kScaleBytes;      // 512
 constexpr int kStageBytes = kHalfCodeBytes + kHalfScaleBytes; // 4608
 constexpr int kQFragWords = 8 * 2 * 32;                       // k-steps x n-tiles x lanes (uint2)
+constexpr int kSegCost = 6;                                   // set-up of a row segment, in blocks
+static_assert(kQFragWords == kThreads, "one query fragment word per thread");
 
 struct __align__(16) DecodeSmem {
   uint8_t stage[kWarps][kStages][kStageBytes];
@@ -42,6 +49,25 @@ struct __align__(16) DecodeSmem {
   int len;
   int qbad;
 };
+
+// Block position of cost position x, where tile t spans [pre[t] + c t,
+// pre[t + 1] + c (t + 1)) in cost space: its first c units are its set-up (the
+// tile's first block), the rest one unit per block. Monotone, so consecutive
+// cost ranges give contiguous, disjoint block ranges covering every block.
+__device__ __forceinline__ int cost_to_block(const int* pre, int ntiles, long long x, int c) {
+  if (x >= pre[ntiles] + static_cast<long long>(c) * ntiles) return pre[ntiles];
+  int l = 0, h = ntiles;   // pc(l) <= x < pc(h)
+  while (h - l > 1) {
+    const int m = (l + h) >> 1;
+    if (pre[m] + static_cast<long long>(c) * m <= x) l = m; else h = m;
+  }
+  const long long o = x - (pre[l] + static_cast<long long>(c) * l);
+  return pre[l] + static_cast<int>(o > c ? o - c : 0);
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -61,9 +87,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
 
   tile_prefix<1>(a, pre, red, kThreads);
   const int ntiles = a.ntiles;
-  const long long N = pre[ntiles];
-  const int lo = static_cast<int>(N * blockIdx.x / gridDim.x);
-  const int hi = static_cast<int>(N * (blockIdx.x + 1) / gridDim.x);
+  const long long C = pre[ntiles] + static_cast<long long>(kSegCost) * ntiles;
+  const int lo = cost_to_block(pre, ntiles, C * blockIdx.x / gridDim.x, kSegCost);
+  const int hi = cost_to_block(pre, ntiles, C * (blockIdx.x + 1) / gridDim.x, kSegCost);
   int tile = tile_at(pre, ntiles, lo);
 
   uint32_t phase_bits = 0;  // per-stage mbarrier parity of this warp
@@ -76,9 +102,38 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     const int seg_hi = min(hi, pre[tile + 1]) - pre[tile];
     const TileInfo<1> ti = tile_info<1>(a, tile, false);
 
+    // ---- the row's queries (one fragment word per thread), weights and length:
+    // the loads go out first, so their round trip overlaps the block-table
+    // fetch of the first copies below ----
+    uint2 qraw = make_uint2(0u, 0u);
+    {
+      const int ln = tid & 31, c = (tid >> 5) & 1, j = tid >> 6;
+      const int h = 8 * c + (ln >> 2), tt = ln & 3;
+      if (ti.nrows && h < a.Hi)
+        qraw = *reinterpret_cast<const uint2*>(
+            a.q_idx + (static_cast<size_t>(ti.row0) * a.Hi + h) * kHeadDim + 32 * tt + 4 * j);
+    }
+    const float wrow = (tid < 16 && ti.nrows && tid < a.Hi) ? a.w[static_cast<size_t>(ti.row0) * a.Hi + tid] : 0.f;
+    const int lrow = (tid == 0 && ti.nrows) ? a.row_len[ti.row0] : 0;
+
+    // ---- a range that goes on into the next row warms L2 with that row's
+    // queries and first block-table entries while this segment runs ----
+    const int next_pos = pre[tile] + seg_hi;
+    if (warp == kWarps - 1 && next_pos < hi) {
+      int nt = tile + 1;
+      while (pre[nt + 1] <= next_pos) ++nt;
+      const TileInfo<1> tn = tile_info<1>(a, nt, false);
+      if (tn.nrows) {
+        if (lane * 64 < a.Hi * kHeadDim)
+          prefetch_l2(a.q_idx + static_cast<size_t>(tn.row0) * a.Hi * kHeadDim + lane * 64);
+        const int j0 = next_pos - pre[nt] + 32 * lane;
+        if (lane < 16 && j0 < min(hi, pre[nt + 1]) - pre[nt])
+          prefetch_l2(a.block_table + static_cast<size_t>(tn.req) * a.bt_stride + j0);
+      }
+    }
+
     // ---- this warp's blocks: seg_lo + warp + k * kWarps, two halves each; its
-    // first two copies go out before the queries are staged, so the two global
-    // round trips overlap ----
+    // first two copies go out before the queries are staged ----
     const int first = seg_lo + warp;
     const int count = first < seg_hi ? (seg_hi - first + kWarps - 1) / kWarps : 0;
     const int nhalf = 2 * count;
@@ -114,24 +169,19 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     if (nhalf > 0) issue(0);
     if (nhalf > 1) issue(1);
 
-    // ---- the row's queries (fp16, fragment order), weights and length ----
+    // ---- the queries to fp16 in fragment order (the previous segment's
+    // readers are past the first barrier) ----
     __syncthreads();
-    for (int e = tid; e < kQFragWords; e += kThreads) {
-      const int ln = e & 31, c = (e >> 5) & 1, j = e >> 6;
-      const int h = 8 * c + (ln >> 2), tt = ln & 3;
-      uint2 v = make_uint2(0u, 0u);
-      if (ti.nrows && h < a.Hi) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(
-            a.q_idx + (static_cast<size_t>(ti.row0) * a.Hi + h) * kHeadDim + 32 * tt + 4 * j);
-        bool bad = false;
-        v.x = bf16x2_to_f16x2(raw.x, bad);
-        v.y = bf16x2_to_f16x2(raw.y, bad);
-        if (bad) sm.qbad = 1;
-      }
-      sm.qfrag[e] = v;
+    {
+      bool bad = false;
+      uint2 v;
+      v.x = bf16x2_to_f16x2(qraw.x, bad);
+      v.y = bf16x2_to_f16x2(qraw.y, bad);
+      if (bad) sm.qbad = 1;
+      sm.qfrag[tid] = v;
     }
-    if (tid < 16) sm.w[tid] = (ti.nrows && tid < a.Hi) ? a.w[static_cast<size_t>(ti.row0) * a.Hi + tid] : 0.f;
-    if (tid == 0) sm.len = ti.nrows ? a.row_len[ti.row0] : 0;
+    if (tid < 16) sm.w[tid] = wrow;
+    if (tid == 0) sm.len = lrow;
     __syncthreads();
 
     const float w0 = sm.w[2 * t], w1 = sm.w[2 * t + 1], w2 = sm.w[8 + 2 * t], w3 = sm.w[9 + 2 * t];
