@@ -132,9 +132,12 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
       }
     }
 
-    // ---- this warp's blocks: seg_lo + warp + k * kWarps, two halves each; its
-    // first two copies go out before the queries are staged ----
-    const int first = seg_lo + warp;
+    // ---- this warp's blocks: every kWarps-th block of the segment, two halves
+    // each, the warp order carried on from the CTA's previous segment (so a
+    // range over two rows does not give the low warps an extra block in each);
+    // its first two copies go out before the queries are staged ----
+    const int rot = (pos - lo) % kWarps;
+    const int first = seg_lo + (warp - rot + kWarps) % kWarps;
     const int count = first < seg_hi ? (seg_hi - first + kWarps - 1) / kWarps : 0;
     const int nhalf = 2 * count;
     const int32_t* bt_row = a.block_table + static_cast<size_t>(ti.req) * a.bt_stride;
@@ -151,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
         if (page < 0 || page >= a.num_pages) {
           if (half == 0) raise(a.err, M3S_DEVERR_PAGE);
         } else {
-          fence_proxy_async();
+          // (no proxy fence: every generic read of this stage has returned, its
+          // values having gone through the mma and the shuffles above)
           mbar_expect_tx(&sm.bar[warp][s], kStageBytes);
           bulk_g2s(sm.stage[warp][s],
                    a.codes + static_cast<size_t>(page) * kPageCodeBytes + half * kHalfCodeBytes,
