@@ -24,6 +24,13 @@ three pull requests on the MiniMax-M3.1 NVFP4 caches):
   score = max over the block's causal tokens, top-k blocks by score.
 * Fused verify top-k -- #2744, Fused verify top-k: the same selection as
   score + top-k, ids only.
+* MXFP4 record -- #2744, Follow-up: MXFP4 caches, and vllm #64198, Overview /
+  Claims: e2m1 data with one E8M0 scale per 32 elements, 68 B per token and
+  head, a page [128 x 64 B e2m1][128 x 4 B e8m0]. The pages name the format
+  and not its rounding; the shared exponent is the OCP MX one,
+  floor(log2(amax)) - 2 (2 = the exponent of e2m1's largest value, 6),
+  clamped to E8M0's range, and each element is rounded half-to-even on the
+  e2m1 grid after division by 2^exponent, saturating at 6.
 * Sparse attention -- #2746 Summary / Attention and #2744 Design / Attention:
   softmax attention over the tokens of the selected blocks, addressed through
   the block table, against the dequantised cache.
@@ -57,6 +64,8 @@ PAGE = 128
 GROUP = 16
 PAYLOAD_BYTES = HEAD_DIM // 2       # 64 B of e2m1 codes per token and head
 SCALE_BYTES = HEAD_DIM // GROUP     # 8 B of E4M3 scales per token and head
+MX_GROUP = 32
+MX_SCALE_BYTES = HEAD_DIM // MX_GROUP   # 4 B of E8M0 scales per token and head (MXFP4)
 
 # error bits reported by the store / scorer / attention (same meaning as the
 # CUDA library's device error word)
@@ -113,6 +122,16 @@ def _nearest_even(x: np.ndarray, values: np.ndarray, scale=None) -> np.ndarray:
     return np.where(at & (below % 2 == 1), below + 1, below)
 
 
+def e8m0_value(code: int) -> float:
+    """Value of an OCP E8M0 byte: 2^(code - 127); 0xFF is NaN."""
+    code = int(code) & 0xFF
+    return math.nan if code == 0xFF else math.ldexp(1.0, code - 127)
+
+
+#: value of every E8M0 byte (NaN for 0xFF)
+E8M0_ALL = np.array([e8m0_value(c) for c in range(256)])
+
+
 def e4m3_encode_nonneg(v: np.ndarray) -> np.ndarray:
     """Round non-negative reals to E4M3 (nearest, ties to even code, saturate at 448)."""
     return _nearest_even(v, E4M3_POS).astype(np.uint8)
@@ -127,18 +146,21 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return b.view(np.float32).astype(np.float64)
 
 
-def quantize(bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
-    """NVFP4-quantise BF16 rows (see ``_quantize``), in slices to bound memory."""
+def quantize(bits: np.ndarray, mx: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """NVFP4- (or, with ``mx``, MXFP4-) quantise BF16 rows (see ``_quantize`` and
+    ``_quantize_mx``), in slices to bound memory."""
     bits = np.asarray(bits, dtype=np.uint16)
     flat = bits.reshape(-1, HEAD_DIM)
     n = flat.shape[0]
+    nsb = MX_SCALE_BYTES if mx else SCALE_BYTES
     codes = np.empty((n, PAYLOAD_BYTES), dtype=np.uint8)
-    scales = np.empty((n, SCALE_BYTES), dtype=np.uint8)
+    scales = np.empty((n, nsb), dtype=np.uint8)
     step = 1 << 15
+    fn = _quantize_mx if mx else _quantize
     for i in range(0, n, step):
-        codes[i:i + step], scales[i:i + step] = _quantize(flat[i:i + step])
+        codes[i:i + step], scales[i:i + step] = fn(flat[i:i + step])
     lead = bits.shape[:-1]
-    return codes.reshape(lead + (PAYLOAD_BYTES,)), scales.reshape(lead + (SCALE_BYTES,))
+    return codes.reshape(lead + (PAYLOAD_BYTES,)), scales.reshape(lead + (nsb,))
 
 
 def _quantize(bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
@@ -171,37 +193,77 @@ def _quantize(bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return packed, scode
 
 
+def _quantize_mx(bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """MXFP4-quantise BF16 rows.
+
+    ``bits``: uint16 BF16 bit patterns, shape [..., 128].
+    Returns (codes uint8 [..., 64], scales uint8 [..., 4]).
+
+    Per group of 32 elements: amax = max |x|; the shared exponent is
+    E = floor(log2(amax)) - 2, clamped to [-127, 127] (amax = 0 gives -127);
+    the scale byte is E + 127 (E8M0). Each element's magnitude code is the
+    e2m1 grid value nearest to |x| / 2^E (ties to the even code, beyond 6
+    saturating to 6) and its sign bit is the sign bit of x.
+    """
+    bits = np.asarray(bits, dtype=np.uint16)
+    lead = bits.shape[:-1]
+    assert bits.shape[-1] == HEAD_DIM
+    x = bf16_to_f64(bits).reshape(lead + (MX_SCALE_BYTES, MX_GROUP))
+    sign = ((bits >> np.uint16(15)) & np.uint16(1)).astype(np.uint8).reshape(x.shape)
+    amax = np.abs(x).max(axis=-1)                             # [..., 4]
+    _, e = np.frexp(amax)                                     # amax = m 2^e, m in [0.5, 1)
+    E = np.where(amax > 0.0, e.astype(np.int64) - 1 - 2, -127)
+    E = np.clip(E, -127, 127)
+    scode = (E + 127).astype(np.uint8)
+    s = np.ldexp(1.0, E)                                      # exact powers of two
+    # nearest grid value to |x| / 2^E  <=>  compare |x| with 2^E x (grid midpoints), exact
+    mag = _nearest_even(np.abs(x), E2M1_GRID, s[..., None]).astype(np.uint8)
+    code = ((sign << np.uint8(3)) | mag).reshape(lead + (HEAD_DIM,))
+    packed = (code[..., 0::2] | (code[..., 1::2] << np.uint8(4))).astype(np.uint8)
+    return packed, scode
+
+
 def dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """x_hat = e2m1(code) * e4m3(scale), float64, shape [..., 128]."""
+    """x_hat = e2m1(code) * scale, float64, shape [..., 128].
+
+    The format follows the scale array: 8 bytes per record are E4M3 scales of
+    16 elements each (NVFP4), 4 bytes are E8M0 scales of 32 elements (MXFP4).
+    """
     codes = np.asarray(codes, dtype=np.uint8)
+    scales = np.asarray(scales, dtype=np.uint8)
     lo = codes & np.uint8(0xF)
     hi = codes >> np.uint8(4)
     c = np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (HEAD_DIM,))
     val = E2M1_GRID[c & 7] * np.where(c & 8, -1.0, 1.0)
-    s = E4M3_ALL[np.asarray(scales, dtype=np.uint8)]
-    return val * np.repeat(s, GROUP, axis=-1)
+    if scales.shape[-1] == MX_SCALE_BYTES:
+        return val * np.repeat(E8M0_ALL[scales], MX_GROUP, axis=-1)
+    assert scales.shape[-1] == SCALE_BYTES
+    return val * np.repeat(E4M3_ALL[scales], GROUP, axis=-1)
 
 
-def new_planes(num_pages: int, heads: int) -> tuple[np.ndarray, np.ndarray]:
-    """Zeroed planes: codes [P, H, 128, 64] and scales [P, H, 128, 8] (uint8)."""
+def new_planes(num_pages: int, heads: int, mx: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """Zeroed planes: codes [P, H, 128, 64] and scales [P, H, 128, 8] (NVFP4) or
+    [P, H, 128, 4] (MXFP4), uint8."""
     return (np.zeros((num_pages, heads, PAGE, PAYLOAD_BYTES), dtype=np.uint8),
-            np.zeros((num_pages, heads, PAGE, SCALE_BYTES), dtype=np.uint8))
+            np.zeros((num_pages, heads, PAGE, MX_SCALE_BYTES if mx else SCALE_BYTES),
+                     dtype=np.uint8))
 
 
 def nvfp4_store(src: np.ndarray, slot_mapping: np.ndarray, codes: np.ndarray,
                 scales: np.ndarray) -> int:
     """Quantise rows ``src`` [T, H, 128] (BF16 bits) into the planes at their slots.
 
-    slot = page * 128 + offset. A negative slot is a pad row and is skipped,
-    leaving the planes untouched; a slot beyond the planes sets ERR_SLOT and is
-    skipped. Returns the error bits.
+    The planes' format follows the scale plane (8 bytes per record: NVFP4, 4:
+    MXFP4). slot = page * 128 + offset. A negative slot is a pad row and is
+    skipped, leaving the planes untouched; a slot beyond the planes sets
+    ERR_SLOT and is skipped. Returns the error bits.
     """
     src = np.asarray(src, dtype=np.uint16)
     slot_mapping = np.asarray(slot_mapping, dtype=np.int64)
     P, H = codes.shape[0], codes.shape[1]
     assert src.shape[1] == H
     err = 0
-    c, s = quantize(src)
+    c, s = quantize(src, mx=scales.shape[-1] == MX_SCALE_BYTES)
     for r, slot in enumerate(slot_mapping):
         if slot < 0:
             continue

@@ -425,3 +425,186 @@ def test_forced_blocks_against_restatement():
         exp = _forced_rank_restatement(sc, k, init, local)
         cnt = min(k, nb)
         assert got[:cnt].tolist() == exp and (got[cnt:] == -1).all()
+
+
+# --------------------------------------------------------------------------
+# MXFP4 (e2m1 + E8M0 per 32): "[MiniMax-M3.1] FP4 index cache and NVFP4
+# sparse KV cache" (#2744), Follow-up: MXFP4 caches; vllm #64198, Overview
+# --------------------------------------------------------------------------
+
+MX_GOLDEN = __file__.rsplit("/", 1)[0] + "/golden/mxfp4_quant_groups.txt"
+
+
+def _mx_golden_cases():
+    cases, cur = [], None
+    for line in open(MX_GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        if line.startswith("case "):
+            cur = {"name": line[5:]}
+            cases.append(cur)
+        else:
+            k, v = line.split(":", 1)
+            cur[k] = v.split()
+    return cases
+
+
+def _mx_value(tok):
+    return float.fromhex(tok) if tok.lstrip("-").startswith("0x") else float(tok)
+
+
+def _mx_row(case):
+    g = int(case["group"][0])
+    x = np.zeros(128, dtype=np.float32)
+    vals = [_mx_value(t) for t in case["x"]]
+    x[32 * g: 32 * g + len(vals)] = vals
+    bits = W.f32_to_bf16_bits(x)
+    assert np.array_equal(W.bf16_bits_to_f32(bits), x)   # BF16-exact inputs
+    return bits, g, len(vals)
+
+
+@pytest.mark.parametrize("case", _mx_golden_cases(), ids=lambda c: c["name"])
+def test_mx_quantiser_hand_worked(case):
+    bits, g, n = _mx_row(case)
+    codes, scales = O.quantize(bits, mx=True)
+    assert scales.shape == (4,) and codes.shape == (64,)
+    for j in range(4):
+        assert scales[j] == (int(case["scale"][0], 16) if j == g else 0), j
+    got = [(codes[(32 * g + i) // 2] >> (4 * (i % 2))) & 0xF for i in range(32)]
+    assert got[:n] == [int(c, 16) for c in case["codes"]]
+    assert not any(got[n:])
+    other = np.delete(codes.reshape(4, 16), g, axis=0)
+    assert not other.any()
+
+
+def test_e8m0_table_matches_torch():
+    """Every E8M0 byte decodes as torch's float8_e8m0fnu does (library routine)."""
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch without float8_e8m0fnu")
+    allb = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).float().double().numpy()
+    nan = np.isnan(allb)
+    assert nan.sum() == 1 and nan[255]
+    assert np.array_equal(allb[~nan], O.E8M0_ALL[~nan])
+
+
+def _exact_quantise_mx_group(xs):
+    """Independent restatement in exact rationals of one 32-group: the shared
+    exponent is the largest k with 2^(k+2) <= amax (found by stepping), clamped."""
+    fr = [Fraction(float(x)) for x in xs]
+    amax = max(abs(x) for x in fr)
+    if amax == 0:
+        k = -127
+    else:
+        k = 0
+        while Fraction(2) ** (k + 2) > amax:
+            k -= 1
+        while Fraction(2) ** (k + 3) <= amax:
+            k += 1
+        k = max(-127, min(127, k))
+    s = Fraction(2) ** k
+    grid = [Fraction(g) for g in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    codes = []
+    for x, xf in zip(xs, fr):
+        q = abs(xf) / s
+        m = min(range(8), key=lambda i: (abs(grid[i] - q), i % 2))
+        codes.append(m | (8 if math.copysign(1.0, float(x)) < 0 else 0))
+    return k + 127, codes
+
+
+def test_mx_quantiser_equals_exact_rational_definition():
+    """Vectorised MX quantiser == exact-rational brute force on random groups over
+    a wide exponent range (BF16 subnormals included), with ties planted."""
+    rng = np.random.default_rng(11)
+    rows = []
+    for i in range(40):
+        e = int(rng.integers(-135, 120))
+        x = rng.standard_normal(128) * 2.0 ** e
+        if i % 3 == 0:        # exact ties at a power-of-two scale
+            x[:7] = np.array([.25, .75, 1.25, 1.75, 2.5, 3.5, 5]) * 2.0 ** (e - 3)
+            x[7] = 7 * 2.0 ** (e - 3)
+        rows.append(x)
+    bits = W.f32_to_bf16_bits(np.array(rows, dtype=np.float32))
+    bits[(bits & 0x7F80) == 0x7F80] &= 0x807F     # no inf / NaN from the float32 range
+    xs = W.bf16_bits_to_f32(bits).astype(np.float64)
+    codes, scales = O.quantize(bits, mx=True)
+    for r in range(len(rows)):
+        for g in range(4):
+            s, c = _exact_quantise_mx_group(xs[r, 32 * g: 32 * g + 32])
+            assert scales[r, g] == s, (r, g)
+            got = [(codes[r, 16 * g + i // 2] >> (4 * (i % 2))) & 0xF for i in range(32)]
+            assert got == c, (r, g)
+
+
+def test_mx_round_trip_error_bound():
+    """|x - x_hat| <= half the local e2m1 step x 2^E below 6 x 2^E, and <= 2 x 2^E
+    in the saturating band (6, 8) x 2^E; every group uses its top code range
+    (amax / 2^E lies in [4, 8))."""
+    bits = W.bf16_tensor(7, "mxrt", (512, 128), 4, 20.0)
+    x = W.bf16_bits_to_f32(bits).astype(np.float64)
+    c, s = O.quantize(bits, mx=True)
+    xh = O.dequantize(c, s)
+    sv = np.repeat(O.E8M0_ALL[s], 32, axis=-1)
+    q = np.abs(x) / sv
+    step = np.where(q < 2, 0.5, np.where(q < 4, 1.0, 2.0))
+    unsat = q <= 6
+    assert np.all(np.abs(x - xh)[unsat] <= (0.5 * step * sv)[unsat])
+    assert np.all(np.abs(x - xh)[~unsat] <= (2.0 * sv)[~unsat])
+    amax_q = q.reshape(512, 4, 32).max(-1)
+    assert np.all((amax_q >= 4) & (amax_q < 8))
+
+
+def test_mx_record_and_page_size_reproduce_pages():
+    """68 B per token and head, and a 128-token page per head of
+    [128 x 64 B e2m1][128 x 4 B e8m0] = 8704 B (vllm #64198, Claims)."""
+    c, s = O.new_planes(1, 1, mx=True)
+    assert c.shape[-1] + s.shape[-1] == 68
+    assert c[0, 0].nbytes + s[0, 0].nbytes == 8704
+
+
+def test_mx_and_nvfp4_dequantise_alike_where_both_represent_the_values():
+    """Records whose every group has scale 1 in both formats (E8M0 0x7f, E4M3
+    0x38) dequantise to the same values, and the oracle's scorer and attention
+    give the same results over them."""
+    rng = np.random.default_rng(5)
+    P, L = 3, 300
+    codes = rng.integers(0, 256, size=(P, 1, 128, 64), dtype=np.uint8)
+    s_nv = np.full((P, 1, 128, 8), 0x38, dtype=np.uint8)
+    s_mx = np.full((P, 1, 128, 4), 0x7F, dtype=np.uint8)
+    assert np.array_equal(O.dequantize(codes, s_nv), O.dequantize(codes, s_mx))
+    bt = np.array([[2, 0, 1]], dtype=np.int32)
+    rr, rl = np.array([0], dtype=np.int32), np.array([L], dtype=np.int32)
+    q = W.f32_to_bf16_bits(rng.standard_normal((1, 2, 128)).astype(np.float32))
+    w = rng.random((1, 2))
+    ids_nv, bs_nv, _ = O.index_score_topk(q, w, codes, s_nv, bt, rr, rl, 2)
+    ids_mx, bs_mx, _ = O.index_score_topk(q, w, codes, s_mx, bt, rr, rl, 2)
+    assert np.array_equal(ids_nv, ids_mx) and np.array_equal(bs_nv, bs_mx)
+    qa = W.f32_to_bf16_bits(rng.standard_normal((1, 4, 128)).astype(np.float32))
+    ids = np.array([[0, 2]], dtype=np.int32)
+    o_nv, l_nv, _ = O.sparse_attention(qa, 1, codes, s_nv, codes, s_nv, bt, rr, rl, ids, 0.1)
+    o_mx, l_mx, _ = O.sparse_attention(qa, 1, codes, s_mx, codes, s_mx, bt, rr, rl, ids, 0.1)
+    assert np.array_equal(o_nv, o_mx) and np.array_equal(l_nv, l_mx)
+
+
+def test_mx_store_into_mx_planes():
+    """The store picks the MXFP4 quantiser from the planes' 4-byte scale records and
+    leaves pad rows untouched."""
+    H, T, P = 2, 30, 3
+    src = W.bf16_tensor(4, "mxst", (T, H, 128), 2, 10.0)
+    slots = W.permutation(4, "mxslots", P * 128)[:T].astype(np.int64)
+    slots[4] = -1
+    c, s = O.new_planes(P, H, mx=True)
+    c[:] = 0xA5
+    s[:] = 0x5A
+    assert O.nvfp4_store(src, slots, c, s) == 0
+    qc, qs = O.quantize(src, mx=True)
+    for r, slot in enumerate(slots):
+        if slot < 0:
+            continue
+        assert np.array_equal(c[slot // 128, :, slot % 128], qc[r])
+        assert np.array_equal(s[slot // 128, :, slot % 128], qs[r])
+    written = set(int(v) for v in slots if v >= 0)
+    for slot in range(P * 128):
+        if slot not in written:
+            assert (c[slot // 128, :, slot % 128] == 0xA5).all()
+            assert (s[slot // 128, :, slot % 128] == 0x5A).all()
