@@ -62,25 +62,36 @@ extern "C" {
 #define M3S_MAX_GQA 16 /* q heads per KV head */
 
 /*
- * A paged NVFP4 plane pair (the pool of one K, V or index-K tensor).
+ * A paged FP4 plane pair (the pool of one K, V or index-K tensor).
  * "NVFP4 sparse KV" (ROCm/ATOM #2746), Summary: the pool's k/v and scale fields
  * are uint8 planes; per token and head a 64 B e2m1 payload plus 8 B of E4M3
  * scales. Within a page the payloads of the 128 tokens come first and the
  * scales sit in their own plane (vllm #64198, Claims: [128 x payload][128 x scales]).
+ * The MXFP4 record ("[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache"
+ * (ROCm/ATOM #2744), Follow-up: MXFP4 caches; vllm #64198, Overview) has the
+ * same payload and one E8M0 scale per 32 elements: 68 B per token and head.
  *
  *   codes  : uint8 [num_pages][num_heads][128][64]; byte i of a token holds
  *            element 2i in its low nibble and element 2i+1 in its high nibble;
  *            nibble = sign(bit 3) | e2m1 magnitude code (bits 0-2).
- *   scales : uint8 [num_pages][num_heads][128][8]; byte j is the E4M3 scale
- *            of elements 16j .. 16j+15.
+ *   scales : M3S_FMT_NVFP4: uint8 [num_pages][num_heads][128][8]; byte j is the
+ *            E4M3 scale of elements 16j .. 16j+15.
+ *            M3S_FMT_MXFP4: uint8 [num_pages][num_heads][128][4]; byte j is the
+ *            E8M0 scale 2^(byte - 127) of elements 32j .. 32j+31.
+ *   format : M3S_FMT_*; a zero-initialised plane is NVFP4. Any other value is
+ *            M3S_ERR_INVALID.
  *   A token's slot is page * 128 + position within the page.
  */
+#define M3S_FMT_NVFP4 0
+#define M3S_FMT_MXFP4 1
 typedef struct {
   uint8_t* codes;
   uint8_t* scales;
   int32_t num_pages;
   int32_t num_heads;
-} m3s_nvfp4_plane;
+  int32_t format;
+} m3s_fp4_plane;
+typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type */
 
 /* ops for m3s_workspace_bytes */
 #define M3S_OP_INDEX_SCORE_TOPK 1
@@ -107,6 +118,12 @@ size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int
  * scale = e4m3(amax / 6) (saturating at 448), codes rounded half-to-even on the
  * e2m1 grid and saturating at 6. A group whose scale rounds to 0 stores zero
  * codes; a code's sign bit is the sign bit of the input.
+ * Into an MXFP4 plane (dst.format == M3S_FMT_MXFP4; #2744, Follow-up: MXFP4
+ * caches -- one E8M0 scale per 32 elements), per 32 elements the shared
+ * exponent is E = floor(log2(amax)) - 2 clamped to [-127, 127] (amax 0 gives
+ * -127; the pages name the format, this is its OCP MX rule), the scale byte
+ * is E + 127, and each code is |x| / 2^E rounded half-to-even on the e2m1
+ * grid, saturating at 6, with the sign bit of the input.
  *
  *   src          : BF16 [T][H][128] (row r, head h at src + r*src_row_stride + h*128)
  *   src_row_stride: elements between consecutive rows (>= H*128, multiple of 8)
@@ -117,7 +134,7 @@ size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int
  * T == 0 is a no-op.
  */
 int m3s_nvfp4_store(const uint16_t* src, int64_t src_row_stride, int32_t T, int32_t H,
-                    const int64_t* slot_mapping, m3s_nvfp4_plane dst, int32_t* err,
+                    const int64_t* slot_mapping, m3s_fp4_plane dst, int32_t* err,
                     void* stream);
 
 /*
@@ -131,7 +148,7 @@ typedef struct {
   const uint16_t* src;    /* BF16 [T][H][128] device rows */
   int64_t src_row_stride; /* elements between rows (>= H*128, multiple of 8) */
   int32_t H;              /* heads per row; must equal dst.num_heads */
-  m3s_nvfp4_plane dst;
+  m3s_fp4_plane dst;      /* either format; jobs may differ */
 } m3s_store_job;
 
 int m3s_nvfp4_store_batch(const m3s_store_job* jobs, int32_t njobs, int32_t T,
@@ -154,7 +171,9 @@ int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int3
  * score grid; "NVFP4 sparse KV", Summary (fused verify top-k emits ids only).
  * For row r of request b = row_req[r] with causal length L = row_len[r]:
  *   score[t] = sum_h w[r,h] * ReLU(q_idx[r,h,:] . k_hat[t,:]),  t < L,
- *   k_hat = the dequantised NVFP4 index key (index plane, one head),
+ *   k_hat = the dequantised index key (index plane, one head; NVFP4, or MXFP4
+ *           (exact when a key's four E8M0 scales lie within a factor 2^23 of
+ *           each other; smaller groups beyond that are rounded in fp16)),
  *   block_score[blk] = max of score over the block's causal tokens,
  *   topk_ids[r] = the topk blocks with the highest block score, the lower id
  *                 on equal scores, sorted ascending, padded with -1.
@@ -175,7 +194,7 @@ int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int3
  * ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, ...).
  */
 int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
-                         m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
+                         m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
                          const int32_t* row_req, const int32_t* row_len, int32_t R, int32_t B,
                          int32_t topk, int32_t init_blocks, int32_t local_blocks,
                          int32_t* topk_ids, float* block_scores, void* ws, size_t ws_bytes,
@@ -192,7 +211,7 @@ int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
  * rows are taken as valid when 0 < row_len <= bt_stride*128 and B > 0).
  */
 int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int32_t Hi,
-                           m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
+                           m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
                            const int32_t* row_req, const int32_t* row_len, int32_t R, int32_t B,
                            float* block_scores, int32_t bs_stride, int32_t* err, void* stream);
 int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* row_req,
@@ -219,7 +238,7 @@ int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* 
  */
 #define M3S_STATIC_SCRATCH_BYTES (4u << 20)
 int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t Hi,
-                                m3s_nvfp4_plane idx_k, const int32_t* block_table,
+                                m3s_fp4_plane idx_k, const int32_t* block_table,
                                 int32_t bt_stride, const int32_t* row_req, const int32_t* row_len,
                                 int32_t R, int32_t B, int32_t topk, int32_t* topk_ids,
                                 int32_t* err, void* stream);
@@ -234,10 +253,12 @@ int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t H
  *   cu_q int32 [B+1] groups rows by request (as for m3s_decode_rows),
  *   row_len int32 [R] their causal lengths (m3s_decode_rows),
  *   max_q >= every cu_q[b+1]-cu_q[b] (sizes the request-row tiling).
- * Other arguments as for m3s_index_score_topk.
+ * Other arguments as for m3s_index_score_topk. The index plane must be NVFP4
+ * in this build (an MXFP4 plane returns M3S_ERR_UNSUPPORTED; its rows can go
+ * through m3s_index_score_topk, which gives the same result).
  */
 int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
-                          m3s_nvfp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
+                          m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
                           const int32_t* cu_q, const int32_t* row_len, int32_t B, int32_t R,
                           int32_t max_q, int32_t topk, int32_t init_blocks, int32_t local_blocks,
                           int32_t* topk_ids, void* ws, size_t ws_bytes, int32_t* err,
@@ -261,9 +282,14 @@ int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
  * and is skipped (never wrapped onto another page). A row with no token
  * (pad row, all ids -1) outputs zeros and lse = -inf. Duplicate ids count
  * their block once per occurrence.
+ * k and v share one format (NVFP4 or MXFP4; mixed formats return
+ * M3S_ERR_UNSUPPORTED, as the pages' startup refuses mixing them: #2744,
+ * Follow-up: MXFP4 caches). NVFP4 K/V dequantise exactly to fp16 (the q
+ * operand is fp16, see M3S_DEVERR_QRANGE); MXFP4 K/V dequantise exactly to
+ * bf16 and meet q in bf16 as given, the softmax weights rounded to bf16.
  */
-int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_nvfp4_plane k,
-                         m3s_nvfp4_plane v, const int32_t* block_table, int32_t bt_stride,
+int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k,
+                         m3s_fp4_plane v, const int32_t* block_table, int32_t bt_stride,
                          int32_t B, const int32_t* row_req, const int32_t* row_len, const int32_t* topk_ids,
                          int32_t topk, int32_t R, float sm_scale, uint16_t* out, float* lse,
                          void* ws, size_t ws_bytes, int32_t* err, void* stream);

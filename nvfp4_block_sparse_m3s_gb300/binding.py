@@ -24,6 +24,7 @@ STATUS = {1: "M3S_ERR_INVALID", 2: "M3S_ERR_UNSUPPORTED", 3: "M3S_ERR_WORKSPACE"
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_PAGE, DEVERR_ROW, DEVERR_QRANGE, DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16, 32
 OP_INDEX_SCORE_TOPK, OP_VERIFY_SCORE_TOPK, OP_SPARSE_ATTENTION = 1, 2, 3
+FMT_NVFP4, FMT_MXFP4 = 0, 1
 HEAD_DIM = PAGE = 128
 
 
@@ -32,10 +33,12 @@ class M3SError(RuntimeError):
 
 
 class Plane(ctypes.Structure):
-    """m3s_nvfp4_plane: codes [P, H, 128, 64] and scales [P, H, 128, 8] (uint8, device)."""
+    """m3s_fp4_plane: codes [P, H, 128, 64] and scales [P, H, 128, 8] (NVFP4) or
+    [P, H, 128, 4] (MXFP4), uint8 device tensors; ``format`` is FMT_*."""
 
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
-                ("num_pages", ctypes.c_int32), ("num_heads", ctypes.c_int32)]
+                ("num_pages", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+                ("format", ctypes.c_int32)]
 
 
 class StoreJob(ctypes.Structure):
@@ -104,16 +107,22 @@ def _stream(stream) -> int:
 
 
 def plane(codes: torch.Tensor, scales: torch.Tensor) -> Plane:
+    """The C plane of a (codes, scales) pair; its format follows the scale records'
+    width (8 bytes: NVFP4, 4 bytes: MXFP4)."""
     assert codes.dtype == torch.uint8 and scales.dtype == torch.uint8
     assert codes.dim() == 4 and codes.shape[2:] == (PAGE, HEAD_DIM // 2)
-    assert scales.shape == codes.shape[:3] + (HEAD_DIM // 16,)
+    assert scales.shape[:3] == codes.shape[:3] and scales.shape[3] in (HEAD_DIM // 16, HEAD_DIM // 32)
     assert codes.is_contiguous() and scales.is_contiguous()
-    return Plane(codes.data_ptr(), scales.data_ptr(), codes.shape[0], codes.shape[1])
+    fmt = FMT_MXFP4 if scales.shape[3] == HEAD_DIM // 32 else FMT_NVFP4
+    return Plane(codes.data_ptr(), scales.data_ptr(), codes.shape[0], codes.shape[1], fmt)
 
 
-def new_plane(num_pages: int, heads: int, device="cuda") -> tuple[torch.Tensor, torch.Tensor]:
+def new_plane(num_pages: int, heads: int, device="cuda", mx: bool = False
+              ) -> tuple[torch.Tensor, torch.Tensor]:
+    """Zeroed planes: codes [P, H, 128, 64], scales [P, H, 128, 8] (or 4 with ``mx``)."""
     return (torch.zeros((num_pages, heads, PAGE, HEAD_DIM // 2), dtype=torch.uint8, device=device),
-            torch.zeros((num_pages, heads, PAGE, HEAD_DIM // 16), dtype=torch.uint8, device=device))
+            torch.zeros((num_pages, heads, PAGE, HEAD_DIM // (32 if mx else 16)), dtype=torch.uint8,
+                        device=device))
 
 
 def m3s_workspace_bytes(op: int, R: int, B: int, max_blocks: int, Hq: int = 0, Hkv: int = 0,
@@ -163,9 +172,22 @@ def m3s_decode_rows(cu_q: torch.Tensor, seq_len: torch.Tensor, R: int,
     return row_req, row_len
 
 
+def _index_inputs(q_idx, w, block_table, *int32s):
+    """The dtypes the C calls assume for the index-scoring tensors (they pass raw
+    pointers: a float64 weight tensor would be read as fp32 pairs)."""
+    if q_idx.dtype != torch.bfloat16 or not q_idx.is_contiguous():
+        raise TypeError("q_idx must be a contiguous bfloat16 tensor [R, Hi, 128]")
+    if w.dtype != torch.float32 or not w.is_contiguous() or tuple(w.shape) != tuple(q_idx.shape[:2]):
+        raise TypeError("w must be a contiguous float32 tensor [R, Hi]")
+    for t in (block_table,) + int32s:
+        if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+            raise TypeError("block tables, row maps and cu_q must be contiguous int32 tensors")
+
+
 def m3s_index_score_topk(q_idx, w, codes, scales, block_table, row_req, row_len, topk: int,
                          topk_ids=None, block_scores=None, ws=None, err=None, stream=None,
                          init_blocks: int = 0, local_blocks: int = 0):
+    _index_inputs(q_idx, w, block_table, row_req, row_len)
     R, Hi = q_idx.shape[0], q_idx.shape[1]
     B, bt_stride = block_table.shape
     if topk_ids is None:
@@ -184,6 +206,7 @@ def m3s_index_score_topk(q_idx, w, codes, scales, block_table, row_req, row_len,
 
 def m3s_index_score_topk_static(q_idx, w, codes, scales, block_table, row_req, row_len, topk: int,
                                 topk_ids=None, err=None, stream=None):
+    _index_inputs(q_idx, w, block_table, row_req, row_len)
     R, Hi = q_idx.shape[0], q_idx.shape[1]
     B, bt_stride = block_table.shape
     if topk_ids is None:
@@ -197,6 +220,9 @@ def m3s_index_score_topk_static(q_idx, w, codes, scales, block_table, row_req, r
 
 def m3s_index_block_scores(q_idx, w, codes, scales, block_table, row_req, row_len, block_scores,
                            err=None, stream=None):
+    _index_inputs(q_idx, w, block_table, row_req, row_len)
+    if block_scores.dtype != torch.float32:
+        raise TypeError("block_scores must be float32")
     R, Hi = q_idx.shape[0], q_idx.shape[1]
     B, bt_stride = block_table.shape
     rc = load().m3s_index_block_scores(
@@ -222,6 +248,7 @@ def m3s_block_topk(block_scores, row_req, row_len, B: int, bt_stride: int, topk:
 def m3s_verify_score_topk(q_idx, w, codes, scales, block_table, cu_q, row_len, max_q: int,
                           topk: int, topk_ids=None, ws=None, err=None, stream=None,
                           init_blocks: int = 0, local_blocks: int = 0):
+    _index_inputs(q_idx, w, block_table, cu_q, row_len)
     R, Hi = q_idx.shape[0], q_idx.shape[1]
     B, bt_stride = block_table.shape
     if topk_ids is None:
@@ -240,6 +267,11 @@ def m3s_verify_score_topk(q_idx, w, codes, scales, block_table, cu_q, row_len, m
 def m3s_sparse_attention(q, hkv: int, k_codes, k_scales, v_codes, v_scales, block_table, row_req,
                          row_len, topk_ids, sm_scale: float | None = None, out=None, lse=None,
                          ws=None, err=None, stream=None):
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise TypeError("q must be a contiguous bfloat16 tensor [R, Hq, 128]")
+    for t in (block_table, row_req, row_len, topk_ids):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError("block tables, row maps and top-k ids must be contiguous int32 tensors")
     R, Hq = q.shape[0], q.shape[1]
     B, bt_stride = block_table.shape
     topk = topk_ids.shape[1]

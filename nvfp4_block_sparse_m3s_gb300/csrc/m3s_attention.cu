@@ -18,6 +18,11 @@
 // head-dim order (each thread reads one 16-byte chunk of a token, the q
 // fragments follow the same order), V two tokens at a time with the nibbles of
 // the same byte interleaved (each n8 tile covers every other dimension).
+//
+// MXFP4 K/V (one E8M0 scale per 32 elements) run the same kernel on bf16
+// operands: e2m1 x 2^(E-127) is exact in bf16 over E8M0's whole range (in fp16
+// it is not), the query is used as the BF16 it arrives in, and the softmax
+// weights are rounded to bf16 for the P V product.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -78,7 +83,43 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Two e2m1 codes -> bf16x2, exactly: the fp16 conversion, then each nonzero
+// half's exponent re-biased from 15 to 127 (the mantissa keeps its top bits).
+__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t two) {
+  const uint32_t h = e2m1x2_to_f16x2(two);
+  const uint32_t mag = h & 0x7FFF7FFFu;
+  const uint32_t nz = __vcmpne2(mag, 0u);
+  return (h & 0x80008000u) | ((((mag >> 3) & 0x0FFF0FFFu) + 0x38003800u) & nz);
+}
+
+// bf16 bits of the E8M0 scale 2^(e - 127) (e = 0 is the subnormal 2^-127).
+__device__ __forceinline__ uint32_t e8m0_to_bf16(uint32_t e) { return e ? (e << 7) : 0x0040u; }
+
+__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <bool MX>
 __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a) {
+  // a page's K (or V) scale bytes, and where they sit in a stage
+  constexpr int kPageScaleB = MX ? kMxPageScaleBytes : kPageScaleBytes;
+  constexpr int kStageB = 2 * (kPageCodeBytes + kPageScaleB);
   __shared__ AttnSmem sm;
   const int split = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -105,10 +146,17 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       uint2 v0 = make_uint2(0u, 0u), v1 = make_uint2(0u, 0u);
       if (h0 < a.G) v0 = *reinterpret_cast<const uint2*>(q0 + 4 * j);
       if (h1 < a.G) v1 = *reinterpret_cast<const uint2*>(q1 + 4 * j);
-      qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
-      qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
-      qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
-      qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
+      if constexpr (MX) {   // bf16 operands: the query as it arrives
+        qa[j][0] = v0.x;
+        qa[j][1] = v1.x;
+        qa[j][2] = v0.y;
+        qa[j][3] = v1.y;
+      } else {
+        qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
+        qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
+        qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
+        qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
+      }
     }
   }
 
@@ -120,13 +168,13 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     const size_t rec = static_cast<size_t>(page) * a.Hkv + kvh;
     uint8_t* dst = sm.stage[s];
     fence_proxy_async();
-    mbar_expect_tx(&sm.bar[s], kBlockBytes);
+    mbar_expect_tx(&sm.bar[s], kStageB);
     bulk_g2s(dst, a.kc + rec * kPageCodeBytes, kPageCodeBytes, &sm.bar[s]);
-    bulk_g2s(dst + kPageCodeBytes, a.ks + rec * kPageScaleBytes, kPageScaleBytes, &sm.bar[s]);
-    bulk_g2s(dst + kPageCodeBytes + kPageScaleBytes, a.vc + rec * kPageCodeBytes, kPageCodeBytes,
+    bulk_g2s(dst + kPageCodeBytes, a.ks + rec * kPageScaleB, kPageScaleB, &sm.bar[s]);
+    bulk_g2s(dst + kPageCodeBytes + kPageScaleB, a.vc + rec * kPageCodeBytes, kPageCodeBytes,
              &sm.bar[s]);
-    bulk_g2s(dst + 2 * kPageCodeBytes + kPageScaleBytes, a.vs + rec * kPageScaleBytes,
-             kPageScaleBytes, &sm.bar[s]);
+    bulk_g2s(dst + 2 * kPageCodeBytes + kPageScaleB, a.vs + rec * kPageScaleB, kPageScaleB,
+             &sm.bar[s]);
   };
   if (warp == 0) {
     __syncwarp();   // the barriers lane 0 initialised
@@ -195,7 +243,7 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     if (!aborted) {
       const uint8_t* kcs = sm.stage[s];
       const uint8_t* kss = kcs + kPageCodeBytes;
-      const uint8_t* vcs = kss + kPageScaleBytes;
+      const uint8_t* vcs = kss + kPageScaleB;
       const uint8_t* vss = vcs + kPageCodeBytes;
       const int ntok = sm.ntok[i];
       const int tb = warp * 32;  // this warp's first token in the block
@@ -207,16 +255,29 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
         sacc[c][0] = sacc[c][1] = sacc[c][2] = sacc[c][3] = 0.f;
         const int tok = tb + 8 * c + g;
         const uint4 kw = *reinterpret_cast<const uint4*>(kcs + tok * kCodeBytes + 16 * t);
-        const uint32_t sc = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(kss + tok * kScaleBytes + 2 * t));
-        const uint32_t s0 = bcast_lo(sc), s1 = bcast_hi(sc);
         const uint32_t wv[4] = {kw.x, kw.y, kw.z, kw.w};
+        if constexpr (MX) {
+          // the thread's 16-byte chunk (dims 32t .. 32t+31) is E8M0 group t
+          const uint32_t e = e8m0_to_bf16(kss[tok * kMxScaleBytes + t]);
+          const uint32_t sj = e | (e << 16);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
-          const uint32_t sj = j < 4 ? s0 : s1;
-          const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
-          const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
-          mma16816(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
+            const uint32_t b0 = hmul2_bf16(e2m1x2_to_bf16x2(x & 0xFFu), sj);
+            const uint32_t b1 = hmul2_bf16(e2m1x2_to_bf16x2((x >> 8) & 0xFFu), sj);
+            mma16816_bf16(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+          }
+        } else {
+          const uint32_t sc = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(kss + tok * kScaleBytes + 2 * t));
+          const uint32_t s0 = bcast_lo(sc), s1 = bcast_hi(sc);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
+            const uint32_t sj = j < 4 ? s0 : s1;
+            const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
+            const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
+            mma16816(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+          }
         }
       }
       // ---- online softmax (log2 domain), causal mask inside the block ----
@@ -266,18 +327,26 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       // ---- O += P V over the warp's 32 tokens (2 k-steps of 16) ----
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        const uint32_t pa0 = pack_f16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
-        const uint32_t pa1 = pack_f16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
-        const uint32_t pa2 = pack_f16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-        const uint32_t pa3 = pack_f16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+        const auto pack = [](float lo, float hi) { return MX ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi); };
+        const uint32_t pa0 = pack(sacc[2 * kk][0], sacc[2 * kk][1]);
+        const uint32_t pa1 = pack(sacc[2 * kk][2], sacc[2 * kk][3]);
+        const uint32_t pa2 = pack(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+        const uint32_t pa3 = pack(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
         const int t0 = tb + 16 * kk + 2 * t;  // tokens t0, t0+1 (b0) and t0+8, t0+9 (b1)
         // bytes 8g .. 8g+7 of each token: dims 16g .. 16g+15 (scale group g)
         const uint2 v0 = *reinterpret_cast<const uint2*>(vcs + t0 * kCodeBytes + 8 * g);
         const uint2 v1 = *reinterpret_cast<const uint2*>(vcs + (t0 + 1) * kCodeBytes + 8 * g);
         const uint2 v2 = *reinterpret_cast<const uint2*>(vcs + (t0 + 8) * kCodeBytes + 8 * g);
         const uint2 v3 = *reinterpret_cast<const uint2*>(vcs + (t0 + 9) * kCodeBytes + 8 * g);
-        const uint32_t s01 = e4m3x2_to_f16x2(vss[t0 * kScaleBytes + g] | (vss[(t0 + 1) * kScaleBytes + g] << 8));
-        const uint32_t s23 = e4m3x2_to_f16x2(vss[(t0 + 8) * kScaleBytes + g] | (vss[(t0 + 9) * kScaleBytes + g] << 8));
+        uint32_t s01, s23;   // the (token, token + 1) scale pairs of these dims
+        if constexpr (MX) {   // dims 16g .. 16g+15 lie in E8M0 group g / 2
+          const int gm = g >> 1;
+          s01 = e8m0_to_bf16(vss[t0 * kMxScaleBytes + gm]) | (e8m0_to_bf16(vss[(t0 + 1) * kMxScaleBytes + gm]) << 16);
+          s23 = e8m0_to_bf16(vss[(t0 + 8) * kMxScaleBytes + gm]) | (e8m0_to_bf16(vss[(t0 + 9) * kMxScaleBytes + gm]) << 16);
+        } else {
+          s01 = e4m3x2_to_f16x2(vss[t0 * kScaleBytes + g] | (vss[(t0 + 1) * kScaleBytes + g] << 8));
+          s23 = e4m3x2_to_f16x2(vss[(t0 + 8) * kScaleBytes + g] | (vss[(t0 + 9) * kScaleBytes + g] << 8));
+        }
         const uint32_t wa[2] = {v0.x, v0.y}, wb[2] = {v1.x, v1.y};
         const uint32_t wc[2] = {v2.x, v2.y}, wd[2] = {v3.x, v3.y};
 #pragma unroll
@@ -292,12 +361,21 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
           for (int bb = 0; bb < 4; ++bb) {
             const int jj = 4 * hw + bb;
             const uint32_t sh = 8 * bb;
-            const uint32_t be0 = hmul2(e2m1x2_to_f16x2((lo01 >> sh) & 0xFFu), s01);
-            const uint32_t be1 = hmul2(e2m1x2_to_f16x2((lo23 >> sh) & 0xFFu), s23);
-            const uint32_t bo0 = hmul2(e2m1x2_to_f16x2((hi01 >> sh) & 0xFFu), s01);
-            const uint32_t bo1 = hmul2(e2m1x2_to_f16x2((hi23 >> sh) & 0xFFu), s23);
-            mma16816(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
-            mma16816(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
+            if constexpr (MX) {
+              const uint32_t be0 = hmul2_bf16(e2m1x2_to_bf16x2((lo01 >> sh) & 0xFFu), s01);
+              const uint32_t be1 = hmul2_bf16(e2m1x2_to_bf16x2((lo23 >> sh) & 0xFFu), s23);
+              const uint32_t bo0 = hmul2_bf16(e2m1x2_to_bf16x2((hi01 >> sh) & 0xFFu), s01);
+              const uint32_t bo1 = hmul2_bf16(e2m1x2_to_bf16x2((hi23 >> sh) & 0xFFu), s23);
+              mma16816_bf16(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
+              mma16816_bf16(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
+            } else {
+              const uint32_t be0 = hmul2(e2m1x2_to_f16x2((lo01 >> sh) & 0xFFu), s01);
+              const uint32_t be1 = hmul2(e2m1x2_to_f16x2((lo23 >> sh) & 0xFFu), s23);
+              const uint32_t bo0 = hmul2(e2m1x2_to_f16x2((hi01 >> sh) & 0xFFu), s01);
+              const uint32_t bo1 = hmul2(e2m1x2_to_f16x2((hi23 >> sh) & 0xFFu), s23);
+              mma16816(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
+              mma16816(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
+            }
           }
         }
       }
@@ -423,8 +501,8 @@ int attention_splits(int R, int Hkv, int topk, int* ips) {
 
 }  // namespace m3s
 
-extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_nvfp4_plane k,
-                                    m3s_nvfp4_plane v, const int32_t* block_table,
+extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k,
+                                    m3s_fp4_plane v, const int32_t* block_table,
                                     int32_t bt_stride, int32_t B, const int32_t* row_req,
                                     const int32_t* row_len, const int32_t* topk_ids, int32_t topk,
                                     int32_t R, float sm_scale, uint16_t* out, float* lse, void* ws,
@@ -435,6 +513,10 @@ extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, 
   if (Hq / Hkv > M3S_MAX_GQA || topk > M3S_MAX_TOPK) return M3S_ERR_UNSUPPORTED;
   if (k.num_heads != Hkv || v.num_heads != Hkv || k.num_pages != v.num_pages || k.num_pages < 0)
     return M3S_ERR_INVALID;
+  if ((k.format != M3S_FMT_NVFP4 && k.format != M3S_FMT_MXFP4) ||
+      (v.format != M3S_FMT_NVFP4 && v.format != M3S_FMT_MXFP4))
+    return M3S_ERR_INVALID;
+  if (k.format != v.format) return M3S_ERR_UNSUPPORTED;   // one format per cache
   if (R == 0) return M3S_OK;
   if (R > 65535) return M3S_ERR_UNSUPPORTED;
   if (!q || !out || !row_req || !row_len || (topk > 0 && !topk_ids)) return M3S_ERR_INVALID;
@@ -450,7 +532,8 @@ extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, 
   AttnArgs a{q, Hq, Hkv, Hq / Hkv, k.codes, k.scales, v.codes, v.scales, k.num_pages, block_table,
              bt_stride, row_req, row_len, topk_ids, topk, R, B,
              sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err};
-  if (launch_kernel(attention_kernel, dim3(nsplit, Hkv, R), dim3(kAttThreads), 0,
+  const auto kernel = k.format == M3S_FMT_MXFP4 ? attention_kernel<true> : attention_kernel<false>;
+  if (launch_kernel(kernel, dim3(nsplit, Hkv, R), dim3(kAttThreads), 0,
                     static_cast<cudaStream_t>(stream), nsplit, a) != cudaSuccess)
     return M3S_ERR_LAUNCH;
   return M3S_OK;

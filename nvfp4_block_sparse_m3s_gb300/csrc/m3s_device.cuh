@@ -19,6 +19,8 @@ constexpr int kCodeBytes = 64;     // e2m1 payload per token and head
 constexpr int kScaleBytes = 8;     // E4M3 scales per token and head
 constexpr int kPageCodeBytes = kPage * kCodeBytes;    // 8192
 constexpr int kPageScaleBytes = kPage * kScaleBytes;  // 1024
+constexpr int kMxScaleBytes = 4;   // MXFP4: E8M0 scales per token and head (one per 32)
+constexpr int kMxPageScaleBytes = kPage * kMxScaleBytes;  // 512
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

@@ -595,10 +595,11 @@ int launch_topk(const float* bscores, int bs_stride, const int32_t* row_req, con
              : M3S_ERR_LAUNCH;
 }
 
-int check_common(const uint16_t* q_idx, const float* w, int Hi, const m3s_nvfp4_plane& idx_k,
+int check_common(const uint16_t* q_idx, const float* w, int Hi, const m3s_fp4_plane& idx_k,
                  const int32_t* block_table, int bt_stride, int R, int B, int topk,
                  const int32_t* topk_ids) {
   if (R < 0 || B < 0 || topk < 0 || bt_stride < 0) return M3S_ERR_INVALID;
+  if (idx_k.format != M3S_FMT_NVFP4 && idx_k.format != M3S_FMT_MXFP4) return M3S_ERR_INVALID;
   if (Hi < 1 || Hi > M3S_MAX_INDEX_HEADS || topk > M3S_MAX_TOPK) return M3S_ERR_UNSUPPORTED;
   if (idx_k.num_heads != 1 || idx_k.num_pages < 0) return M3S_ERR_INVALID;
   if (R == 0) return M3S_OK;
@@ -613,7 +614,7 @@ int check_common(const uint16_t* q_idx, const float* w, int Hi, const m3s_nvfp4_
 }  // namespace m3s
 
 extern "C" int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int32_t Hi,
-                                      m3s_nvfp4_plane idx_k, const int32_t* block_table,
+                                      m3s_fp4_plane idx_k, const int32_t* block_table,
                                       int32_t bt_stride, const int32_t* row_req,
                                       const int32_t* row_len, int32_t R, int32_t B,
                                       float* block_scores, int32_t bs_stride, int32_t* err,
@@ -627,7 +628,8 @@ extern "C" int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int
   if (R > kMaxTiles) return M3S_ERR_UNSUPPORTED;
   if (B == 0) return M3S_OK;
   ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-              row_req, nullptr, row_len, R, B, R, 1, block_scores, bs_stride, err};
+              row_req, nullptr, row_len, R, B, R, 1, block_scores, bs_stride, err,
+              idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
   return launch_score_decode(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -647,7 +649,7 @@ extern "C" int m3s_block_topk(const float* block_scores, int32_t bs_stride, cons
 }
 
 extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
-                                    m3s_nvfp4_plane idx_k, const int32_t* block_table,
+                                    m3s_fp4_plane idx_k, const int32_t* block_table,
                                     int32_t bt_stride, const int32_t* row_req,
                                     const int32_t* row_len, int32_t R, int32_t B, int32_t topk,
                                     int32_t init_blocks, int32_t local_blocks, int32_t* topk_ids,
@@ -670,7 +672,8 @@ extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (B > 0) {
     ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-                row_req, nullptr, row_len, R, B, R, 1, bs, stride, err};
+                row_req, nullptr, row_len, R, B, R, 1, bs, stride, err,
+                idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
     rc = launch_score_decode(a, st);
     if (rc != M3S_OK) return rc;
   }
@@ -679,7 +682,7 @@ extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32
 }
 
 extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
-                                     m3s_nvfp4_plane idx_k, const int32_t* block_table,
+                                     m3s_fp4_plane idx_k, const int32_t* block_table,
                                      int32_t bt_stride, const int32_t* cu_q,
                                      const int32_t* row_len, int32_t B, int32_t R, int32_t max_q,
                                      int32_t topk, int32_t init_blocks, int32_t local_blocks,
@@ -689,6 +692,7 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
   int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk_ids);
   if (rc != M3S_OK || R == 0) return rc;
   if (!cu_q || !row_len || max_q < 0 || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
+  if (idx_k.format != M3S_FMT_NVFP4) return M3S_ERR_UNSUPPORTED;   // this scorer reads NVFP4 only
   if (topk == 0 || B == 0) {
     if (topk > 0) {
       // no requests: every row is padding
@@ -762,7 +766,7 @@ float* static_scratch() {
 }  // namespace m3s
 
 extern "C" int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t Hi,
-                                           m3s_nvfp4_plane idx_k, const int32_t* block_table,
+                                           m3s_fp4_plane idx_k, const int32_t* block_table,
                                            int32_t bt_stride, const int32_t* row_req,
                                            const int32_t* row_len, int32_t R, int32_t B,
                                            int32_t topk, int32_t* topk_ids, int32_t* err,
@@ -782,7 +786,8 @@ extern "C" int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (B > 0) {
     ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-                row_req, nullptr, row_len, R, B, R, 1, bs, stride, err};
+                row_req, nullptr, row_len, R, B, R, 1, bs, stride, err,
+                idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
     rc = launch_score_decode(a, st);
     if (rc != M3S_OK) return rc;
   }

@@ -26,6 +26,7 @@ struct ScoreArgs {
   float* bscores;
   int bs_stride;
   int32_t* err;
+  int mx;                  // 1: the index plane is MXFP4 (E8M0 per 32), else NVFP4
 };
 
 template <int QT>

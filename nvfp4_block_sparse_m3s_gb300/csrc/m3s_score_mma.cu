@@ -14,6 +14,12 @@
 // every thread's key bytes are one contiguous 16-byte chunk (the query
 // fragments use the same order, which leaves every dot product unchanged).
 //
+// MXFP4 keys (one E8M0 scale per 32 elements) take the same loop: a thread's
+// 16-byte chunk of a key is exactly one of its four 32-element groups, so the
+// chunk is scaled by 2^(E_t - E_max) (E_max = the key's largest exponent; exact
+// in fp16 while the key's exponents span at most 23) and the key's score by
+// 2^(E_max - 127) in fp32 after the head sum.
+//
 // Each of the 16 warps streams whole blocks of its share (every 16th block of
 // the CTA's contiguous range) as two halves of 64 keys through its own
 // double-buffered shared-memory stages, filled by 1-D bulk copies (TMA) that
@@ -69,7 +75,22 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// fp16x2 broadcast of 2^-d (d >= 0): normal down to 2^-14, subnormal to 2^-24,
+// zero beyond.
+__device__ __forceinline__ uint32_t pow2_neg_f16x2(int d) {
+  const uint32_t h = d <= 14 ? static_cast<uint32_t>(15 - d) << 10 : (d <= 24 ? 1u << (24 - d) : 0u);
+  return h | (h << 16);
+}
+
+// 2^e as fp32 for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float pow2_f32(int e) {
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+template <bool MX>
 __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreArgs a) {
+  constexpr int kKeyScaleBytes = MX ? kMxScaleBytes : kScaleBytes;
+  constexpr int kHalfScaleB = kHalfKeys * kKeyScaleBytes;  // 256 or 512
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
   int* pre = reinterpret_cast<int*>(smem_raw + sizeof(DecodeSmem));
@@ -156,13 +177,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
         } else {
           // (no proxy fence: every generic read of this stage has returned, its
           // values having gone through the mma and the shuffles above)
-          mbar_expect_tx(&sm.bar[warp][s], kStageBytes);
+          mbar_expect_tx(&sm.bar[warp][s], kHalfCodeBytes + kHalfScaleB);
           bulk_g2s(sm.stage[warp][s],
                    a.codes + static_cast<size_t>(page) * kPageCodeBytes + half * kHalfCodeBytes,
                    kHalfCodeBytes, &sm.bar[warp][s]);
           bulk_g2s(sm.stage[warp][s] + kHalfCodeBytes,
-                   a.scales + static_cast<size_t>(page) * kPageScaleBytes + half * kHalfScaleBytes,
-                   kHalfScaleBytes, &sm.bar[warp][s]);
+                   a.scales + static_cast<size_t>(page) * (kPage * kKeyScaleBytes) + half * kHalfScaleB,
+                   kHalfScaleB, &sm.bar[warp][s]);
           ok = 1;
         }
       }
@@ -230,10 +251,27 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
           const int key0 = mt * 16 + g;
           const uint4 ca = *reinterpret_cast<const uint4*>(cs + key0 * kCodeBytes + 16 * t);
           const uint4 cb = *reinterpret_cast<const uint4*>(cs + (key0 + 8) * kCodeBytes + 16 * t);
-          const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + key0 * kScaleBytes + 2 * t));
-          const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + (key0 + 8) * kScaleBytes + 2 * t));
-          const uint32_t sa0 = bcast_lo(sa), sa1 = bcast_hi(sa);
-          const uint32_t sb0 = bcast_lo(sb), sb1 = bcast_hi(sb);
+          uint32_t sa0, sa1, sb0, sb1;
+          float fa = 1.f, fb = 1.f;   // MXFP4: the keys' 2^(E_max - 127)
+          if constexpr (MX) {
+            // the key's four E8M0 bytes; this thread's chunk is group t
+            const uint32_t wa4 = *reinterpret_cast<const uint32_t*>(ss + key0 * kMxScaleBytes);
+            const uint32_t wb4 = *reinterpret_cast<const uint32_t*>(ss + (key0 + 8) * kMxScaleBytes);
+            const uint32_t ma = __vmaxu4(wa4, wa4 >> 16), mb = __vmaxu4(wb4, wb4 >> 16);
+            const int ea = static_cast<int>(max(ma & 0xFFu, (ma >> 8) & 0xFFu));
+            const int eb = static_cast<int>(max(mb & 0xFFu, (mb >> 8) & 0xFFu));
+            sa0 = sa1 = pow2_neg_f16x2(ea - static_cast<int>((wa4 >> (8 * t)) & 0xFFu));
+            sb0 = sb1 = pow2_neg_f16x2(eb - static_cast<int>((wb4 >> (8 * t)) & 0xFFu));
+            fa = pow2_f32(ea - 127);
+            fb = pow2_f32(eb - 127);
+          } else {
+            const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + key0 * kScaleBytes + 2 * t));
+            const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + (key0 + 8) * kScaleBytes + 2 * t));
+            sa0 = bcast_lo(sa);
+            sa1 = bcast_hi(sa);
+            sb0 = bcast_lo(sb);
+            sb1 = bcast_hi(sb);
+          }
           const uint32_t wa[4] = {ca.x, ca.y, ca.z, ca.w};
           const uint32_t wb[4] = {cb.x, cb.y, cb.z, cb.w};
           float acc[2][4];
@@ -271,6 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
           p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
           p0 += __shfl_xor_sync(0xffffffffu, p0, 2);
           p1 += __shfl_xor_sync(0xffffffffu, p1, 2);
+          if constexpr (MX) {
+            p0 *= fa;
+            p1 *= fb;
+          }
           const int tok0 = blk * kPage + half * kHalfKeys + key0;
           if (tok0 < rlen) best = fmaxf(best, p0);
           if (tok0 + 8 < rlen) best = fmaxf(best, p1);
@@ -299,10 +341,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
 int launch_score_decode(const ScoreArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(DecodeSmem) + (a.ntiles + 1) * 4 + 16;
   if (smem > 227 * 1024) return M3S_ERR_UNSUPPORTED;
-  if (cudaFuncSetAttribute(score_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const auto kernel = a.mx ? score_decode_kernel<true> : score_decode_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
-  return launch_kernel(score_decode_kernel, dim3(sm_count()), dim3(kThreads), smem, st, 0, a) ==
+  return launch_kernel(kernel, dim3(sm_count()), dim3(kThreads), smem, st, 0, a) ==
                  cudaSuccess
              ? M3S_OK
              : M3S_ERR_LAUNCH;

@@ -1,10 +1,13 @@
-// Quantise-store of BF16 rows into paged NVFP4 planes, and the row map.
+// Quantise-store of BF16 rows into paged NVFP4 or MXFP4 planes, and the row map.
 //
 // Quantisation: "[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache"
 // (ROCm/ATOM #2744), Design / Write path -- per 16 elements
 // scale = e4m3(amax / 6), codes rounded half-to-even on the e2m1 grid and
-// saturating at 6. Row map: same page, Design / Attention (one launch maps
-// each row to its request and causal length).
+// saturating at 6. MXFP4 (same page, Follow-up: MXFP4 caches) -- one E8M0
+// scale per 32 elements, 2^E with E = floor(log2(amax)) - 2 clamped to
+// [-127, 127] (the OCP MX shared exponent), codes |x| / 2^E rounded the same
+// way. Row map: same page, Design / Attention (one launch maps each row to
+// its request and causal length).
 #include <cuda_runtime.h>
 
 #include "m3s_device.cuh"
@@ -43,6 +46,23 @@ __device__ __forceinline__ void quantise_group(const uint32_t (&x)[8], uint32_t&
   if (scale == 0.0f) lo = hi = 0;  // a zero (or underflowed) scale stores zero codes
 }
 
+// The MXFP4 shared exponent of a group whose largest magnitude has BF16 bits
+// am: floor(log2(amax)) - 2, clamped to E8M0's [-127, 127]. A normal BF16's
+// floor(log2) is its exponent field minus 127; a subnormal one is m * 2^-133
+// (m = its mantissa bits); amax 0 gives -127.
+__device__ __forceinline__ int mx_shared_exponent(uint32_t am) {
+  int fl;
+  if (am >= 0x80u) fl = static_cast<int>(am >> 7) - 127;
+  else if (am != 0) fl = (31 - __clz(static_cast<int>(am))) - 133;
+  else fl = -200;
+  return min(127, max(-127, fl - 2));
+}
+
+// 2^E as an fp32 value (exact: 2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float pow2_f32(int E) {
+  return E >= -126 ? __uint_as_float(static_cast<uint32_t>(E + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
 // Largest |x| of a group, as BF16 magnitude bits (non-negative floats order as
 // their bit patterns).
 __device__ __forceinline__ uint32_t group_amax_bits(const uint32_t (&x)[8]) {
@@ -52,15 +72,16 @@ __device__ __forceinline__ uint32_t group_amax_bits(const uint32_t (&x)[8]) {
   return max(m & 0xFFFFu, m >> 16);
 }
 
-// One thread quantises 32 elements (two scale groups) of one (row, head): it
-// reads 64 B, writes 16 B of codes with one 128-bit store, and the four
-// threads of a (row, head) gather their scale pairs so one of them writes the
-// 8 scale bytes with one 64-bit store.
+// One thread quantises 32 elements (two NVFP4 scale groups, one MXFP4 group)
+// of one (row, head): it reads 64 B, writes 16 B of codes with one 128-bit
+// store, and the four threads of a (row, head) gather their scale bytes so one
+// of them writes the record's 8 (NVFP4) or 4 (MXFP4) scale bytes in one store.
 struct StoreJob {
   const uint16_t* src;
   int64_t stride;
   int64_t total_threads;  // T * H * 4
   int32_t H;
+  int32_t mx;             // 1: MXFP4 plane
   uint8_t* codes;
   uint8_t* scales;
   int64_t capacity;       // num_pages * 128
@@ -98,6 +119,28 @@ __global__ void __launch_bounds__(256) nvfp4_store_kernel(const StoreBatch batch
   const uint4 v0 = __ldg(p), v1 = __ldg(p + 1), v2 = __ldg(p + 2), v3 = __ldg(p + 3);
   const uint32_t g0[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   const uint32_t g1[8] = {v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+  const int64_t page = slot / kPage, pos = slot % kPage;
+  const int64_t rec = (page * H + h) * kPage + pos;
+  const int lane = threadIdx.x & 31;
+  const unsigned mask = 0xFu << (lane & 28);
+
+  if (jb.mx) {
+    // one E8M0 group: the codes are |x| / 2^E on the grid, decided against the
+    // midpoints times 2^E (exact in fp32 down to 2^-129)
+    const int E = mx_shared_exponent(max(group_amax_bits(g0), group_amax_bits(g1)));
+    const float s = pow2_f32(E);
+    uint4 out;
+    quantise_group(g0, out.x, out.y, s);
+    quantise_group(g1, out.z, out.w, s);
+    *reinterpret_cast<uint4*>(codes + rec * kCodeBytes + part * 16) = out;
+    const uint32_t mine = static_cast<uint32_t>(E + 127);
+    const uint32_t p1 = __shfl_sync(mask, mine, (lane & 28) + 1);
+    const uint32_t p2 = __shfl_sync(mask, mine, (lane & 28) + 2);
+    const uint32_t p3 = __shfl_sync(mask, mine, (lane & 28) + 3);
+    if (part == 0)
+      *reinterpret_cast<uint32_t*>(scales + rec * kMxScaleBytes) = mine | (p1 << 8) | (p2 << 16) | (p3 << 24);
+    return;
+  }
 
   // scale = E4M3(amax / 6): the correctly rounded fp32 quotient cannot sit on or
   // across an E4M3 rounding boundary unless the exact quotient does (amax has 8
@@ -114,13 +157,8 @@ __global__ void __launch_bounds__(256) nvfp4_store_kernel(const StoreBatch batch
   uint4 out;
   quantise_group(g0, out.x, out.y, s0);
   quantise_group(g1, out.z, out.w, s1);
-
-  const int64_t page = slot / kPage, pos = slot % kPage;
-  const int64_t rec = (page * H + h) * kPage + pos;
   *reinterpret_cast<uint4*>(codes + rec * kCodeBytes + part * 16) = out;
 
-  const int lane = threadIdx.x & 31;
-  const unsigned mask = 0xFu << (lane & 28);
   const uint32_t mine = pair;
   const uint32_t p1 = __shfl_sync(mask, mine, (lane & 28) + 1);
   const uint32_t p2 = __shfl_sync(mask, mine, (lane & 28) + 2);
@@ -159,8 +197,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 namespace m3s {
 namespace {
-int check_job(const uint16_t* src, int64_t stride, int32_t H, const m3s_nvfp4_plane& dst) {
+int check_job(const uint16_t* src, int64_t stride, int32_t H, const m3s_fp4_plane& dst) {
   if (H <= 0 || dst.num_pages < 0 || dst.num_heads != H) return M3S_ERR_INVALID;
+  if (dst.format != M3S_FMT_NVFP4 && dst.format != M3S_FMT_MXFP4) return M3S_ERR_INVALID;
   if (!src || !dst.codes || !dst.scales) return M3S_ERR_INVALID;
   if (!aligned16(src) || !aligned16(dst.codes) || !aligned16(dst.scales)) return M3S_ERR_INVALID;
   if (stride < static_cast<int64_t>(H) * kHeadDim || (stride & 7)) return M3S_ERR_INVALID;
@@ -174,7 +213,8 @@ int launch_store(const m3s_store_job* jobs, int32_t njobs, int32_t T, const int6
   for (int i = 0; i < njobs; ++i) {
     const m3s_store_job& j = jobs[i];
     b.job[i] = StoreJob{j.src, j.src_row_stride, static_cast<int64_t>(T) * j.H * 4, j.H,
-                        j.dst.codes, j.dst.scales, static_cast<int64_t>(j.dst.num_pages) * kPage};
+                        j.dst.format == M3S_FMT_MXFP4 ? 1 : 0, j.dst.codes, j.dst.scales,
+                        static_cast<int64_t>(j.dst.num_pages) * kPage};
     most = b.job[i].total_threads > most ? b.job[i].total_threads : most;
   }
   const int64_t blocks = (most + 255) / 256;
@@ -188,7 +228,7 @@ int launch_store(const m3s_store_job* jobs, int32_t njobs, int32_t T, const int6
 }  // namespace m3s
 
 extern "C" int m3s_nvfp4_store(const uint16_t* src, int64_t src_row_stride, int32_t T, int32_t H,
-                               const int64_t* slot_mapping, m3s_nvfp4_plane dst, int32_t* err,
+                               const int64_t* slot_mapping, m3s_fp4_plane dst, int32_t* err,
                                void* stream) {
   using namespace m3s;
   if (T < 0 || H <= 0 || dst.num_pages < 0 || dst.num_heads != H) return M3S_ERR_INVALID;

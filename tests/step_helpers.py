@@ -31,15 +31,17 @@ def i64(x, dev="cuda"):
 
 
 class DeviceCache:
-    """The workload's paged K / V / index-K planes on the device, filled by the CUDA store."""
+    """The workload's paged K / V / index-K planes on the device, filled by the CUDA store.
 
-    def __init__(self, wl: W.Workload, dev="cuda"):
+    ``mx_kv`` / ``mx_index``: MXFP4 K/V or index planes (else NVFP4)."""
+
+    def __init__(self, wl: W.Workload, dev="cuda", mx_kv: bool = False, mx_index: bool = False):
         s = wl.spec
         self.wl = wl
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.kc, self.ks = M.new_plane(wl.num_pages, s.hkv, dev)
-        self.vc, self.vs = M.new_plane(wl.num_pages, s.hkv, dev)
-        self.ic, self.is_ = M.new_plane(wl.num_pages, 1, dev)
+        self.kc, self.ks = M.new_plane(wl.num_pages, s.hkv, dev, mx=mx_kv)
+        self.vc, self.vs = M.new_plane(wl.num_pages, s.hkv, dev, mx=mx_kv)
+        self.ic, self.is_ = M.new_plane(wl.num_pages, 1, dev, mx=mx_index)
         self.k_src = bf16_dev(wl.k_src, dev)
         self.v_src = bf16_dev(wl.v_src, dev)
         self.ik_src = bf16_dev(wl.ik_src, dev)
@@ -80,12 +82,12 @@ class DeviceCache:
 class OracleCache:
     """Oracle planes of the workload, quantised by the oracle (optionally only some requests)."""
 
-    def __init__(self, wl: W.Workload, requests=None):
+    def __init__(self, wl: W.Workload, requests=None, mx_kv: bool = False, mx_index: bool = False):
         s = wl.spec
         self.wl = wl
-        self.kc, self.ks = O.new_planes(wl.num_pages, s.hkv)
-        self.vc, self.vs = O.new_planes(wl.num_pages, s.hkv)
-        self.ic, self.is_ = O.new_planes(wl.num_pages, 1)
+        self.kc, self.ks = O.new_planes(wl.num_pages, s.hkv, mx=mx_kv)
+        self.vc, self.vs = O.new_planes(wl.num_pages, s.hkv, mx=mx_kv)
+        self.ic, self.is_ = O.new_planes(wl.num_pages, 1, mx=mx_index)
         if requests is None:
             tok = np.arange(wl.ntok)
         else:

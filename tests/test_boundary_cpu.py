@@ -78,3 +78,31 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.m3s_sparse_attention(None, 32, 1, P2, P2, None, 1, 1, None, None, None, 16, 1,
                                     ctypes.c_float(0.1), None, None, None, 0, None,
                                     None) == M.ERR_UNSUPPORTED
+
+
+def test_plane_format_rules(lib):
+    """A plane's format field: 0 = NVFP4, 1 = MXFP4, anything else is rejected; K and V
+    must share one format; the fused verify scorer reads NVFP4 only. All decided on
+    the host (the fake device pointers are never dereferenced)."""
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    fake = ctypes.c_void_p(1 << 20)
+    nv = M.Plane(fake, fake, 4, 1, M.FMT_NVFP4)
+    mx = M.Plane(fake, fake, 4, 1, M.FMT_MXFP4)
+    bad = M.Plane(fake, fake, 4, 1, 7)
+    assert ctypes.sizeof(M.Plane) == 32
+    # store: an unknown format is an invalid argument
+    assert lib.m3s_nvfp4_store(fake, 128, 4, 1, fake, bad, None, None) == M.ERR_INVALID
+    # index scorer: unknown format rejected; both known formats pass validation (checked
+    # with R = 0, which returns before any launch)
+    assert lib.m3s_index_score_topk(fake, fake, 16, bad, fake, 8, fake, fake, 1, 1, 8, 0, 0, fake,
+                                    None, fake, 1 << 20, None, None) == M.ERR_INVALID
+    for p in (nv, mx):
+        assert lib.m3s_index_score_topk(fake, fake, 16, p, fake, 8, fake, fake, 0, 1, 8, 0, 0, fake,
+                                        None, fake, 1 << 20, None, None) == M.OK
+    # fused verify: MXFP4 is not read by this scorer
+    assert lib.m3s_verify_score_topk(fake, fake, 16, mx, fake, 8, fake, fake, 1, 1, 8, 16, 0, 0,
+                                     fake, fake, 1 << 20, None, None) == M.ERR_UNSUPPORTED
+    # attention: mixed K / V formats refused, unknown format invalid
+    args = (fake, 1, 1, fake, fake, fake, 16, 1, ctypes.c_float(0.1), fake, None, None, 0, None, None)
+    assert lib.m3s_sparse_attention(fake, 16, 1, nv, mx, *args) == M.ERR_UNSUPPORTED
+    assert lib.m3s_sparse_attention(fake, 16, 1, bad, bad, *args) == M.ERR_INVALID
