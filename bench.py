@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--workload", default="skewed",
                     choices=["tiny", "decode", "verify", "skewed", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cache-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
+                    help="K / V / index-K record format (MXFP4: decode-shaped workloads only, "
+                         "the fused verify scorer reads NVFP4)")
     ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-reps", type=int, default=2, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -115,7 +118,12 @@ def job_rows_per_s(world: int, rows_per_rank: int, ms: float) -> float:
     return world * rows_per_rank / (ms * 1e-3)
 
 
-def workload_config(spec, ntok):
+#: bytes per token and head of a K, V or index-K record
+RECORD_BYTES = {"nvfp4": 72, "mxfp4": 68}
+
+
+def workload_config(spec, ntok, fmt="nvfp4"):
+    mx = fmt == "mxfp4"
     return {
         "workload": spec.description,
         "name": spec.name,
@@ -126,8 +134,12 @@ def workload_config(spec, ntok):
         "kv_heads": spec.hkv,
         "index_heads": spec.hi,
         "topk": spec.topk,
-        "cache_format": "NVFP4 (e2m1 + E4M3 per 16), 72 B per token and head",
-        "arithmetic": "NVFP4 decoded exactly to f16, f16 x f16 tensor-core products, f32 accumulation",
+        "cache_format": ("MXFP4 (e2m1 + E8M0 per 32), 68 B per token and head" if mx else
+                         "NVFP4 (e2m1 + E4M3 per 16), 72 B per token and head"),
+        "arithmetic": ("MXFP4 index keys decoded exactly to f16 (per-key exponent normalisation), "
+                       "f16 x f16 tensor-core products; K/V decoded exactly to bf16, bf16 x bf16 "
+                       "products; f32 accumulation" if mx else
+                       "NVFP4 decoded exactly to f16, f16 x f16 tensor-core products, f32 accumulation"),
         "l2": "flushed between timed steps: a 2 x L2 scratch written then read, outside the timed events",
     }
 
@@ -136,7 +148,7 @@ def workload_config(spec, ntok):
 # The CPU oracle arm (also the cpu_baseline sample)
 # --------------------------------------------------------------------------
 
-def oracle_sample(spec_name: str, reps: int):
+def oracle_sample(spec_name: str, reps: int, fmt: str = "nvfp4"):
     """Time the oracle's step for a bounded sample of the workload.
 
     The sample is the last request's step restricted to at most 8 of its
@@ -162,9 +174,10 @@ def oracle_sample(spec_name: str, reps: int):
     r0 = int(wl.cu_q[b])
     nsamp = min(qb, 8)
     sample = sorted({int(round(i * (qb - 1) / max(1, nsamp - 1))) for i in range(nsamp)} | {qb - 1})
-    kc, ks = O.new_planes(wl.num_pages, s.hkv)
-    vc, vs = O.new_planes(wl.num_pages, s.hkv)
-    ic, is_ = O.new_planes(wl.num_pages, 1)
+    mx = fmt == "mxfp4"
+    kc, ks = O.new_planes(wl.num_pages, s.hkv, mx=mx)
+    vc, vs = O.new_planes(wl.num_pages, s.hkv, mx=mx)
+    ic, is_ = O.new_planes(wl.num_pages, 1, mx=mx)
     srcs = {}
     for name, h, c, sc in (("k", s.hkv, kc, ks), ("v", s.hkv, vc, vs), ("ik", 1, ic, is_)):
         src = W.bf16_tensor(s.seed, name, (wl.ntok, h, 128), s.n_out, s.out_factor, rows=(t0, t1))
@@ -197,16 +210,16 @@ def oracle_sample(spec_name: str, reps: int):
 
 
 def run_oracle_leg(args):
-    t, desc, rows, scale = oracle_sample(args.workload, args.oracle_reps)
+    t, desc, rows, scale = oracle_sample(args.workload, args.oracle_reps, args.cache_format)
     print(json.dumps({"seconds_per_sample": t, "sample": desc, "rows": rows, "scale": scale,
                       "value": rows / (t * scale), "cores": 1}))
 
 
-def cpu_baseline(workload: str, reps: int = 2):
+def cpu_baseline(workload: str, reps: int = 2, fmt: str = "nvfp4"):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload",
-                        workload, "--oracle-reps", str(reps)], capture_output=True, text=True,
-                       env=env, timeout=900)
+                        workload, "--oracle-reps", str(reps), "--cache-format", fmt],
+                       capture_output=True, text=True, env=env, timeout=900)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
     d = json.loads(r.stdout.strip().splitlines()[-1])
@@ -223,10 +236,10 @@ def run_reference(args):
     spec = W.SPECS[args.workload]
     steps, warm = max(1, args.steps), max(0, args.warmup)
     # each step is one bounded sample (one request's step), extrapolated to the batch
-    t, desc, rows, scale = oracle_sample(args.workload, 1 + 0 * warm)
+    t, desc, rows, scale = oracle_sample(args.workload, 1 + 0 * warm, args.cache_format)
     samples = [t]
     for _ in range(min(steps, 3) - 1):
-        t2, _, _, _ = oracle_sample(args.workload, 1)
+        t2, _, _, _ = oracle_sample(args.workload, 1, args.cache_format)
         samples.append(t2)
     t_best = min(samples)
     value = rows / (t_best * scale)
@@ -235,7 +248,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": len(samples), "warmup": 0, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": workload_config(spec, int(sum(spec.ctx))),
+            "config": workload_config(spec, int(sum(spec.ctx)), args.cache_format),
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
                              "sample": desc + f"; {len(samples)} timed samples"},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
@@ -345,15 +358,20 @@ def run_ours(args):
     s = wl.spec
     R = s.rows
     fused = s.name in ("verify", "prefill")
+    mx = args.cache_format == "mxfp4"
+    if mx and fused:
+        raise SystemExit("--cache-format mxfp4 runs the decode-shaped workloads (tiny, decode, "
+                         "skewed): the fused verify scorer reads NVFP4 planes only")
+    rec_bytes = RECORD_BYTES[args.cache_format]
 
     def bf16(x):
         return torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev).view(torch.bfloat16)
 
     # ---- resident cache: planes filled by our store (setup, untimed) ----
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    kc, ks = M.new_plane(wl.num_pages, s.hkv, dev)
-    vc, vs = M.new_plane(wl.num_pages, s.hkv, dev)
-    ic, is_ = M.new_plane(wl.num_pages, 1, dev)
+    kc, ks = M.new_plane(wl.num_pages, s.hkv, dev, mx=mx)
+    vc, vs = M.new_plane(wl.num_pages, s.hkv, dev, mx=mx)
+    ic, is_ = M.new_plane(wl.num_pages, 1, dev, mx=mx)
     slot_all = torch.from_numpy(wl.slot_all).to(dev)
     for src, c, sc in ((wl.k_src, kc, ks), (wl.v_src, vc, vs), (wl.ik_src, ic, is_)):
         t = bf16(src)
@@ -517,9 +535,9 @@ def run_ours(args):
         distinct += len(set(int(x) for x in sel.ravel() if x >= 0))
     keys = int(np.sum(host_in["seq_len"].astype(np.int64)))
     nb_rows = int(np.sum((row_len.cpu().numpy().astype(np.int64) + 127) // 128))
-    score_bytes = keys * 72 + R * s.hi * (256 + 4) + nb_rows * 4
-    attn_bytes = distinct * 128 * 144 * s.hkv + R * s.hq * 256 * 2
-    store_bytes = R * (2 * s.hkv + 1) * (256 + 72)
+    score_bytes = keys * rec_bytes + R * s.hi * (256 + 4) + nb_rows * 4
+    attn_bytes = distinct * 128 * 2 * rec_bytes * s.hkv + R * s.hq * 256 * 2
+    store_bytes = R * (2 * s.hkv + 1) * (256 + rec_bytes)
     step_bytes = score_bytes + attn_bytes + store_bytes + R * 8
 
     # ---- timed region (device time, per step, L2 flushed between steps) ----
@@ -621,14 +639,15 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
+        "dtype": "f16/bf16" if mx else "f16",
         "data": "synthetic",
-        "config": workload_config(s, keys),
+        "config": workload_config(s, keys, args.cache_format),
         "achieved_gbs_step": world * step_bytes / (ms * 1e-3) / 1e9,
         "algorithmic_bytes_per_step": step_bytes,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak,
-                     "traffic": ncu_traffic(s.name, "score_kernel" if fused else "score_decode_kernel"),
+                     "traffic": ncu_traffic(s.name + ("-mxfp4" if mx else ""),
+                                            "score_kernel" if fused else "score_decode_kernel"),
                      "kernel": ("score_kernel<8> + topk (m3s_verify_score_topk)" if fused
                                 else "score_decode_kernel (m3s_index_block_scores)"),
                      "kernel_ms": score_ms, "bytes_per_launch": score_bytes,
@@ -645,7 +664,7 @@ def run_ours(args):
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload)
+        line["cpu_baseline"] = cpu_baseline(args.workload, fmt=args.cache_format)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

@@ -18,7 +18,9 @@
 // 16-byte chunk of a key is exactly one of its four 32-element groups, so the
 // chunk is scaled by 2^(E_t - E_max) (E_max = the key's largest exponent; exact
 // in fp16 while the key's exponents span at most 23) and the key's score by
-// 2^(E_max - 127) in fp32 after the head sum.
+// 2^(E_max - 127) in fp32 after the head sum. When a half lands, its warp turns
+// each key's four E8M0 bytes into those factors once (two keys per lane, into a
+// per-warp scratch), so the tile loop only loads them.
 //
 // Each of the 16 warps streams whole blocks of its share (every 16th block of
 // the CTA's contiguous range) as two halves of 64 keys through its own
@@ -46,6 +48,13 @@ constexpr int kStageBytes = kHalfCodeBytes + kHalfScaleBytes; // 4608
 constexpr int kQFragWords = 8 * 2 * 32;                       // k-steps x n-tiles x lanes (uint2)
 constexpr int kSegCost = 6;                                   // set-up of a row segment, in blocks
 static_assert(kQFragWords == kThreads, "one query fragment word per thread");
+
+// MXFP4 factors of one warp's current half: per key the fp16x2 factor of each
+// of its four groups and its fp32 2^(E_max - 127).
+struct MxScratch {
+  uint32_t fac[kWarps][kHalfKeys][4];
+  float key[kWarps][kHalfKeys];
+};
 
 struct __align__(16) DecodeSmem {
   uint8_t stage[kWarps][kStages][kStageBytes];
@@ -93,7 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
   constexpr int kHalfScaleB = kHalfKeys * kKeyScaleBytes;  // 256 or 512
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
-  int* pre = reinterpret_cast<int*>(smem_raw + sizeof(DecodeSmem));
+  MxScratch& mxs = *reinterpret_cast<MxScratch*>(smem_raw + sizeof(DecodeSmem));   // MX only
+  int* pre = reinterpret_cast<int*>(smem_raw + sizeof(DecodeSmem) + (MX ? sizeof(MxScratch) : 0));
   __shared__ int red[kWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -246,6 +256,21 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
       if (have) {
         const uint8_t* cs = sm.stage[warp][s];
         const uint8_t* ss = cs + kHalfCodeBytes;
+        if constexpr (MX) {
+          // the half's per-key factors, two keys per lane (the previous half's
+          // readers are this warp's lanes, all past the loop below)
+#pragma unroll
+          for (int kk = lane; kk < kHalfKeys; kk += 32) {
+            const uint32_t w4 = *reinterpret_cast<const uint32_t*>(ss + kk * kMxScaleBytes);
+            const uint32_t m2 = __vmaxu4(w4, w4 >> 16);
+            const int em = static_cast<int>(max(m2 & 0xFFu, (m2 >> 8) & 0xFFu));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              mxs.fac[warp][kk][j] = pow2_neg_f16x2(em - static_cast<int>((w4 >> (8 * j)) & 0xFFu));
+            mxs.key[warp][kk] = pow2_f32(em - 127);
+          }
+          __syncwarp();
+        }
 #pragma unroll 1
         for (int mt = 0; mt < kHalfKeys / 16; ++mt) {
           const int key0 = mt * 16 + g;
@@ -253,17 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
           const uint4 cb = *reinterpret_cast<const uint4*>(cs + (key0 + 8) * kCodeBytes + 16 * t);
           uint32_t sa0, sa1, sb0, sb1;
           float fa = 1.f, fb = 1.f;   // MXFP4: the keys' 2^(E_max - 127)
-          if constexpr (MX) {
-            // the key's four E8M0 bytes; this thread's chunk is group t
-            const uint32_t wa4 = *reinterpret_cast<const uint32_t*>(ss + key0 * kMxScaleBytes);
-            const uint32_t wb4 = *reinterpret_cast<const uint32_t*>(ss + (key0 + 8) * kMxScaleBytes);
-            const uint32_t ma = __vmaxu4(wa4, wa4 >> 16), mb = __vmaxu4(wb4, wb4 >> 16);
-            const int ea = static_cast<int>(max(ma & 0xFFu, (ma >> 8) & 0xFFu));
-            const int eb = static_cast<int>(max(mb & 0xFFu, (mb >> 8) & 0xFFu));
-            sa0 = sa1 = pow2_neg_f16x2(ea - static_cast<int>((wa4 >> (8 * t)) & 0xFFu));
-            sb0 = sb1 = pow2_neg_f16x2(eb - static_cast<int>((wb4 >> (8 * t)) & 0xFFu));
-            fa = pow2_f32(ea - 127);
-            fb = pow2_f32(eb - 127);
+          if constexpr (MX) {   // this thread's chunk is group t of keys key0, key0 + 8
+            sa0 = sa1 = mxs.fac[warp][key0][t];
+            sb0 = sb1 = mxs.fac[warp][key0 + 8][t];
+            fa = mxs.key[warp][key0];
+            fb = mxs.key[warp][key0 + 8];
           } else {
             const uint32_t sa = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + key0 * kScaleBytes + 2 * t));
             const uint32_t sb = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(ss + (key0 + 8) * kScaleBytes + 2 * t));
@@ -339,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
 }  // namespace
 
 int launch_score_decode(const ScoreArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(DecodeSmem) + (a.ntiles + 1) * 4 + 16;
+  const size_t smem = sizeof(DecodeSmem) + (a.mx ? sizeof(MxScratch) : 0) + (a.ntiles + 1) * 4 + 16;
   if (smem > 227 * 1024) return M3S_ERR_UNSUPPORTED;
   const auto kernel = a.mx ? score_decode_kernel<true> : score_decode_kernel<false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
