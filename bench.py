@@ -43,8 +43,7 @@ def parse():
                     choices=["tiny", "decode", "verify", "skewed", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cache-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
-                    help="K / V / index-K record format (MXFP4: decode-shaped workloads only, "
-                         "the fused verify scorer reads NVFP4)")
+                    help="K / V / index-K record format")
     ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-reps", type=int, default=2, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -359,9 +358,6 @@ def run_ours(args):
     R = s.rows
     fused = s.name in ("verify", "prefill")
     mx = args.cache_format == "mxfp4"
-    if mx and fused:
-        raise SystemExit("--cache-format mxfp4 runs the decode-shaped workloads (tiny, decode, "
-                         "skewed): the fused verify scorer reads NVFP4 planes only")
     rec_bytes = RECORD_BYTES[args.cache_format]
 
     def bf16(x):

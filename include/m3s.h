@@ -253,9 +253,8 @@ int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t H
  *   cu_q int32 [B+1] groups rows by request (as for m3s_decode_rows),
  *   row_len int32 [R] their causal lengths (m3s_decode_rows),
  *   max_q >= every cu_q[b+1]-cu_q[b] (sizes the request-row tiling).
- * Other arguments as for m3s_index_score_topk. The index plane must be NVFP4
- * in this build (an MXFP4 plane returns M3S_ERR_UNSUPPORTED; its rows can go
- * through m3s_index_score_topk, which gives the same result).
+ * Other arguments as for m3s_index_score_topk (the index plane NVFP4 or MXFP4,
+ * with the same exactness).
  */
 int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                           m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,

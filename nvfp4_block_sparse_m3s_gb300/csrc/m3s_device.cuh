@@ -141,6 +141,24 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
   return r;
 }
 
+// fp16x2 broadcast of 2^-d (d >= 0): normal down to 2^-14, subnormal to 2^-24,
+// zero beyond.
+__device__ __forceinline__ uint32_t pow2_neg_f16x2(int d) {
+  const uint32_t h = d <= 14 ? static_cast<uint32_t>(15 - d) << 10 : (d <= 24 ? 1u << (24 - d) : 0u);
+  return h | (h << 16);
+}
+
+// 2^e as fp32 for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float pow2_f32(int e) {
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// The largest of the four E8M0 bytes of a word (an MXFP4 record's exponents).
+__device__ __forceinline__ int e8m0_max4(uint32_t w4) {
+  const uint32_t m2 = __vmaxu4(w4, w4 >> 16);
+  return static_cast<int>(max(m2 & 0xFFu, (m2 >> 8) & 0xFFu));
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

@@ -106,10 +106,17 @@ __device__ __forceinline__ bool role_wait(ScoreSmem<QT>& sm, uint64_t* bar, uint
   return false;
 }
 
-template <int QT>
+// MX: MXFP4 index keys (one E8M0 scale per 32 elements). The dequantising
+// thread of a key scales each 32-dim chunk by 2^(E_chunk - E_max) in fp16 (exact
+// while the key's exponents span at most 23), and the key's epilogue thread
+// multiplies its head sums by 2^(E_max - 127), reading the key's four scale
+// bytes from the plane itself (L2-resident: the stage holding them is recycled
+// long before the epilogue runs).
+template <int QT, bool MX>
 __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
     score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap codes_map) {
   using C = Cfg<QT>;
+  constexpr int kPageScaleB = MX ? kMxPageScaleBytes : kPageScaleBytes;
   constexpr uint32_t kIdesc = idesc_f16(128, C::kN);
   extern __shared__ uint8_t smem_raw[];
   ScoreSmem<QT>& sm = *reinterpret_cast<ScoreSmem<QT>*>(
@@ -205,10 +212,10 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
             raise(a.err, M3S_DEVERR_PAGE);
             mbar_arrive(&sm.full[s]);  // nothing to copy: complete the phase empty
           } else {
-            mbar_expect_tx(&sm.full[s], kStageBytes);
+            mbar_expect_tx(&sm.full[s], kPageCodeBytes + kPageScaleB);
             tma_load_2d(sm.stage[s], &codes_map, 0, page * kPage, &sm.full[s]);
             bulk_g2s(sm.stage[s] + kPageCodeBytes,
-                     a.scales + static_cast<size_t>(page) * kPageScaleBytes, kPageScaleBytes,
+                     a.scales + static_cast<size_t>(page) * kPageScaleB, kPageScaleB,
                      &sm.full[s]);
           }
         }
@@ -257,6 +264,12 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
         const int g = g0 + j, ds = g % C::kND, ud = g / C::kND;
         const int blk = seg_lo + j;
         const int page = pw.get(bt_row + seg_lo, j, C::kNEpi, nseg, lane);
+        uint32_t kexp = 0;   // MX: the key's four E8M0 bytes, loaded while the MMA runs
+        if constexpr (MX) {
+          if (page >= 0 && page < a.num_pages)
+            kexp = *reinterpret_cast<const uint32_t*>(
+                a.scales + static_cast<size_t>(page) * kMxPageScaleBytes + (32 * wq + lane) * kMxScaleBytes);
+        }
         const bool ok = __all_sync(0xffffffffu, role_wait(sm, &sm.dfull[ds], ud & 1, a.err));
         tc_fence_after();
         const int tok = blk * kPage + (32 * wq + lane);
@@ -293,6 +306,11 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
               }
               sc[rho] = s0 + s1;
             }
+          }
+          if constexpr (MX) {   // the key's 2^(E_max - 127): positive, so it commutes with ReLU
+            const float kf = pow2_f32(e8m0_max4(kexp) - 127);
+#pragma unroll
+            for (int rho = 0; rho < QT; ++rho) sc[rho] *= kf;
           }
         } else {
           tc_fence_before();
@@ -338,14 +356,25 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
         if (page >= 0 && page < a.num_pages) {
           const uint8_t* cs = sm.stage[s];
           const uint8_t* ss = cs + kPageCodeBytes;
-          const uint2 sc = *reinterpret_cast<const uint2*>(ss + key * kScaleBytes);
-          const uint32_t spair[4] = {e4m3x2_to_f16x2(sc.x & 0xFFFFu), e4m3x2_to_f16x2(sc.x >> 16),
-                                     e4m3x2_to_f16x2(sc.y & 0xFFFFu), e4m3x2_to_f16x2(sc.y >> 16)};
+          uint32_t spair[4];
+          if constexpr (MX) {   // chunk c is E8M0 group c: one factor for both halves
+            const uint32_t w4 = *reinterpret_cast<const uint32_t*>(ss + key * kMxScaleBytes);
+            const int em = e8m0_max4(w4);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) spair[c] = pow2_neg_f16x2(em - static_cast<int>((w4 >> (8 * c)) & 0xFFu));
+          } else {
+            const uint2 sc = *reinterpret_cast<const uint2*>(ss + key * kScaleBytes);
+            spair[0] = e4m3x2_to_f16x2(sc.x & 0xFFFFu);
+            spair[1] = e4m3x2_to_f16x2(sc.x >> 16);
+            spair[2] = e4m3x2_to_f16x2(sc.y & 0xFFFFu);
+            spair[3] = e4m3x2_to_f16x2(sc.y >> 16);
+          }
           const uint32_t a_tm = tmem + as * C::kACols;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {  // chunk c = dims 32c .. 32c+31 = scale groups 2c, 2c+1
             const uint4 wv = *reinterpret_cast<const uint4*>(cs + key * kCodeBytes + 16 * (c ^ sw));
-            const uint32_t g0s = bcast_lo(spair[c]), g1s = bcast_hi(spair[c]);
+            const uint32_t g0s = MX ? spair[c] : bcast_lo(spair[c]);
+            const uint32_t g1s = MX ? spair[c] : bcast_hi(spair[c]);
             uint32_t v[16];
             e2m1x8_to_f16x2(wv.x, v[0], v[1], v[2], v[3]);
             e2m1x8_to_f16x2(wv.y, v[4], v[5], v[6], v[7]);
@@ -571,10 +600,11 @@ int launch_score(const ScoreArgs& a, cudaStream_t st) {
   CUtensorMap map;
   if (a.num_pages > 0 && !make_codes_map(&map, a.codes, a.num_pages)) return M3S_ERR_LAUNCH;
   if (a.num_pages <= 0) memset(&map, 0, sizeof(map));
-  if (cudaFuncSetAttribute(score_kernel<QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const auto kernel = a.mx ? score_kernel<QT, true> : score_kernel<QT, false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
-  return launch_kernel(score_kernel<QT>, dim3(sm_count()), dim3(Cfg<QT>::kThreads), smem, st, 0, a,
+  return launch_kernel(kernel, dim3(sm_count()), dim3(Cfg<QT>::kThreads), smem, st, 0, a,
                        map) == cudaSuccess
              ? M3S_OK
              : M3S_ERR_LAUNCH;
@@ -692,7 +722,6 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
   int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk_ids);
   if (rc != M3S_OK || R == 0) return rc;
   if (!cu_q || !row_len || max_q < 0 || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
-  if (idx_k.format != M3S_FMT_NVFP4) return M3S_ERR_UNSUPPORTED;   // this scorer reads NVFP4 only
   if (topk == 0 || B == 0) {
     if (topk > 0) {
       // no requests: every row is padding
@@ -709,7 +738,8 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
   if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
   float* bs = static_cast<float*>(ws);
   ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-              nullptr, cu_q, row_len, R, B, static_cast<int>(ntiles), cpr, bs, bt_stride, err};
+              nullptr, cu_q, row_len, R, B, static_cast<int>(ntiles), cpr, bs, bt_stride, err,
+              idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   rc = launch_score<8>(a, st);
   if (rc != M3S_OK) return rc;

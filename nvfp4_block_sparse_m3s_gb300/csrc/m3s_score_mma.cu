@@ -84,18 +84,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// fp16x2 broadcast of 2^-d (d >= 0): normal down to 2^-14, subnormal to 2^-24,
-// zero beyond.
-__device__ __forceinline__ uint32_t pow2_neg_f16x2(int d) {
-  const uint32_t h = d <= 14 ? static_cast<uint32_t>(15 - d) << 10 : (d <= 24 ? 1u << (24 - d) : 0u);
-  return h | (h << 16);
-}
-
-// 2^e as fp32 for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
-__device__ __forceinline__ float pow2_f32(int e) {
-  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
-}
-
 template <bool MX>
 __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreArgs a) {
   constexpr int kKeyScaleBytes = MX ? kMxScaleBytes : kScaleBytes;
@@ -262,8 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
 #pragma unroll
           for (int kk = lane; kk < kHalfKeys; kk += 32) {
             const uint32_t w4 = *reinterpret_cast<const uint32_t*>(ss + kk * kMxScaleBytes);
-            const uint32_t m2 = __vmaxu4(w4, w4 >> 16);
-            const int em = static_cast<int>(max(m2 & 0xFFu, (m2 >> 8) & 0xFFu));
+            const int em = e8m0_max4(w4);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               mxs.fac[warp][kk][j] = pow2_neg_f16x2(em - static_cast<int>((w4 >> (8 * j)) & 0xFFu));

@@ -58,11 +58,6 @@ __device__ __forceinline__ int mx_shared_exponent(uint32_t am) {
   return min(127, max(-127, fl - 2));
 }
 
-// 2^E as an fp32 value (exact: 2^-127 is the subnormal 0x00400000).
-__device__ __forceinline__ float pow2_f32(int E) {
-  return E >= -126 ? __uint_as_float(static_cast<uint32_t>(E + 127) << 23) : __uint_as_float(0x00400000u);
-}
-
 // Largest |x| of a group, as BF16 magnitude bits (non-negative floats order as
 // their bit patterns).
 __device__ __forceinline__ uint32_t group_amax_bits(const uint32_t (&x)[8]) {

@@ -82,8 +82,8 @@ def test_host_validation_rejects_before_launch(lib):
 
 def test_plane_format_rules(lib):
     """A plane's format field: 0 = NVFP4, 1 = MXFP4, anything else is rejected; K and V
-    must share one format; the fused verify scorer reads NVFP4 only. All decided on
-    the host (the fake device pointers are never dereferenced)."""
+    must share one format. All decided on the host (the fake device pointers are
+    never dereferenced and nothing is launched)."""
     from nvfp4_block_sparse_m3s_gb300 import binding as M
     fake = ctypes.c_void_p(1 << 20)
     nv = M.Plane(fake, fake, 4, 1, M.FMT_NVFP4)
@@ -99,9 +99,13 @@ def test_plane_format_rules(lib):
     for p in (nv, mx):
         assert lib.m3s_index_score_topk(fake, fake, 16, p, fake, 8, fake, fake, 0, 1, 8, 0, 0, fake,
                                         None, fake, 1 << 20, None, None) == M.OK
-    # fused verify: MXFP4 is not read by this scorer
-    assert lib.m3s_verify_score_topk(fake, fake, 16, mx, fake, 8, fake, fake, 1, 1, 8, 16, 0, 0,
-                                     fake, fake, 1 << 20, None, None) == M.ERR_UNSUPPORTED
+    # fused verify: both formats pass validation (R = 0: nothing is launched), an
+    # unknown one is rejected before any launch
+    for p in (nv, mx):
+        assert lib.m3s_verify_score_topk(fake, fake, 16, p, fake, 8, fake, fake, 1, 0, 8, 16, 0, 0,
+                                         fake, fake, 1 << 20, None, None) == M.OK
+    assert lib.m3s_verify_score_topk(fake, fake, 16, bad, fake, 8, fake, fake, 1, 1, 8, 16, 0, 0,
+                                     fake, fake, 1 << 20, None, None) == M.ERR_INVALID
     # attention: mixed K / V formats refused, unknown format invalid
     args = (fake, 1, 1, fake, fake, fake, 16, 1, ctypes.c_float(0.1), fake, None, None, 0, None, None)
     assert lib.m3s_sparse_attention(fake, 16, 1, nv, mx, *args) == M.ERR_UNSUPPORTED

@@ -83,24 +83,26 @@ def test_batch_store_mixed_formats(lib):
 
 
 CASES = [
-    # (spec, contexts, rows per request, MXFP4 index plane, MXFP4 K/V planes)
-    ("tiny", (4096,), (1,), True, True),
-    ("decode", (1000, 3000, 129, 128, 5000, 257), (1,) * 6, True, True),
-    ("skewed", (9000, 3000, 3000, 3000), (1, 1, 1, 1), True, True),
-    ("decode", (2000, 700, 4100), (1, 1, 1), False, True),    # NVFP4 index, MXFP4 K/V
-    ("decode", (2000, 700, 4100), (1, 1, 1), True, False),    # MXFP4 index, NVFP4 K/V
+    # (spec, contexts, rows per request, MXFP4 index plane, MXFP4 K/V planes, fused verify)
+    ("tiny", (4096,), (1,), True, True, False),
+    ("decode", (1000, 3000, 129, 128, 5000, 257), (1,) * 6, True, True, False),
+    ("skewed", (9000, 3000, 3000, 3000), (1, 1, 1, 1), True, True, False),
+    ("decode", (2000, 700, 4100), (1, 1, 1), False, True, False),   # NVFP4 index, MXFP4 K/V
+    ("decode", (2000, 700, 4100), (1, 1, 1), True, False, False),   # MXFP4 index, NVFP4 K/V
+    ("verify", (700, 2500, 1300, 999), (8, 3, 8, 1), True, True, True),
+    ("prefill", (2000,), (40,), True, True, True),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-{'mx' if c[3] else 'nv'}idx-{'mx' if c[4] else 'nv'}kv"
                                               for c in CASES])
 def test_mx_step_small_vs_oracle(lib, case):
-    name, ctx, qr, mx_index, mx_kv = case
+    name, ctx, qr, mx_index, mx_kv, fused = case
     wl = W.make(name, ctx=ctx, q_rows=qr)
     s = wl.spec
     dev = DeviceCache(wl, mx_kv=mx_kv, mx_index=mx_index)
     dev.store_all()
-    row_req, row_len, ids, bscores, out, lse = dev.step(False)
+    row_req, row_len, ids, bscores, out, lse = dev.step(fused)
     torch.cuda.synchronize()
     assert int(dev.err.item()) == 0
     ref = OracleCache(wl, mx_kv=mx_kv, mx_index=mx_index)
@@ -113,8 +115,10 @@ def test_mx_step_small_vs_oracle(lib, case):
                                               rl, s.topk)
     assert err == 0
     gids = ids.cpu().numpy()
-    gbs = bscores.cpu().numpy()
-    check_block_scores(gbs, ref_bs, range(R))
+    gbs = None
+    if bscores is not None:
+        gbs = bscores.cpu().numpy()
+        check_block_scores(gbs, ref_bs, range(R))
     check_topk(gids, ref_bs, s.topk, range(R), gbs)
     o_ref, lse_ref, err = O.sparse_attention(wl.q, s.hkv, ref.kc, ref.ks, ref.vc, ref.vs,
                                              wl.block_table, rr, rl, gids, SM_SCALE)
