@@ -283,9 +283,11 @@ int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
  * their block once per occurrence.
  * k and v share one format (NVFP4 or MXFP4; mixed formats return
  * M3S_ERR_UNSUPPORTED, as the pages' startup refuses mixing them: #2744,
- * Follow-up: MXFP4 caches). NVFP4 K/V dequantise exactly to fp16 (the q
- * operand is fp16, see M3S_DEVERR_QRANGE); MXFP4 K/V dequantise exactly to
- * bf16 and meet q in bf16 as given, the softmax weights rounded to bf16.
+ * Follow-up: MXFP4 caches). The products are fp16 x fp16 (q is converted, see
+ * M3S_DEVERR_QRANGE): NVFP4 K/V dequantise exactly to fp16; MXFP4 K is scaled
+ * per token by its largest exponent and V per 32-dim group by the largest
+ * exponent of the row's selected tokens so far, the factors re-applied in
+ * fp32, which is exact while the exponents so normalised span at most 23.
  */
 int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k,
                          m3s_fp4_plane v, const int32_t* block_table, int32_t bt_stride,

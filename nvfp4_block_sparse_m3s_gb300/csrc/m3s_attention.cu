@@ -19,10 +19,15 @@
 // fragments follow the same order), V two tokens at a time with the nibbles of
 // the same byte interleaved (each n8 tile covers every other dimension).
 //
-// MXFP4 K/V (one E8M0 scale per 32 elements) run the same kernel on bf16
-// operands: e2m1 x 2^(E-127) is exact in bf16 over E8M0's whole range (in fp16
-// it is not), the query is used as the BF16 it arrives in, and the softmax
-// weights are rounded to bf16 for the P V product.
+// MXFP4 K/V (one E8M0 scale per 32 elements) run the same fp16 products after
+// exponent normalisation, since e2m1 x 2^(E-127) does not fit fp16 over E8M0's
+// range. K: a thread's 16-byte chunk of a token is one 32-element group, scaled
+// by 2^(E - E_max) (E_max = the token's largest exponent), and the token's scores
+// by 2^(E_max - 127) in fp32. V: every output accumulator of a thread lies in one
+// 32-dim group, so each warp keeps a running reference exponent R per group (the
+// largest of its live tokens so far), scales V by 2^(E - R), rescales its
+// accumulators exactly when R grows, and multiplies them by 2^(R - 127) at the
+// end. Both are exact while the exponents involved span at most 23.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -83,36 +88,10 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Two e2m1 codes -> bf16x2, exactly: the fp16 conversion, then each nonzero
-// half's exponent re-biased from 15 to 127 (the mantissa keeps its top bits).
-__device__ __forceinline__ uint32_t e2m1x2_to_bf16x2(uint32_t two) {
-  const uint32_t h = e2m1x2_to_f16x2(two);
-  const uint32_t mag = h & 0x7FFF7FFFu;
-  const uint32_t nz = __vcmpne2(mag, 0u);
-  return (h & 0x80008000u) | ((((mag >> 3) & 0x0FFF0FFFu) + 0x38003800u) & nz);
-}
-
-// bf16 bits of the E8M0 scale 2^(e - 127) (e = 0 is the subnormal 2^-127).
-__device__ __forceinline__ uint32_t e8m0_to_bf16(uint32_t e) { return e ? (e << 7) : 0x0040u; }
-
-__device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                              uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// 2^d as fp32 for d <= 0, zero below fp32's subnormal range.
+__device__ __forceinline__ float pow2_f32_nonpos(int d) {
+  if (d >= -126) return __uint_as_float(static_cast<uint32_t>(d + 127) << 23);
+  return d >= -149 ? __uint_as_float(1u << (d + 149)) : 0.f;
 }
 
 template <bool MX>
@@ -146,17 +125,10 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       uint2 v0 = make_uint2(0u, 0u), v1 = make_uint2(0u, 0u);
       if (h0 < a.G) v0 = *reinterpret_cast<const uint2*>(q0 + 4 * j);
       if (h1 < a.G) v1 = *reinterpret_cast<const uint2*>(q1 + 4 * j);
-      if constexpr (MX) {   // bf16 operands: the query as it arrives
-        qa[j][0] = v0.x;
-        qa[j][1] = v1.x;
-        qa[j][2] = v0.y;
-        qa[j][3] = v1.y;
-      } else {
-        qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
-        qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
-        qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
-        qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
-      }
+      qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
+      qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
+      qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
+      qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
     }
   }
 
@@ -227,6 +199,7 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY;  // running max (log2 units) of heads g, g+8
   float l0 = 0.f, l1 = 0.f;              // this thread's share of the sums
+  uint32_t vref = 0;                     // MX: this warp's V reference exponent per group (bytes)
   bool aborted = false;
 
   for (int i = 0; i < nblocks; ++i) {
@@ -258,15 +231,24 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
         const uint32_t wv[4] = {kw.x, kw.y, kw.z, kw.w};
         if constexpr (MX) {
           // the thread's 16-byte chunk (dims 32t .. 32t+31) is E8M0 group t
-          const uint32_t e = e8m0_to_bf16(kss[tok * kMxScaleBytes + t]);
-          const uint32_t sj = e | (e << 16);
+          const uint32_t kw4 = *reinterpret_cast<const uint32_t*>(kss + tok * kMxScaleBytes);
+          const int em = e8m0_max4(kw4);
+          const uint32_t sj = pow2_neg_f16x2(em - static_cast<int>((kw4 >> (8 * t)) & 0xFFu));
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
-            const uint32_t b0 = hmul2_bf16(e2m1x2_to_bf16x2(x & 0xFFu), sj);
-            const uint32_t b1 = hmul2_bf16(e2m1x2_to_bf16x2((x >> 8) & 0xFFu), sj);
-            mma16816_bf16(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+            const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
+            const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
+            mma16816(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
           }
+          // columns 2t, 2t + 1 of this tile are the tokens decoded by lanes 8t, 8t + 4
+          const float fk = pow2_f32(em - 127);
+          const float f0 = __shfl_sync(0xffffffffu, fk, 8 * t);
+          const float f1 = __shfl_sync(0xffffffffu, fk, 8 * t + 4);
+          sacc[c][0] *= f0;
+          sacc[c][1] *= f1;
+          sacc[c][2] *= f0;
+          sacc[c][3] *= f1;
         } else {
           const uint32_t sc = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(kss + tok * kScaleBytes + 2 * t));
           const uint32_t s0 = bcast_lo(sc), s1 = bcast_hi(sc);
@@ -324,14 +306,35 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
           l1 += p1;
         }
       }
+      if constexpr (MX) {
+        // the reference exponents take in this block's live tokens; the
+        // accumulators (all of group t for this thread) follow exactly
+        uint32_t e4 = tb + lane < ntok
+                          ? *reinterpret_cast<const uint32_t*>(vss + (tb + lane) * kMxScaleBytes)
+                          : 0u;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) e4 = __vmaxu4(e4, __shfl_xor_sync(0xffffffffu, e4, sh));
+        const uint32_t rnew = __vmaxu4(vref, e4);
+        if (rnew != vref) {   // warp-uniform
+          const float f = pow2_f32_nonpos(static_cast<int>((vref >> (8 * t)) & 0xFFu) -
+                                          static_cast<int>((rnew >> (8 * t)) & 0xFFu));
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            o[n][0] *= f;
+            o[n][1] *= f;
+            o[n][2] *= f;
+            o[n][3] *= f;
+          }
+          vref = rnew;
+        }
+      }
       // ---- O += P V over the warp's 32 tokens (2 k-steps of 16) ----
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        const auto pack = [](float lo, float hi) { return MX ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi); };
-        const uint32_t pa0 = pack(sacc[2 * kk][0], sacc[2 * kk][1]);
-        const uint32_t pa1 = pack(sacc[2 * kk][2], sacc[2 * kk][3]);
-        const uint32_t pa2 = pack(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-        const uint32_t pa3 = pack(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+        const uint32_t pa0 = pack_f16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
+        const uint32_t pa1 = pack_f16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
+        const uint32_t pa2 = pack_f16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+        const uint32_t pa3 = pack_f16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
         const int t0 = tb + 16 * kk + 2 * t;  // tokens t0, t0+1 (b0) and t0+8, t0+9 (b1)
         // bytes 8g .. 8g+7 of each token: dims 16g .. 16g+15 (scale group g)
         const uint2 v0 = *reinterpret_cast<const uint2*>(vcs + t0 * kCodeBytes + 8 * g);
@@ -339,10 +342,15 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
         const uint2 v2 = *reinterpret_cast<const uint2*>(vcs + (t0 + 8) * kCodeBytes + 8 * g);
         const uint2 v3 = *reinterpret_cast<const uint2*>(vcs + (t0 + 9) * kCodeBytes + 8 * g);
         uint32_t s01, s23;   // the (token, token + 1) scale pairs of these dims
-        if constexpr (MX) {   // dims 16g .. 16g+15 lie in E8M0 group g / 2
+        if constexpr (MX) {   // dims 16g .. 16g+15 lie in E8M0 group g / 2: 2^(E - R)
           const int gm = g >> 1;
-          s01 = e8m0_to_bf16(vss[t0 * kMxScaleBytes + gm]) | (e8m0_to_bf16(vss[(t0 + 1) * kMxScaleBytes + gm]) << 16);
-          s23 = e8m0_to_bf16(vss[(t0 + 8) * kMxScaleBytes + gm]) | (e8m0_to_bf16(vss[(t0 + 9) * kMxScaleBytes + gm]) << 16);
+          const int rg = static_cast<int>((vref >> (8 * gm)) & 0xFFu);
+          // (a masked token's exponent may exceed R: its weight is 0, keep its factor finite)
+          const auto fac = [&](int tk) {
+            return pow2_neg_f16x2(max(rg - static_cast<int>(vss[tk * kMxScaleBytes + gm]), 0)) & 0xFFFFu;
+          };
+          s01 = fac(t0) | (fac(t0 + 1) << 16);
+          s23 = fac(t0 + 8) | (fac(t0 + 9) << 16);
         } else {
           s01 = e4m3x2_to_f16x2(vss[t0 * kScaleBytes + g] | (vss[(t0 + 1) * kScaleBytes + g] << 8));
           s23 = e4m3x2_to_f16x2(vss[(t0 + 8) * kScaleBytes + g] | (vss[(t0 + 9) * kScaleBytes + g] << 8));
@@ -361,21 +369,12 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
           for (int bb = 0; bb < 4; ++bb) {
             const int jj = 4 * hw + bb;
             const uint32_t sh = 8 * bb;
-            if constexpr (MX) {
-              const uint32_t be0 = hmul2_bf16(e2m1x2_to_bf16x2((lo01 >> sh) & 0xFFu), s01);
-              const uint32_t be1 = hmul2_bf16(e2m1x2_to_bf16x2((lo23 >> sh) & 0xFFu), s23);
-              const uint32_t bo0 = hmul2_bf16(e2m1x2_to_bf16x2((hi01 >> sh) & 0xFFu), s01);
-              const uint32_t bo1 = hmul2_bf16(e2m1x2_to_bf16x2((hi23 >> sh) & 0xFFu), s23);
-              mma16816_bf16(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
-              mma16816_bf16(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
-            } else {
-              const uint32_t be0 = hmul2(e2m1x2_to_f16x2((lo01 >> sh) & 0xFFu), s01);
-              const uint32_t be1 = hmul2(e2m1x2_to_f16x2((lo23 >> sh) & 0xFFu), s23);
-              const uint32_t bo0 = hmul2(e2m1x2_to_f16x2((hi01 >> sh) & 0xFFu), s01);
-              const uint32_t bo1 = hmul2(e2m1x2_to_f16x2((hi23 >> sh) & 0xFFu), s23);
-              mma16816(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
-              mma16816(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
-            }
+            const uint32_t be0 = hmul2(e2m1x2_to_f16x2((lo01 >> sh) & 0xFFu), s01);
+            const uint32_t be1 = hmul2(e2m1x2_to_f16x2((lo23 >> sh) & 0xFFu), s23);
+            const uint32_t bo0 = hmul2(e2m1x2_to_f16x2((hi01 >> sh) & 0xFFu), s01);
+            const uint32_t bo1 = hmul2(e2m1x2_to_f16x2((hi23 >> sh) & 0xFFu), s23);
+            mma16816(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
+            mma16816(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
           }
         }
       }
@@ -384,6 +383,16 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     if (tid == 0 && !aborted && i + 2 < nblocks) issue(i + 2, sm.page[i + 2]);
   }
 
+  if constexpr (MX) {   // undo the V reference: this thread's accumulators are group t
+    const float f = pow2_f32(static_cast<int>((vref >> (8 * t)) & 0xFFu) - 127);
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      o[n][0] *= f;
+      o[n][1] *= f;
+      o[n][2] *= f;
+      o[n][3] *= f;
+    }
+  }
   // ---- merge the four warps ----
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);

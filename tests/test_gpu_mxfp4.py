@@ -129,10 +129,10 @@ def test_mx_step_small_vs_oracle(lib, case):
 
 
 def test_mx_extreme_scales_stay_exact(lib):
-    """Keys whose four groups span a wide exponent range, and K/V groups at the
-    smallest and largest E8M0 exponents the BF16 range produces: the scorer
-    (exact while a key's exponents span <= 23) and the bf16 attention (exact over
-    the whole range) still match the oracle."""
+    """Keys whose four groups span a wide exponent range, K near the smallest E8M0
+    exponents and V near the largest, V growing 2^4 per block (the running V
+    reference rises block by block): the scorer and the attention, both exact
+    while the exponents they normalise against span <= 23, match the oracle."""
     rng = np.random.default_rng(17)
     L, hi, hq = 700, 16, 16
     nb = (L + 127) // 128
@@ -146,10 +146,11 @@ def test_mx_extreme_scales_stay_exact(lib):
 
     ik = keys(20.0)                                           # group exponents 20 apart
     kv = W.f32_to_bf16_bits((rng.standard_normal((L, 1, 128)) * 2.0 ** -120).astype(np.float32))
-    vv = W.f32_to_bf16_bits((rng.standard_normal((L, 1, 128)) * 2.0 ** 100).astype(np.float32))
+    vgrow = 2.0 ** (100 + 4 * (np.arange(L) // 128))[:, None, None]
+    vv = W.f32_to_bf16_bits((rng.standard_normal((L, 1, 128)) * vgrow).astype(np.float32))
     q_idx = W.f32_to_bf16_bits(rng.standard_normal((1, hi, 128)).astype(np.float32))
     w = rng.random((1, hi)).astype(np.float32)
-    q = W.f32_to_bf16_bits(rng.standard_normal((1, hq, 128)).astype(np.float32) * 2.0 ** 110)
+    q = W.f32_to_bf16_bits(rng.standard_normal((1, hq, 128)).astype(np.float32))
     bt = np.zeros((1, nb), dtype=np.int32)
     bt[0] = rng.permutation(P)[:nb]
     slots = (bt[0][np.arange(L) // 128].astype(np.int64) * 128 + np.arange(L) % 128)
