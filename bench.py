@@ -67,14 +67,22 @@ def peaks():
 # captured; after any change it is null until the counters are taken again.
 NCU_TRAFFIC = {
     ("skewed", "score_decode_kernel"): {
-        "bytes": 110_713_856 + 2_951_168,
-        "sources": {"m3s_score_mma.cu": "3d81366d360493f1",
-                    "m3s_score_common.cuh": "e9a56987dac063b1"},
+        "bytes": 110_715_904 + 3_092_480,
+        "sources": {"m3s_score_mma.cu": "2dd3407ad8628139",
+                    "m3s_score_common.cuh": "76d51994d51a9f16",
+                    "m3s_device.cuh": "9fc60929d766978e"},
+    },
+    ("skewed-mxfp4", "score_decode_kernel"): {
+        "bytes": 104_573_184 + 2_823_424,
+        "sources": {"m3s_score_mma.cu": "2dd3407ad8628139",
+                    "m3s_score_common.cuh": "76d51994d51a9f16",
+                    "m3s_device.cuh": "9fc60929d766978e"},
     },
     ("verify", "score_kernel"): {
-        "bytes": 143_940_352 + 4_349_184,
-        "sources": {"m3s_score.cu": "2db925a504238f53",
-                    "m3s_score_common.cuh": "e9a56987dac063b1"},
+        "bytes": 143_923_968 + 4_821_760,
+        "sources": {"m3s_score.cu": "658d24fe629d8179",
+                    "m3s_score_common.cuh": "76d51994d51a9f16",
+                    "m3s_device.cuh": "9fc60929d766978e"},
     },
 }
 
