@@ -469,3 +469,92 @@ def sparse_attention(q: np.ndarray, hkv: int, k_codes, k_scales, v_codes, v_scal
                 out[r, h] = (p @ vh) / l
                 lse[r, h] = m + math.log(l)
     return out, lse, err
+
+
+# --------------------------------------------------------------------------
+# Quantise-at-write: the normalise / rotate / cache-write step with the
+# quantisation inside it ("[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV
+# cache" (#2744), Follow-up: MXFP4 caches -- "the quantization happens inside
+# the fused qk-norm/RoPE/cache kernel, so there is no staging buffer and no
+# store launch"; the unfused path of the same page, Summary / Write, writes
+# the normalised rows BF16 to a staging buffer and quantises them after).
+# --------------------------------------------------------------------------
+
+def _f32(x):
+    return np.asarray(x, dtype=np.float32)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to BF16, nearest, ties to even (NaN kept quiet)."""
+    u = _f32(x).view(np.uint32).astype(np.uint64)
+    nan = (u & 0x7F800000) == 0x7F800000
+    nan &= (u & 0x007FFFFF) != 0
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    r = np.where(nan, (u >> 16) | 0x40, r)
+    return r.astype(np.uint16)
+
+
+def head_sum_sq_f32(x: np.ndarray) -> np.ndarray:
+    """sum of x^2 over the last axis (128) in float32, in the order the write
+    kernel's warp takes it: lane l owns elements 4l .. 4l+3 and adds their
+    squares left to right; the 32 lane sums are then combined by an xor
+    butterfly (offsets 16, 8, 4, 2, 1) and lane 0's value is the result.
+    Float addition is commutative, so only this tree of additions matters."""
+    sq = _f32(x) * _f32(x)                                   # rounded products
+    sq = sq.reshape(sq.shape[:-1] + (32, 4))
+    p = ((sq[..., 0] + sq[..., 1]) + sq[..., 2]) + sq[..., 3]
+    lanes = np.arange(32)
+    for off in (16, 8, 4, 2, 1):
+        p = p + p[..., lanes ^ off]
+    return p[..., 0]
+
+
+def norm_rope_rows(bits: np.ndarray, weight, cos, sin, rotary_dim: int, eps: float) -> np.ndarray:
+    """The normalised, rotated BF16 rows [T, H, 128] of BF16 rows ``bits``.
+
+    Per (row, head), in float32 with every operation rounded (no fused
+    multiply-add), as the write kernel computes it:
+      - RMSNorm (``weight`` [128] given): r = 1 / sqrt(sum(x^2) / 128 + eps),
+        y_i = (x_i * r) * weight_i; else y = x;
+      - RoPE (``cos``/``sin`` [T, rotary_dim / 2] given): for i < rotary_dim / 2,
+        with j = i + rotary_dim / 2, c = cos[t, i], s = sin[t, i]:
+        o_i = y_i * c - y_j * s,  o_j = y_j * c + y_i * s;  dims >= rotary_dim
+        pass unchanged;
+      - the result rounded to BF16 (nearest, ties to even), as the staging
+        buffer of the unfused path holds it.
+    """
+    x = bf16_to_f64(bits).astype(np.float32)                 # exact
+    T, H, D = x.shape
+    assert D == HEAD_DIM
+    if weight is not None:
+        ss = head_sum_sq_f32(x)                              # [T, H]
+        v = ss * np.float32(1.0 / 128) + np.float32(eps)
+        r = np.float32(1.0) / np.sqrt(v)
+        y = (x * r[..., None]) * _f32(weight)
+    else:
+        y = x
+    if cos is not None:
+        h = rotary_dim // 2
+        c = _f32(cos)[:, None, :h]
+        s = _f32(sin)[:, None, :h]
+        y1, y2 = y[..., :h], y[..., h:rotary_dim]
+        o1 = y1 * c - y2 * s
+        o2 = y2 * c + y1 * s
+        y = np.concatenate([o1, o2, y[..., rotary_dim:]], axis=-1)
+    return f32_to_bf16_bits(y)
+
+
+def qk_norm_rope_store(jobs, slot_mapping, cos, sin, rotary_dim: int, eps: float) -> int:
+    """The fused write: each job is (src bits [T, H, 128], weight [128] or None,
+    rope: bool, destination), the destination either a (codes, scales) plane
+    pair, filled as ``nvfp4_store`` would fill it from the normalised rows, or
+    a BF16 array [T, H, 128] that receives them. Returns the store's error bits."""
+    err = 0
+    for src, weight, rope, dst in jobs:
+        rows = norm_rope_rows(src, weight, cos if rope else None, sin if rope else None,
+                              rotary_dim, eps)
+        if isinstance(dst, tuple):
+            err |= nvfp4_store(rows, slot_mapping, dst[0], dst[1])
+        else:
+            dst[...] = rows
+    return err

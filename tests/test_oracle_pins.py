@@ -608,3 +608,101 @@ def test_mx_store_into_mx_planes():
         if slot not in written:
             assert (c[slot // 128, :, slot % 128] == 0xA5).all()
             assert (s[slot // 128, :, slot % 128] == 0x5A).all()
+
+
+# --------------------------------------------------------------------------
+# Quantise-at-write (normalise / rotate / write, the quantisation inside):
+# #2744, Follow-up: MXFP4 caches ("the quantization happens inside the fused
+# qk-norm/RoPE/cache kernel, so there is no staging buffer and no store launch")
+# --------------------------------------------------------------------------
+
+def _rope_tables(T, half, base=10000.0, pos0=3):
+    t = (pos0 + np.arange(T))[:, None] * (base ** (-np.arange(half) / half))[None, :]
+    return np.cos(t).astype(np.float32), np.sin(t).astype(np.float32)
+
+
+def test_bf16_rounding_matches_torch():
+    """f32 -> BF16 (nearest, ties to even) equals torch's conversion, ties included."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(4096).astype(np.float32) * np.float32(2.0) ** rng.integers(-60, 60, 4096)
+    hi = rng.integers(0, 1 << 16, 512).astype(np.uint32)
+    hi = hi[(hi & 0x7F80) != 0x7F80]                      # finite patterns only
+    ties = ((hi << np.uint32(16)) | np.uint32(0x8000)).astype(np.uint32)
+    x = np.concatenate([x, ties.view(np.float32)])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.f32_to_bf16_bits(x), want)
+
+
+def test_head_sum_of_squares_within_f32_rounding_of_exact():
+    """The kernel-order float32 sum of squares lies within the rounding bound of
+    the exact sum (math.fsum over the exact squares)."""
+    rng = np.random.default_rng(4)
+    x = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal((64, 128)).astype(np.float32) * 3))
+    got = O.head_sum_sq_f32(x)
+    for r in range(64):
+        exact = math.fsum(float(v) * float(v) for v in x[r].astype(np.float64))
+        assert abs(float(got[r]) - exact) <= 140 * 2.0 ** -24 * exact
+
+
+def test_norm_rope_against_torch_rms_norm_and_complex_rotation():
+    """RMSNorm (torch.nn.functional.rms_norm, fp64) followed by rotate-half RoPE
+    written as complex multiplication: the oracle's BF16 rows agree within BF16
+    rounding plus float32 arithmetic."""
+    rng = np.random.default_rng(6)
+    T, H, r = 6, 3, 64
+    x = W.f32_to_bf16_bits((rng.standard_normal((T, H, 128)) * 4).astype(np.float32))
+    w = (rng.random(128) + 0.5).astype(np.float32)
+    cos, sin = _rope_tables(T, r // 2)
+    got = O.bf16_to_f64(O.norm_rope_rows(x, w, cos, sin, r, 1e-6))
+    xt = torch.from_numpy(O.bf16_to_f64(x))
+    nt = torch.nn.functional.rms_norm(xt, (128,), torch.from_numpy(w.astype(np.float64)), eps=1e-6)
+    rot = torch.complex(nt[..., : r // 2], nt[..., r // 2: r]) * torch.complex(
+        torch.from_numpy(cos.astype(np.float64))[:, None, :], torch.from_numpy(sin.astype(np.float64))[:, None, :])
+    ref = torch.cat([rot.real, rot.imag, nt[..., r:]], -1).numpy()
+    assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6)
+
+
+def test_norm_rope_special_cases():
+    """No norm and no rotation give the rows back bit for bit; angle 0 is the
+    identity; a zero row stays zero; a constant row of c with unit weights
+    normalises to c / sqrt(c^2 + eps); the rotation keeps each pair's norm."""
+    rng = np.random.default_rng(8)
+    x = W.f32_to_bf16_bits(rng.standard_normal((4, 2, 128)).astype(np.float32))
+    assert np.array_equal(O.norm_rope_rows(x, None, None, None, 0, 1e-6), x)
+    c1, s0 = np.ones((4, 64), np.float32), np.zeros((4, 64), np.float32)
+    assert np.array_equal(O.norm_rope_rows(x, None, c1, s0, 128, 1e-6), x)
+    z = np.zeros((1, 1, 128), dtype=np.uint16)
+    assert not O.norm_rope_rows(z, np.ones(128, np.float32), None, None, 0, 1e-6).any()
+    c = np.full((1, 1, 128), W.f32_to_bf16_bits(np.float32([-0.75]))[0], dtype=np.uint16)
+    y = O.bf16_to_f64(O.norm_rope_rows(c, np.ones(128, np.float32), None, None, 0, 1e-6))
+    assert np.allclose(y, -0.75 / math.sqrt(0.5625 + 1e-6), rtol=2.0 ** -8)
+    cos, sin = _rope_tables(4, 64)
+    xr = O.bf16_to_f64(x)
+    yr = O.bf16_to_f64(O.norm_rope_rows(x, None, cos, sin, 128, 1e-6))
+    n0 = np.hypot(xr[..., :64], xr[..., 64:])
+    n1 = np.hypot(yr[..., :64], yr[..., 64:])
+    assert np.all(np.abs(n1 - n0) <= n0 * 2.0 ** -7 + 1e-30)
+
+
+def test_quantise_at_write_equals_staging_then_store():
+    """The fused write fills the planes exactly as the unfused path does: the
+    normalised rows to a BF16 staging buffer, then the store (#2744, Summary /
+    Write), for both record formats; BF16 destinations receive the rows."""
+    rng = np.random.default_rng(9)
+    T, P = 20, 2
+    cos, sin = _rope_tables(T, 32)
+    slots = rng.permutation(P * 128)[:T].astype(np.int64)
+    slots[3] = -1
+    k = W.f32_to_bf16_bits(rng.standard_normal((T, 2, 128)).astype(np.float32))
+    q = W.f32_to_bf16_bits(rng.standard_normal((T, 4, 128)).astype(np.float32))
+    wk = (rng.random(128) + 0.5).astype(np.float32)
+    for mx in (False, True):
+        kc, ks = O.new_planes(P, 2, mx=mx)
+        qo = np.zeros_like(q)
+        assert O.qk_norm_rope_store([(k, wk, True, (kc, ks)), (q, None, True, qo)], slots,
+                                    cos, sin, 64, 1e-6) == 0
+        staged = O.norm_rope_rows(k, wk, cos, sin, 64, 1e-6)
+        rc, rs = O.new_planes(P, 2, mx=mx)
+        O.nvfp4_store(staged, slots, rc, rs)
+        assert np.array_equal(kc, rc) and np.array_equal(ks, rs)
+        assert np.array_equal(qo, O.norm_rope_rows(q, None, cos, sin, 64, 1e-6))
