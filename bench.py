@@ -29,6 +29,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("sparse-attn+index rows/s and achieved HBM GB/s vs ~8 TB/s peak, bs8 mixed ctx")
 SM_SCALE = 1.0 / math.sqrt(128)
+ROTARY_DIM = 64       # --write-path fused / staged: rotated dims per head
+NORM_EPS = 1e-6       # and the RMSNorm epsilon
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -44,6 +46,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cache-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="K / V / index-K record format")
+    ap.add_argument("--write-path", choices=["store", "fused", "staged"], default="store",
+                    help="store: the step's rows arrive normalised and are stored; fused: they "
+                         "arrive before RMSNorm / RoPE and one quantise-at-write launch normalises, "
+                         "rotates and stores them; staged: the same normalisation writes BF16 "
+                         "staging rows that the batched store then quantises (the unfused path)")
     ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-reps", type=int, default=2, help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -388,6 +395,22 @@ def run_ours(args):
         "ik_new": np.ascontiguousarray(wl.ik_src[new]), "slots": wl.slot_all[new].copy(),
         "q": wl.q, "q_idx": wl.q_idx, "w": wl.w, "cu_q": wl.cu_q, "seq_len": wl.seq_len,
     }
+    write_path = args.write_path
+    if write_path != "store":
+        # the same seeded rows taken as the pre-normalisation ones; RMSNorm weights
+        # U(0.5, 1.5) per tensor, RoPE over the first ROTARY_DIM dims at each new
+        # token's position (10000^(-i / (ROTARY_DIM / 2)) frequencies)
+        wrng = np.random.default_rng(s.seed + 101)
+        for k in ("wq", "wk", "wik"):
+            host_in[k] = (wrng.random(128) + 0.5).astype(np.float32)
+        pos = np.zeros(R, dtype=np.float64)   # row j of request b sits at seq_len - Q_b + j
+        for b in range(len(wl.seq_len)):
+            qb = int(wl.cu_q[b + 1] - wl.cu_q[b])
+            pos[int(wl.cu_q[b]): int(wl.cu_q[b]) + qb] = int(wl.seq_len[b]) - qb + np.arange(qb)
+        half = ROTARY_DIM // 2
+        ang = pos[:, None] * (10000.0 ** (-np.arange(half) / half))[None, :]
+        host_in["cos"] = np.cos(ang).astype(np.float32)
+        host_in["sin"] = np.sin(ang).astype(np.float32)
     del wl.k_src, wl.v_src, wl.ik_src
     # The step's inputs live in one device buffer (each tensor at a 256-byte
     # aligned offset) mirrored by one pinned host buffer, so the end-to-end run
@@ -419,6 +442,10 @@ def run_ours(args):
         out_off[k] = out_bytes
         out_bytes += (int(np.prod(shape)) * es + 255) // 256 * 256
     dev_out = torch.zeros(out_bytes, dtype=torch.uint8, device=dev)
+    if write_path != "store":
+        q_n = torch.empty_like(d["q"])            # the step's normalised, rotated queries
+        qidx_n = torch.empty_like(d["q_idx"])
+        staging = {k: torch.empty_like(d[k]) for k in ("k_new", "v_new", "ik_new")}
 
     def out_view(k):
         shape, dt, es = out_shapes[k]
@@ -445,23 +472,38 @@ def run_ours(args):
         side.wait_stream(cur)
         with torch.cuda.stream(side):
             M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
-        M.m3s_nvfp4_store_batch([(d["k_new"], kc, ks), (d["v_new"], vc, vs), (d["ik_new"], ic, is_)],
-                                d["slots"], err)
+        if write_path == "store":
+            M.m3s_nvfp4_store_batch([(d["k_new"], kc, ks), (d["v_new"], vc, vs),
+                                     (d["ik_new"], ic, is_)], d["slots"], err)
+        else:
+            fused_w = write_path == "fused"
+            dst = {"k_new": (kc, ks), "v_new": (vc, vs), "ik_new": (ic, is_)} if fused_w else staging
+            M.m3s_qk_norm_rope_store(
+                [(d["q"], d["wq"], True, q_n), (d["k_new"], d["wk"], True, dst["k_new"]),
+                 (d["v_new"], None, False, dst["v_new"]), (d["q_idx"], None, True, qidx_n),
+                 (d["ik_new"], d["wik"], True, dst["ik_new"])],
+                d["slots"], d["cos"], d["sin"], ROTARY_DIM, NORM_EPS, err)
+            if not fused_w:
+                M.m3s_nvfp4_store_batch([(staging["k_new"], kc, ks), (staging["v_new"], vc, vs),
+                                         (staging["ik_new"], ic, is_)], d["slots"], err)
         cur.wait_stream(side)
+
+    q_in = d["q"] if write_path == "store" else q_n
+    qidx_in = d["q_idx"] if write_path == "store" else qidx_n
 
     def score():
         if fused:
-            M.m3s_verify_score_topk(d["q_idx"], d["w"], ic, is_, bt, d["cu_q"], row_len,
+            M.m3s_verify_score_topk(qidx_in, d["w"], ic, is_, bt, d["cu_q"], row_len,
                                     max(s.q_rows), s.topk, ids, ws_v, err)
         else:
-            M.m3s_index_block_scores(d["q_idx"], d["w"], ic, is_, bt, row_req, row_len, bscores, err)
+            M.m3s_index_block_scores(qidx_in, d["w"], ic, is_, bt, row_req, row_len, bscores, err)
 
     def topk():
         if not fused:
             M.m3s_block_topk(bscores, row_req, row_len, B, bt_stride, s.topk, ids)
 
     def attn():
-        M.m3s_sparse_attention(d["q"], s.hkv, kc, ks, vc, vs, bt, row_req, row_len, ids, SM_SCALE,
+        M.m3s_sparse_attention(q_in, s.hkv, kc, ks, vc, vs, bt, row_req, row_len, ids, SM_SCALE,
                                out, lse, ws_a, err)
 
     # eager warm-up (sets kernel attributes), then the whole step as one CUDA
@@ -513,7 +555,9 @@ def run_ours(args):
         if phase_events:
             phase_events[-1].record(stream)
 
-    launches_per_step = 5   # batched store, row map, scorer, top-k, attention
+    # batched store (or quantise-at-write; staged: + the store), row map, scorer,
+    # top-k, attention
+    launches_per_step = 5 + (1 if write_path == "staged" else 0)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -542,6 +586,8 @@ def run_ours(args):
     score_bytes = keys * rec_bytes + R * s.hi * (256 + 4) + nb_rows * 4
     attn_bytes = distinct * 128 * 2 * rec_bytes * s.hkv + R * s.hq * 256 * 2
     store_bytes = R * (2 * s.hkv + 1) * (256 + rec_bytes)
+    if write_path != "store":   # the queries read and written back normalised / rotated
+        store_bytes += R * (s.hq + s.hi) * 256 * 2
     step_bytes = score_bytes + attn_bytes + store_bytes + R * 8
 
     # ---- timed region (device time, per step, L2 flushed between steps) ----
@@ -645,7 +691,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f16/bf16" if mx else "f16",
         "data": "synthetic",
-        "config": workload_config(s, keys, args.cache_format),
+        "config": dict(workload_config(s, keys, args.cache_format), write_path=write_path),
         "achieved_gbs_step": world * step_bytes / (ms * 1e-3) / 1e9,
         "algorithmic_bytes_per_step": step_bytes,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,

@@ -155,6 +155,50 @@ int m3s_nvfp4_store_batch(const m3s_store_job* jobs, int32_t njobs, int32_t T,
                           const int64_t* slot_mapping, int32_t* err, void* stream);
 
 /*
+ * Quantise-at-write. #2744, Follow-up: MXFP4 caches -- the quantisation moves
+ * into the kernel that normalises and rotates the step's rows and writes the
+ * cache, so there is no BF16 staging buffer and no separate store launch (the
+ * unfused path, #2744 Summary / Write: the rows go BF16 to a staging buffer,
+ * then the store quantises them). The normalisation and rotation belong to the
+ * model; this call takes their parameters. Per job, for each row t and head h
+ * of src (BF16 [T][H][128], row stride src_row_stride):
+ *   RMSNorm, when norm_weight (fp32 [128]) is given:
+ *     r = 1 / sqrt(sum_i(x_i^2) / 128 + eps), y_i = (x_i * r) * norm_weight[i];
+ *     else y = x;
+ *   RoPE, when job.rope != 0 (rotate-half on the first rotary_dim dims; c, s =
+ *     rope_cos[t][i], rope_sin[t][i], fp32 [T][rotary_dim / 2]):
+ *     o_i = y_i c - y_{i+rd/2} s,  o_{i+rd/2} = y_{i+rd/2} c + y_i s  (i < rd/2);
+ *   the result rounded to BF16 (nearest, ties to even) -- the value the staging
+ *   buffer would hold -- and then either quantised into dst at slot_mapping[t]
+ *   exactly as m3s_nvfp4_store does (either format; pad rows skipped, a slot
+ *   past the plane sets M3S_DEVERR_SLOT), or, when out is given, written to out
+ *   as BF16 rows (queries: every row t).
+ * Arithmetic: float32, each operation rounded on its own (no fused
+ * multiply-add); the sum of squares in a fixed order (32 lanes each add the
+ * squares of 4 consecutive elements left to right, then an xor butterfly over
+ * offsets 16, 8, 4, 2, 1, lane 0's value taken), so the bytes are reproducible.
+ * rotary_dim: a multiple of 8 in [8, 128] when any job rotates (else ignored);
+ * rope_cos / rope_sin and norm weights 16-byte aligned; out_row_stride >= H*128
+ * and a multiple of 8. T == 0 is a no-op.
+ */
+#define M3S_MAX_WRITE_JOBS 6
+typedef struct {
+  const uint16_t* src;      /* BF16 [T][H][128] device rows */
+  int64_t src_row_stride;   /* elements between rows (>= H*128, multiple of 8) */
+  int32_t H;                /* heads per row */
+  const float* norm_weight; /* fp32 [128] RMSNorm weight, or NULL (no normalisation) */
+  int32_t rope;             /* nonzero: rotate */
+  m3s_fp4_plane dst;        /* destination plane (num_heads == H) when out is NULL */
+  uint16_t* out;            /* BF16 [T][H][128] output rows, or NULL */
+  int64_t out_row_stride;   /* elements between output rows */
+} m3s_write_job;
+
+int m3s_qk_norm_rope_store(const m3s_write_job* jobs, int32_t njobs, int32_t T,
+                           const int64_t* slot_mapping, const float* rope_cos,
+                           const float* rope_sin, int32_t rotary_dim, float eps, int32_t* err,
+                           void* stream);
+
+/*
  * Row map. #2744, Design / Attention: one launch maps each row to its request
  * and causal length, on device, so it is valid under CUDA-graph capture.
  * Request b owns rows cu_q[b] .. cu_q[b+1]-1 (Q_b rows) and holds seq_len[b]

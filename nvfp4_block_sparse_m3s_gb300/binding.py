@@ -48,6 +48,14 @@ class StoreJob(ctypes.Structure):
                 ("H", ctypes.c_int32), ("dst", Plane)]
 
 
+class WriteJob(ctypes.Structure):
+    """m3s_write_job: one tensor of a quantise-at-write launch."""
+
+    _fields_ = [("src", ctypes.c_void_p), ("src_row_stride", ctypes.c_int64),
+                ("H", ctypes.c_int32), ("norm_weight", ctypes.c_void_p), ("rope", ctypes.c_int32),
+                ("dst", Plane), ("out", ctypes.c_void_p), ("out_row_stride", ctypes.c_int64)]
+
+
 _P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                              ctypes.c_size_t)
 _SIGS = {
@@ -55,6 +63,7 @@ _SIGS = {
     "m3s_nvfp4_store": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, Plane, _P, _P]),
     "m3s_nvfp4_store_batch": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P]),
     "m3s_decode_rows": (ctypes.c_int, [_P, _P, _I32, _I32, _P, _P, _P]),
+    "m3s_qk_norm_rope_store": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _I32, _F32, _P, _P]),
     "m3s_index_score_topk": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32, _I32,
                                             _I32, _I32, _I32, _P, _P, _P, _SZ, _P, _P]),
     "m3s_index_score_topk_static": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _I32,
@@ -155,6 +164,38 @@ def m3s_nvfp4_store_batch(jobs, slot_mapping: torch.Tensor, err: torch.Tensor | 
     rc = load().m3s_nvfp4_store_batch(arr, len(jobs), T, _ptr(slot_mapping), _ptr(err),
                                       _stream(stream))
     _check(rc, "m3s_nvfp4_store_batch")
+
+
+def m3s_qk_norm_rope_store(jobs, slot_mapping, rope_cos=None, rope_sin=None, rotary_dim: int = 0,
+                           eps: float = 1e-6, err=None, stream=None) -> None:
+    """Quantise-at-write. jobs: sequence of (src bf16 [T, H, 128], norm_weight fp32 [128] or
+    None, rope: bool, destination) with the destination either a (codes, scales) plane pair
+    or a bf16 tensor [T, H, 128] for the normalised rows."""
+    arr = (WriteJob * max(1, len(jobs)))()
+    T = None
+    for i, (src, weight, rope, dst) in enumerate(jobs):
+        if src.dtype != torch.bfloat16 or src.dim() != 3 or src.stride(2) != 1:
+            raise TypeError("src must be bfloat16 [T, H, 128] with unit element stride")
+        if weight is not None and (weight.dtype != torch.float32 or not weight.is_contiguous()):
+            raise TypeError("norm_weight must be a contiguous float32 [128] tensor")
+        T = src.shape[0] if T is None else T
+        assert src.shape[0] == T and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
+        if isinstance(dst, torch.Tensor):
+            assert dst.dtype == torch.bfloat16 and dst.shape == src.shape and dst.stride(2) == 1
+            arr[i] = WriteJob(src.data_ptr(), src.stride(0), src.shape[1], _ptr(weight), int(rope),
+                              Plane(), dst.data_ptr(), dst.stride(0))
+        else:
+            arr[i] = WriteJob(src.data_ptr(), src.stride(0), src.shape[1], _ptr(weight), int(rope),
+                              plane(*dst), None, 0)
+    for t in (rope_cos, rope_sin):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise TypeError("rope_cos / rope_sin must be contiguous float32 [T, rotary_dim / 2]")
+    if slot_mapping is not None and slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    rc = load().m3s_qk_norm_rope_store(arr, len(jobs), 0 if T is None else T, _ptr(slot_mapping),
+                                       _ptr(rope_cos), _ptr(rope_sin), rotary_dim, float(eps),
+                                       _ptr(err), _stream(stream))
+    _check(rc, "m3s_qk_norm_rope_store")
 
 
 def m3s_decode_rows(cu_q: torch.Tensor, seq_len: torch.Tensor, R: int,

@@ -163,6 +163,139 @@ __global__ void __launch_bounds__(256) nvfp4_store_kernel(const StoreBatch batch
   }
 }
 
+// ---- quantise-at-write: RMSNorm / rotate-half RoPE / BF16 round / store ----
+// #2744, Follow-up: MXFP4 caches: the quantisation inside the kernel that
+// normalises, rotates and writes the step's rows. One warp per (job, row,
+// head); lane l owns elements 4l .. 4l+3. Every float operation is rounded on
+// its own and the sum of squares runs in one fixed order, so the BF16 values
+// (and hence the stored bytes) are those of the unfused path.
+struct WriteJob {
+  const uint16_t* src;
+  int64_t stride;
+  int32_t H;
+  int32_t rope;
+  int32_t mx;            // destination plane format (1: MXFP4)
+  const float* weight;   // RMSNorm weight [128] or null
+  uint8_t* codes;        // destination plane, or null when out is given
+  uint8_t* scales;
+  int64_t capacity;
+  uint16_t* out;         // BF16 rows, or null
+  int64_t out_stride;
+  int64_t warp0;         // first warp (over the whole launch) of this job
+};
+
+struct WriteBatch {
+  WriteJob job[M3S_MAX_WRITE_JOBS];
+  int32_t njobs;
+  int64_t total_warps;
+};
+
+__global__ void __launch_bounds__(256) write_kernel(const WriteBatch b, const int64_t* __restrict__ slots,
+                                                   const float* __restrict__ cos_t,
+                                                   const float* __restrict__ sin_t, int32_t rd,
+                                                   float eps, int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= b.total_warps) return;  // warp-uniform
+  int j = 0;
+  while (j + 1 < b.njobs && gw >= b.job[j + 1].warp0) ++j;
+  const WriteJob& jb = b.job[j];
+  const int64_t rh = gw - jb.warp0;
+  const int h = static_cast<int>(rh % jb.H);
+  const int64_t t = rh / jb.H;
+  int64_t slot = 0;
+  if (!jb.out) {
+    slot = slots[t];
+    if (slot < 0) return;  // pad row: untouched (warp-uniform)
+    if (slot >= jb.capacity) {
+      if (lane == 0 && h == 0) raise(err, M3S_DEVERR_SLOT);
+      return;
+    }
+  }
+  const uint2 raw = *reinterpret_cast<const uint2*>(jb.src + t * jb.stride + h * kHeadDim + 4 * lane);
+  float y[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
+                bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
+  if (jb.weight) {
+    float p = __fmul_rn(y[0], y[0]);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) p = __fadd_rn(p, __fmul_rn(y[i], y[i]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off));
+    const float ss = __shfl_sync(0xffffffffu, p, 0);
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), eps)));
+    const float4 w = *reinterpret_cast<const float4*>(jb.weight + 4 * lane);
+    const float wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = __fmul_rn(__fmul_rn(y[i], r), wv[i]);
+  }
+  if (jb.rope) {
+    const int half = rd >> 1;  // a multiple of 4: a pair's partner is half / 4 lanes away
+    const int d0 = 4 * lane;
+    const int partner = d0 < half ? lane + (half >> 2) : (d0 < rd ? lane - (half >> 2) : lane);
+    float py[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) py[i] = __shfl_sync(0xffffffffu, y[i], partner);
+    if (d0 < rd) {
+      const int ci = d0 < half ? d0 : d0 - half;
+      const float4 c4 = *reinterpret_cast<const float4*>(cos_t + t * half + ci);
+      const float4 s4 = *reinterpret_cast<const float4*>(sin_t + t * half + ci);
+      const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        y[i] = d0 < half ? __fsub_rn(__fmul_rn(y[i], c[i]), __fmul_rn(py[i], sn[i]))
+                         : __fadd_rn(__fmul_rn(y[i], c[i]), __fmul_rn(py[i], sn[i]));
+    }
+  }
+  uint32_t bv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) bv[i] = f32_to_bf16_bits(y[i]);
+  if (jb.out) {
+    *reinterpret_cast<uint2*>(jb.out + t * jb.out_stride + h * kHeadDim + 4 * lane) =
+        make_uint2(bv[0] | (bv[1] << 16), bv[2] | (bv[3] << 16));
+    return;
+  }
+  // quantise the BF16 values as the store does: NVFP4 groups of 16 span 4
+  // lanes, MXFP4 groups of 32 span 8
+  uint32_t am = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) am = max(am, bv[i] & 0x7FFFu);
+  am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+  am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+  float s;
+  uint32_t sbyte;
+  if (jb.mx) {
+    am = max(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    const int E = mx_shared_exponent(am);
+    s = pow2_f32(E);
+    sbyte = static_cast<uint32_t>(E + 127);
+  } else {
+    const float q = __fdiv_rn(bf16_bits_to_f32(am), 6.0f);
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(q));
+    sbyte = pair & 0xFFu;
+    const uint32_t sh = e4m3x2_to_f16x2(sbyte);
+    s = __half2float(__ushort_as_half(static_cast<unsigned short>(sh & 0xFFFFu)));
+  }
+  const float mids[7] = {0.25f, 0.75f, 1.25f, 1.75f, 2.5f, 3.5f, 5.0f};
+  float thr[7];
+#pragma unroll
+  for (int i = 0; i < 7; ++i) thr[i] = mids[i] * s;
+  uint32_t code = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) code |= e2m1_code(bv[i], thr) << (4 * i);
+  if (s == 0.0f) code = 0;  // NVFP4: a zero scale stores zero codes
+  const int64_t page = slot / kPage, pos = slot % kPage;
+  const int64_t rec = (page * jb.H + h) * kPage + pos;
+  *reinterpret_cast<uint16_t*>(jb.codes + rec * kCodeBytes + 2 * lane) = static_cast<uint16_t>(code);
+  if (jb.mx) {
+    if ((lane & 7) == 0) jb.scales[rec * kMxScaleBytes + (lane >> 3)] = static_cast<uint8_t>(sbyte);
+  } else {
+    if ((lane & 3) == 0) jb.scales[rec * kScaleBytes + (lane >> 2)] = static_cast<uint8_t>(sbyte);
+  }
+}
+
 __global__ void decode_rows_kernel(const int32_t* __restrict__ cu_q,
                                    const int32_t* __restrict__ seq_len, int32_t B, int32_t R,
                                    int32_t* __restrict__ row_req, int32_t* __restrict__ row_len) {
@@ -246,6 +379,53 @@ extern "C" int m3s_nvfp4_store_batch(const m3s_store_job* jobs, int32_t njobs, i
     if (rc != M3S_OK) return rc;
   }
   return launch_store(jobs, njobs, T, slot_mapping, err, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int m3s_qk_norm_rope_store(const m3s_write_job* jobs, int32_t njobs, int32_t T,
+                                      const int64_t* slot_mapping, const float* rope_cos,
+                                      const float* rope_sin, int32_t rotary_dim, float eps,
+                                      int32_t* err, void* stream) {
+  using namespace m3s;
+  if (T < 0 || njobs < 0 || njobs > M3S_MAX_WRITE_JOBS || (njobs > 0 && !jobs)) return M3S_ERR_INVALID;
+  bool any_rope = false, any_plane = false;
+  WriteBatch b{};
+  b.njobs = njobs;
+  int64_t warps = 0;
+  for (int i = 0; i < njobs; ++i) {
+    const m3s_write_job& j = jobs[i];
+    if (j.H <= 0 || !j.src || !aligned16(j.src) || j.src_row_stride < static_cast<int64_t>(j.H) * kHeadDim ||
+        (j.src_row_stride & 7))
+      return M3S_ERR_INVALID;
+    if (j.norm_weight && !aligned16(j.norm_weight)) return M3S_ERR_INVALID;
+    if (j.out) {
+      if (!aligned16(j.out) || j.out_row_stride < static_cast<int64_t>(j.H) * kHeadDim || (j.out_row_stride & 7))
+        return M3S_ERR_INVALID;
+    } else {
+      const int rc = check_job(j.src, j.src_row_stride, j.H, j.dst);
+      if (rc != M3S_OK) return rc;
+      any_plane = true;
+    }
+    any_rope |= j.rope != 0;
+    b.job[i] = WriteJob{j.src, j.src_row_stride, j.H, j.rope != 0 ? 1 : 0,
+                        (!j.out && j.dst.format == M3S_FMT_MXFP4) ? 1 : 0, j.norm_weight,
+                        j.out ? nullptr : j.dst.codes, j.out ? nullptr : j.dst.scales,
+                        j.out ? 0 : static_cast<int64_t>(j.dst.num_pages) * kPage, j.out,
+                        j.out_row_stride, warps};
+    warps += static_cast<int64_t>(T) * j.H;
+  }
+  if (any_rope && (rotary_dim < 8 || rotary_dim > kHeadDim || (rotary_dim & 7) || !rope_cos || !rope_sin ||
+                   !aligned16(rope_cos) || !aligned16(rope_sin)))
+    return M3S_ERR_INVALID;
+  if (T == 0 || njobs == 0) return M3S_OK;
+  if (any_plane && !slot_mapping) return M3S_ERR_INVALID;
+  b.total_warps = warps;
+  const int64_t blocks = (warps * 32 + 255) / 256;
+  if (blocks > 0x7FFFFFFF) return M3S_ERR_UNSUPPORTED;
+  return launch_kernel(write_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                       static_cast<cudaStream_t>(stream), 0, b, slot_mapping, rope_cos, rope_sin,
+                       any_rope ? rotary_dim : 0, eps, err) == cudaSuccess
+             ? M3S_OK
+             : M3S_ERR_LAUNCH;
 }
 
 extern "C" int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int32_t R,

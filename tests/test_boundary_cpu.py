@@ -110,3 +110,29 @@ def test_plane_format_rules(lib):
     args = (fake, 1, 1, fake, fake, fake, 16, 1, ctypes.c_float(0.1), fake, None, None, 0, None, None)
     assert lib.m3s_sparse_attention(fake, 16, 1, nv, mx, *args) == M.ERR_UNSUPPORTED
     assert lib.m3s_sparse_attention(fake, 16, 1, bad, bad, *args) == M.ERR_INVALID
+
+
+def test_quantise_at_write_host_validation(lib):
+    """m3s_qk_norm_rope_store rejects bad jobs and rotary sizes on the host (nothing
+    is launched: every call below either fails validation or has T = 0)."""
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    fake = ctypes.c_void_p(1 << 20)
+    plane = M.Plane(fake, fake, 4, 2, M.FMT_NVFP4)
+
+    def job(H=2, stride=256, weight=None, rope=0, dst=plane, out=None, out_stride=0):
+        return M.WriteJob(fake, stride, H, weight, rope, dst, out, out_stride)
+
+    def call(jobs, T=1, cos=fake, sin=fake, rd=64, slots=fake):
+        arr = (M.WriteJob * len(jobs))(*jobs)
+        return lib.m3s_qk_norm_rope_store(arr, len(jobs), T, slots, cos, sin, rd,
+                                          ctypes.c_float(1e-6), None, None)
+    assert call([job(rope=1)], rd=60) == M.ERR_INVALID           # not a multiple of 8
+    assert call([job(rope=1)], rd=136) == M.ERR_INVALID          # beyond head_dim
+    assert call([job(rope=1)], cos=None) == M.ERR_INVALID        # no table
+    assert call([job(stride=100)]) == M.ERR_INVALID              # row stride below H * 128
+    assert call([job(H=3)]) == M.ERR_INVALID                     # plane heads mismatch
+    assert call([job(dst=M.Plane(fake, fake, 4, 2, 5))]) == M.ERR_INVALID   # unknown format
+    assert call([job(out=fake, out_stride=200)]) == M.ERR_INVALID          # short output rows
+    assert call([job()], slots=None) == M.ERR_INVALID           # plane job without slots
+    assert call([job()] * 7) == M.ERR_INVALID                    # too many jobs
+    assert call([job(rope=1), job(out=fake, out_stride=256)], T=0) == M.OK
