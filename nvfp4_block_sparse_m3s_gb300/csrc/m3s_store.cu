@@ -190,31 +190,15 @@ struct WriteBatch {
   int64_t total_warps;
 };
 
-__global__ void __launch_bounds__(256) write_kernel(const WriteBatch b, const int64_t* __restrict__ slots,
-                                                   const float* __restrict__ cos_t,
-                                                   const float* __restrict__ sin_t, int32_t rd,
-                                                   float eps, int32_t* err) {
-  pdl_trigger();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (gw >= b.total_warps) return;  // warp-uniform
-  int j = 0;
-  while (j + 1 < b.njobs && gw >= b.job[j + 1].warp0) ++j;
-  const WriteJob& jb = b.job[j];
-  const int64_t rh = gw - jb.warp0;
-  const int h = static_cast<int>(rh % jb.H);
-  const int64_t t = rh / jb.H;
-  int64_t slot = 0;
-  if (!jb.out) {
-    slot = slots[t];
-    if (slot < 0) return;  // pad row: untouched (warp-uniform)
-    if (slot >= jb.capacity) {
-      if (lane == 0 && h == 0) raise(err, M3S_DEVERR_SLOT);
-      return;
-    }
-  }
-  const uint2 raw = *reinterpret_cast<const uint2*>(jb.src + t * jb.stride + h * kHeadDim + 4 * lane);
+// Heads of one row handled by one warp: their loads are all issued before any
+// arithmetic, so a warp keeps this many 256-byte rows in flight.
+constexpr int kWriteHeadsPerWarp = 4;
+
+// One head of one row (its 4 elements per lane in raw): normalise, rotate,
+// round to BF16 and write, as described above.
+__device__ __forceinline__ void write_head(const WriteJob& jb, int64_t t, int h, int64_t slot, uint2 raw,
+                                           const float4& w, const float4& c4, const float4& s4,
+                                           int32_t rd, float eps, int lane) {
   float y[4] = {bf16_bits_to_f32(raw.x & 0xFFFFu), bf16_bits_to_f32(raw.x >> 16),
                 bf16_bits_to_f32(raw.y & 0xFFFFu), bf16_bits_to_f32(raw.y >> 16)};
   if (jb.weight) {
@@ -225,7 +209,6 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteBatch b, const in
     for (int off = 16; off > 0; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off));
     const float ss = __shfl_sync(0xffffffffu, p, 0);
     const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), eps)));
-    const float4 w = *reinterpret_cast<const float4*>(jb.weight + 4 * lane);
     const float wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) y[i] = __fmul_rn(__fmul_rn(y[i], r), wv[i]);
@@ -238,9 +221,6 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteBatch b, const in
 #pragma unroll
     for (int i = 0; i < 4; ++i) py[i] = __shfl_sync(0xffffffffu, y[i], partner);
     if (d0 < rd) {
-      const int ci = d0 < half ? d0 : d0 - half;
-      const float4 c4 = *reinterpret_cast<const float4*>(cos_t + t * half + ci);
-      const float4 s4 = *reinterpret_cast<const float4*>(sin_t + t * half + ci);
       const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -294,6 +274,49 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteBatch b, const in
   } else {
     if ((lane & 3) == 0) jb.scales[rec * kScaleBytes + (lane >> 2)] = static_cast<uint8_t>(sbyte);
   }
+}
+
+__global__ void __launch_bounds__(256) write_kernel(const WriteBatch b, const int64_t* __restrict__ slots,
+                                                   const float* __restrict__ cos_t,
+                                                   const float* __restrict__ sin_t, int32_t rd,
+                                                   float eps, int32_t* err) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= b.total_warps) return;  // warp-uniform
+  int j = 0;
+  while (j + 1 < b.njobs && gw >= b.job[j + 1].warp0) ++j;
+  const WriteJob& jb = b.job[j];
+  const int groups = (jb.H + kWriteHeadsPerWarp - 1) / kWriteHeadsPerWarp;
+  const int64_t rg = gw - jb.warp0;
+  const int h0 = static_cast<int>(rg % groups) * kWriteHeadsPerWarp;
+  const int nh = min(kWriteHeadsPerWarp, jb.H - h0);
+  const int64_t t = rg / groups;
+  int64_t slot = 0;
+  if (!jb.out) {
+    slot = slots[t];
+    if (slot < 0) return;  // pad row: untouched (warp-uniform)
+    if (slot >= jb.capacity) {
+      if (lane == 0 && h0 == 0) raise(err, M3S_DEVERR_SLOT);
+      return;
+    }
+  }
+  uint2 raw[kWriteHeadsPerWarp];
+#pragma unroll
+  for (int k = 0; k < kWriteHeadsPerWarp; ++k)
+    if (k < nh) raw[k] = *reinterpret_cast<const uint2*>(jb.src + t * jb.stride + (h0 + k) * kHeadDim + 4 * lane);
+  float4 w = make_float4(0.f, 0.f, 0.f, 0.f), c4 = w, s4 = w;
+  if (jb.weight) w = *reinterpret_cast<const float4*>(jb.weight + 4 * lane);
+  if (jb.rope && 4 * lane < rd) {
+    const int half = rd >> 1, d0 = 4 * lane;
+    const int ci = d0 < half ? d0 : d0 - half;
+    c4 = *reinterpret_cast<const float4*>(cos_t + t * half + ci);
+    s4 = *reinterpret_cast<const float4*>(sin_t + t * half + ci);
+  }
+#pragma unroll
+  for (int k = 0; k < kWriteHeadsPerWarp; ++k)
+    if (k < nh) write_head(jb, t, h0 + k, slot, raw[k], w, c4, s4, rd, eps, lane);   // nh is warp-uniform
 }
 
 __global__ void decode_rows_kernel(const int32_t* __restrict__ cu_q,
@@ -411,7 +434,7 @@ extern "C" int m3s_qk_norm_rope_store(const m3s_write_job* jobs, int32_t njobs, 
                         j.out ? nullptr : j.dst.codes, j.out ? nullptr : j.dst.scales,
                         j.out ? 0 : static_cast<int64_t>(j.dst.num_pages) * kPage, j.out,
                         j.out_row_stride, warps};
-    warps += static_cast<int64_t>(T) * j.H;
+    warps += static_cast<int64_t>(T) * ((j.H + kWriteHeadsPerWarp - 1) / kWriteHeadsPerWarp);
   }
   if (any_rope && (rotary_dim < 8 || rotary_dim > kHeadDim || (rotary_dim & 7) || !rope_cos || !rope_sin ||
                    !aligned16(rope_cos) || !aligned16(rope_sin)))
