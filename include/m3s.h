@@ -1,6 +1,8 @@
 /*
  * m3s.h -- C ABI of libm3s: the decode / verify step of indexed (top-k block)
- * sparse attention over a paged NVFP4 KV cache, hand-written CUDA for sm_103a.
+ * sparse attention over a paged NVFP4 (or MXFP4) KV cache, with the cache
+ * write optionally fused into the rows' normalisation and rotation,
+ * hand-written CUDA for sm_103a.
  *
  * Source of the method: the pull requests "NVFP4 sparse KV" (ROCm/ATOM #2746)
  * and "[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV cache" (ROCm/ATOM

@@ -27,4 +27,4 @@ extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_
   }
 }
 
-extern "C" const char* m3s_version(void) { return "m3s 0.1 (sm_103a)"; }
+extern "C" const char* m3s_version(void) { return "m3s 0.2 (sm_103a; NVFP4 and MXFP4 planes, quantise-at-write)"; }
