@@ -40,21 +40,27 @@ namespace {
 
 constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;  // one block: 9216 = 9 x 1024
 
-// Roles and resources. Warp 0: producer (bulk copies); warp 1: MMA issuer;
-// warps 2 .. 2 + 4 kNEpi - 1: epilogue warpgroups (block g -> g % kNEpi, which
-// owns accumulator slot g % kND); then kNDQ dequantising warpgroups.
+// Roles and resources. Warp 0: producer (bulk copies); warps 1 .. kND: MMA
+// issuers, one per accumulator slot (block g -> issuer g % kND, so one issuer's
+// commits overlap the other's MMAs); warps 1 + kND .. kND + 4 kNEpi: epilogue
+// warpgroups (block g -> g % kNEpi, which owns accumulator slot g % kND); then
+// kNDQ dequantising warpgroups.
 // Tensor memory: kNA A slots of 64 columns (128 keys x 128 f16) and kND
 // accumulator slots of N = 16 * QT f32 columns.
 template <int QT>
 struct Cfg {
   static_assert(QT % 2 == 0 && QT <= 8, "rows per tile: an even count up to 8");
   static constexpr int kN = 16 * QT;
-  // 14 warps: the register file is split over the four SM sub-partitions, so
-  // at most four warps a partition keeps 128 registers a thread
+  // 15 warps: the register file is split over the four SM sub-partitions, so
+  // at most four warps a partition keep 128 registers a thread (the kernel is
+  // compiled for 512 threads to hold it there)
   static constexpr int kNDQ = 1;
   static constexpr int kNEpi = 2;
-  static constexpr int kWarps = 2 + 4 * kNEpi + 4 * kNDQ;
+  static constexpr int kIssuers = kNEpi;  // == kND
+  static constexpr int kWarps = 1 + kIssuers + 4 * kNEpi + 4 * kNDQ;
   static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kBoundThreads = 512;
+  static_assert(kThreads <= kBoundThreads, "register budget");
   // Stages and A slots are multiples of kNDQ: block g goes to warpgroup g % kNDQ,
   // stage g % kNS and slot g % kNA, so each stage and each slot is only ever used
   // by one warpgroup, in order, and a parity wait can never see a phase two back.
@@ -113,7 +119,7 @@ __device__ __forceinline__ bool role_wait(ScoreSmem<QT>& sm, uint64_t* bar, uint
 // bytes from the plane itself (L2-resident: the stage holding them is recycled
 // long before the epilogue runs).
 template <int QT, bool MX>
-__global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
     score_kernel(const ScoreArgs a, const __grid_constant__ CUtensorMap codes_map) {
   using C = Cfg<QT>;
   constexpr int kPageScaleB = MX ? kMxPageScaleBytes : kPageScaleBytes;
@@ -221,10 +227,11 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       }
-    } else if (warp == 1) {
-      // ================= MMA issuer =================
+    } else if (warp <= C::kIssuers) {
+      // ================= MMA issuers (issuer i: blocks g with g % kND == i) =================
+      const int iss = warp - 1;
       if (lane == 0) {
-        for (int j = 0; j < nseg; ++j) {
+        for (int j = ((iss - g0) % C::kND + C::kND) % C::kND; j < nseg; j += C::kND) {
           const int g = g0 + j;
           const int as = g % C::kNA, ua = g / C::kNA, ds = g % C::kND, ud = g / C::kND;
           if (!role_wait(sm, &sm.afull[as], ua & 1, a.err)) break;
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
           last_ud = ud;
         }
       }
-    } else if (warp < 2 + 4 * C::kNEpi) {
+    } else if (warp < 1 + C::kIssuers + 4 * C::kNEpi) {
       // ================= epilogue warpgroups =================
       // Per block: the accumulator (rows x 16 heads, one key per thread) in two
       // loads of half the rows each; the slot is released to the MMA as soon as
@@ -252,8 +259,8 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
       // row's weighted ReLU head sum runs as two interleaved chains, and the
       // block maximum over the warp's 32 keys is one redux on order-preserving
       // integer keys.
-      const int ep = (warp - 2) >> 2;            // warpgroup: blocks g with g % kNEpi == ep
-      const int etid = tid - 64 - 128 * ep;      // 0 .. 127 within the warpgroup
+      const int ep = (warp - 1 - C::kIssuers) >> 2;          // warpgroup: blocks g with g % kNEpi == ep
+      const int etid = tid - 32 * (1 + C::kIssuers) - 128 * ep;  // 0 .. 127 within the warpgroup
       const int wq = warp & 3;                   // lane quarter: keys 32 wq .. 32 wq + 31
       constexpr int kHalfRows = QT / 2;
       int rlen[QT];
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
       }
     } else {
       // ================= dequantising warpgroups =================
-      const int dq = (warp - 2 - 4 * C::kNEpi) >> 2;    // which warpgroup
+      const int dq = (warp - 1 - C::kIssuers - 4 * C::kNEpi) >> 2;    // which warpgroup
       const int key = tid & 127;         // TMEM lane = key within the block
       const int sw = (key >> 1) & 3;     // 64-byte swizzle of this key's row
       PageWindow pw;
@@ -400,7 +407,8 @@ __global__ void __launch_bounds__(Cfg<QT>::kThreads, 1)
   }
 
   // ---- leave: after a timeout, give the last MMA one more bounded wait; free TMEM ----
-  if (warp == 1 && lane == 0 && mma_issued && sm.abort) mbar_wait(&sm.dfull[last_d], last_ud & 1);
+  if (warp >= 1 && warp <= C::kIssuers && lane == 0 && mma_issued && sm.abort)
+    mbar_wait(&sm.dfull[last_d], last_ud & 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
