@@ -86,8 +86,8 @@ NCU_TRAFFIC = {
                     "m3s_device.cuh": "9fc60929d766978e"},
     },
     ("verify", "score_kernel"): {
-        "bytes": 143_923_968 + 4_821_760,
-        "sources": {"m3s_score.cu": "658d24fe629d8179",
+        "bytes": 143_913_216 + 4_538_112,
+        "sources": {"m3s_score.cu": "81174734b4796ab4",
                     "m3s_score_common.cuh": "76d51994d51a9f16",
                     "m3s_device.cuh": "9fc60929d766978e"},
     },
