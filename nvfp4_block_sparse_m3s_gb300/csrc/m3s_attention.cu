@@ -112,23 +112,18 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   pdl_trigger();
   pdl_wait();
   // q fragments (A operand, heads as rows) in the permuted head-dim order:
-  // k-step j covers dims 32t+4j .. 32t+4j+3 for thread t. Loaded first: they do
-  // not depend on the block list.
-  uint32_t qa[8][4];
-  bool qbad = false;
+  // k-step j covers dims 32t+4j .. 32t+4j+3 for thread t. Their loads go out
+  // first (they do not depend on the block list) and are converted after it, so
+  // warp 0's id, length and page loads do not wait behind them.
+  uint2 qr[8][2];
   {
     const int h0 = g, h1 = g + 8;
     const uint16_t* q0 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h0) * kHeadDim + 32 * t;
     const uint16_t* q1 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h1) * kHeadDim + 32 * t;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      uint2 v0 = make_uint2(0u, 0u), v1 = make_uint2(0u, 0u);
-      if (h0 < a.G) v0 = *reinterpret_cast<const uint2*>(q0 + 4 * j);
-      if (h1 < a.G) v1 = *reinterpret_cast<const uint2*>(q1 + 4 * j);
-      qa[j][0] = bf16x2_to_f16x2(v0.x, qbad);
-      qa[j][1] = bf16x2_to_f16x2(v1.x, qbad);
-      qa[j][2] = bf16x2_to_f16x2(v0.y, qbad);
-      qa[j][3] = bf16x2_to_f16x2(v1.y, qbad);
+      qr[j][0] = h0 < a.G ? *reinterpret_cast<const uint2*>(q0 + 4 * j) : make_uint2(0u, 0u);
+      qr[j][1] = h1 < a.G ? *reinterpret_cast<const uint2*>(q1 + 4 * j) : make_uint2(0u, 0u);
     }
   }
 
@@ -188,6 +183,15 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       n += __popc(keep);
     }
     if (lane == 0) sm.nblocks = n;
+  }
+  uint32_t qa[8][4];
+  bool qbad = false;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    qa[j][0] = bf16x2_to_f16x2(qr[j][0].x, qbad);
+    qa[j][1] = bf16x2_to_f16x2(qr[j][1].x, qbad);
+    qa[j][2] = bf16x2_to_f16x2(qr[j][0].y, qbad);
+    qa[j][3] = bf16x2_to_f16x2(qr[j][1].y, qbad);
   }
   if (qbad) raise(a.err, M3S_DEVERR_QRANGE);
   __syncthreads();

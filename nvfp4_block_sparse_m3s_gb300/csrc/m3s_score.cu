@@ -38,6 +38,17 @@
 namespace m3s {
 namespace {
 
+// (a.x * b.x + c.x, a.y * b.y + c.y): two IEEE fma (round to nearest) in one
+// packed f32x2 instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 pa, pb, pc;\n mov.b64 pa, {%2, %3};\n mov.b64 pb, {%4, %5};\n"
+      " mov.b64 pc, {%6, %7};\n fma.rn.f32x2 pc, pa, pb, pc;\n mov.b64 {%0, %1}, pc;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;  // one block: 9216 = 9 x 1024
 
 // Roles and resources. Warp 0: producer (bulk copies); warps 1 .. kND: MMA
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       // Per block: the accumulator (rows x 16 heads, one key per thread) in two
       // loads of half the rows each; the slot is released to the MMA as soon as
       // the second load has landed, before the second half is reduced. Each
-      // row's weighted ReLU head sum runs as two interleaved chains, and the
+      // row's weighted ReLU head sum runs as packed f32x2 fma (even and odd heads), and the
       // block maximum over the warp's 32 keys is one redux on order-preserving
       // integer keys.
       const int ep = (warp - 1 - C::kIssuers) >> 2;          // warpgroup: blocks g with g % kNEpi == ep
@@ -302,16 +313,17 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
             for (int r = 0; r < kHalfRows; ++r) {
               const int rho = kHalfRows * half + r;
               const float4* w4 = reinterpret_cast<const float4*>(sm.wsm + 16 * rho);
-              float s0 = 0.f, s1 = 0.f;
+              // even heads in .x, odd heads in .y, one packed fma per head pair
+              float2 s = make_float2(0.f, 0.f);
 #pragma unroll
               for (int q4 = 0; q4 < 4; ++q4) {
                 const float4 wv = w4[q4];
-                s0 = fmaf(wv.x, fmaxf(d[16 * r + 4 * q4 + 0], 0.f), s0);
-                s1 = fmaf(wv.y, fmaxf(d[16 * r + 4 * q4 + 1], 0.f), s1);
-                s0 = fmaf(wv.z, fmaxf(d[16 * r + 4 * q4 + 2], 0.f), s0);
-                s1 = fmaf(wv.w, fmaxf(d[16 * r + 4 * q4 + 3], 0.f), s1);
+                s = ffma2(make_float2(wv.x, wv.y),
+                          make_float2(fmaxf(d[16 * r + 4 * q4 + 0], 0.f), fmaxf(d[16 * r + 4 * q4 + 1], 0.f)), s);
+                s = ffma2(make_float2(wv.z, wv.w),
+                          make_float2(fmaxf(d[16 * r + 4 * q4 + 2], 0.f), fmaxf(d[16 * r + 4 * q4 + 3], 0.f)), s);
               }
-              sc[rho] = s0 + s1;
+              sc[rho] = s.x + s.y;
             }
           }
           if constexpr (MX) {   // the key's 2^(E_max - 127): positive, so it commutes with ReLU
@@ -432,10 +444,14 @@ constexpr int kTopkThreads = 1024;
 // 0xFFFFFFFE (local), sit above ordered_bits(+inf). Init keys keep the
 // complemented id (lower id first), local keys the id itself (most recent
 // first), so init + local beyond k keeps the row's newest blocks.
-__device__ __forceinline__ unsigned long long block_key(const float* row, int i, int nb, int init, int local) {
+__device__ __forceinline__ unsigned long long block_key_of(float score, int i, int nb, int init, int local) {
   if (i < init) return (0xFFFFFFFFull << 32) | static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(i));
   if (i >= nb - local) return (0xFFFFFFFEull << 32) | static_cast<unsigned long long>(static_cast<uint32_t>(i));
-  return topk_key(row[i], i);
+  return topk_key(score, i);
+}
+
+__device__ __forceinline__ unsigned long long block_key(const float* row, int i, int nb, int init, int local) {
+  return block_key_of(i < init || i >= nb - local ? 0.f : row[i], i, nb, init, local);
 }
 
 __device__ __forceinline__ unsigned long long topk_key_at(const float* row, const unsigned long long* keys,
@@ -456,6 +472,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // each thread's first score loads while the row's length and request resolve
+  // (inside the row's stride, so always in bounds; used only below the block count)
+  const float first = bscores && tid < bs_stride ? bscores[static_cast<size_t>(r) * bs_stride + tid] : 0.f;
   const int len = row_len[r];
   const int req = row_req ? row_req[r] : 0;
   const bool ok = len > 0 && req >= 0 && req < B && len <= bt_stride * kPage;
@@ -472,7 +491,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   const bool in_smem = nb <= smem_keys;
   unsigned long long kmax = 0, kmin = ~0ull;
   for (int i = tid; i < nb; i += kTopkThreads) {
-    const unsigned long long key = block_key(row, i, nb, init_blocks, local_blocks);
+    const unsigned long long key = i == tid ? block_key_of(first, i, nb, init_blocks, local_blocks)
+                                            : block_key(row, i, nb, init_blocks, local_blocks);
     if (in_smem) keys[i] = key;
     kmax = key > kmax ? key : kmax;
     kmin = key < kmin ? key : kmin;
