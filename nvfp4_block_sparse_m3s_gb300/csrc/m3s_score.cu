@@ -267,9 +267,9 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       // Per block: the accumulator (rows x 16 heads, one key per thread) in two
       // loads of half the rows each; the slot is released to the MMA as soon as
       // the second load has landed, before the second half is reduced. Each
-      // row's weighted ReLU head sum runs as packed f32x2 fma (even and odd heads), and the
-      // block maximum over the warp's 32 keys is one redux on order-preserving
-      // integer keys.
+      // row's weighted ReLU head sum runs as packed f32x2 fma (even heads in one
+      // lane of the pair, odd heads in the other), and the block maximum over
+      // the warp's 32 keys is one redux on order-preserving integer keys.
       const int ep = (warp - 1 - C::kIssuers) >> 2;          // warpgroup: blocks g with g % kNEpi == ep
       const int etid = tid - 32 * (1 + C::kIssuers) - 128 * ep;  // 0 .. 127 within the warpgroup
       const int wq = warp & 3;                   // lane quarter: keys 32 wq .. 32 wq + 31
@@ -444,14 +444,10 @@ constexpr int kTopkThreads = 1024;
 // 0xFFFFFFFE (local), sit above ordered_bits(+inf). Init keys keep the
 // complemented id (lower id first), local keys the id itself (most recent
 // first), so init + local beyond k keeps the row's newest blocks.
-__device__ __forceinline__ unsigned long long block_key_of(float score, int i, int nb, int init, int local) {
+__device__ __forceinline__ unsigned long long block_key(const float* row, int i, int nb, int init, int local) {
   if (i < init) return (0xFFFFFFFFull << 32) | static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(i));
   if (i >= nb - local) return (0xFFFFFFFEull << 32) | static_cast<unsigned long long>(static_cast<uint32_t>(i));
-  return topk_key(score, i);
-}
-
-__device__ __forceinline__ unsigned long long block_key(const float* row, int i, int nb, int init, int local) {
-  return block_key_of(i < init || i >= nb - local ? 0.f : row[i], i, nb, init, local);
+  return topk_key(row[i], i);
 }
 
 __device__ __forceinline__ unsigned long long topk_key_at(const float* row, const unsigned long long* keys,
@@ -472,9 +468,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // each thread's first score loads while the row's length and request resolve
-  // (inside the row's stride, so always in bounds; used only below the block count)
-  const float first = bscores && tid < bs_stride ? bscores[static_cast<size_t>(r) * bs_stride + tid] : 0.f;
   const int len = row_len[r];
   const int req = row_req ? row_req[r] : 0;
   const bool ok = len > 0 && req >= 0 && req < B && len <= bt_stride * kPage;
@@ -491,8 +484,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(
   const bool in_smem = nb <= smem_keys;
   unsigned long long kmax = 0, kmin = ~0ull;
   for (int i = tid; i < nb; i += kTopkThreads) {
-    const unsigned long long key = i == tid ? block_key_of(first, i, nb, init_blocks, local_blocks)
-                                            : block_key(row, i, nb, init_blocks, local_blocks);
+    const unsigned long long key = block_key(row, i, nb, init_blocks, local_blocks);
     if (in_smem) keys[i] = key;
     kmax = key > kmax ? key : kmax;
     kmin = key < kmin ? key : kmin;

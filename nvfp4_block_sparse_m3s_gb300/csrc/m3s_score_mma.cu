@@ -46,7 +46,7 @@ constexpr int kHalfCodeBytes = kHalfKeys * kCodeBytes;        // 4096
 constexpr int kHalfScaleBytes = kHalfKeys * kScaleBytes;      // 512
 constexpr int kStageBytes = kHalfCodeBytes + kHalfScaleBytes; // 4608
 constexpr int kQFragWords = 8 * 2 * 32;                       // k-steps x n-tiles x lanes (uint2)
-constexpr int kSegCost = 10;                                  // set-up of a row segment, in blocks
+constexpr int kSegCost = 6;                                   // set-up of a row segment, in blocks
 static_assert(kQFragWords == kThreads, "one query fragment word per thread");
 
 // MXFP4 factors of one warp's current half: per key the fp16x2 factor of each
