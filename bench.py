@@ -86,8 +86,8 @@ NCU_TRAFFIC = {
                     "m3s_device.cuh": "9fc60929d766978e"},
     },
     ("verify", "score_kernel"): {
-        "bytes": 143_918_592 + 4_325_888,
-        "sources": {"m3s_score.cu": "c91bc13265f90735",
+        "bytes": 143_876_096 + 4_267_264,
+        "sources": {"m3s_score.cu": "48f39476bb096202",
                     "m3s_score_common.cuh": "76d51994d51a9f16",
                     "m3s_device.cuh": "9fc60929d766978e"},
     },

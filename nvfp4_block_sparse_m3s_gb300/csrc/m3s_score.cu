@@ -51,6 +51,28 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 
 constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;  // one block: 9216 = 9 x 1024
 
+// The CTA ranges are cut in a cost space where every tile costs its blocks plus
+// kTileSetUp: a tile segment that a CTA takes on stages that tile's queries and
+// refills the role pipeline after the CTA-wide barrier that ends its previous
+// segment (about 5 us, some 7 blocks, on the verify batch), so a CTA whose
+// range spans two tiles is given that many fewer blocks.
+constexpr int kTileSetUp = 7;
+
+// Block position of cost position x, where tile t spans [pre[t] + c t,
+// pre[t + 1] + c (t + 1)) in cost space: its first c units are its set-up, the
+// rest one unit per block. Monotone, so consecutive cost ranges give
+// contiguous, disjoint block ranges covering every block.
+__device__ __forceinline__ int tile_cost_to_block(const int* pre, int ntiles, long long x, int c) {
+  if (x >= pre[ntiles] + static_cast<long long>(c) * ntiles) return pre[ntiles];
+  int l = 0, h = ntiles;   // pc(l) <= x < pc(h)
+  while (h - l > 1) {
+    const int m = (l + h) >> 1;
+    if (pre[m] + static_cast<long long>(c) * m <= x) l = m; else h = m;
+  }
+  const long long o = x - (pre[l] + static_cast<long long>(c) * l);
+  return pre[l] + static_cast<int>(o > c ? o - c : 0);
+}
+
 // Roles and resources. Warp 0: producer (bulk copies); warps 1 .. kND: MMA
 // issuers, one per accumulator slot (block g -> issuer g % kND, so one issuer's
 // commits overlap the other's MMAs); warps 1 + kND .. kND + 4 kNEpi: epilogue
@@ -173,9 +195,9 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
   // ---- exclusive prefix of block counts over tiles, then this CTA's range ----
   tile_prefix<QT>(a, pre, red, C::kThreads);
   const int ntiles = a.ntiles;
-  const long long N = pre[ntiles];
-  const int lo = static_cast<int>(N * blockIdx.x / gridDim.x);
-  const int hi = static_cast<int>(N * (blockIdx.x + 1) / gridDim.x);
+  const long long cost = pre[ntiles] + static_cast<long long>(kTileSetUp) * ntiles;
+  const int lo = tile_cost_to_block(pre, ntiles, cost * blockIdx.x / gridDim.x, kTileSetUp);
+  const int hi = tile_cost_to_block(pre, ntiles, cost * (blockIdx.x + 1) / gridDim.x, kTileSetUp);
   int tile = tile_at(pre, ntiles, lo);
 
   int g0 = 0;               // sequence number of the segment's first block in this CTA
