@@ -102,6 +102,8 @@ CASES = [
     ("tiny", (4096,), (1,), False),
     ("decode", (1000, 3000, 129, 128, 5000, 257), (1,) * 6, False),
     ("verify", (700, 2500, 1300, 999), (8, 3, 8, 1), True),
+    # 20 + 3 rows: three 8-row tiles per request, two of the second request's empty
+    ("verify-uneven", (1500, 2200), (20, 3), True),
     ("skewed", (9000, 3000, 3000, 3000), (1, 1, 1, 1), False),
     ("prefill", (2000,), (40,), True),
 ]
@@ -110,7 +112,7 @@ CASES = [
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_step_small_vs_oracle(lib, case):
     name, ctx, qr, fused = case
-    wl = W.make(name, ctx=ctx, q_rows=qr)
+    wl = W.make(name.split("-")[0], ctx=ctx, q_rows=qr)
     s = wl.spec
     dev = DeviceCache(wl)
     dev.store_all()
