@@ -44,6 +44,12 @@ def parse():
     ap.add_argument("--workload", default="skewed",
                     choices=["tiny", "decode", "verify", "skewed", "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="measure the headline workload only (default: all five, the others "
+                         "reported under per_workload)")
+    ap.add_argument("--topk-path", choices=["fused", "pair"], default="fused",
+                    help="decode rows: fused = m3s_index_score_topk (the top-k merged inside the "
+                         "scorer); pair = m3s_index_block_scores then m3s_block_topk")
     ap.add_argument("--cache-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="K / V / index-K record format")
     ap.add_argument("--write-path", choices=["store", "fused", "staged"], default="store",
@@ -53,6 +59,7 @@ def parse():
                          "staging rows that the batched store then quantises (the unfused path)")
     ap.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--oracle-reps", type=int, default=2, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-procs", type=int, default=1, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -132,6 +139,9 @@ def job_rows_per_s(world: int, rows_per_rank: int, ms: float) -> float:
     return world * rows_per_rank / (ms * 1e-3)
 
 
+#: kernels each way of running score + top-k launches per call
+SCORE_CALL_LAUNCHES = {"verify": 2, "index": 2, "pair": 2}
+
 #: bytes per token and head of a K, V or index-K record
 RECORD_BYTES = {"nvfp4": 72, "mxfp4": 68}
 
@@ -159,20 +169,12 @@ def workload_config(spec, ntok, fmt="nvfp4"):
 
 
 # --------------------------------------------------------------------------
-# The CPU oracle arm (also the cpu_baseline sample)
+# The CPU oracle arm (also the cpu_baseline samples)
 # --------------------------------------------------------------------------
 
-def oracle_sample(spec_name: str, reps: int, fmt: str = "nvfp4"):
-    """Time the oracle's step for a bounded sample of the workload.
-
-    The sample is the last request's step restricted to at most 8 of its
-    rows, evenly spaced and always including its last row: the new K / V /
-    index-K rows of those positions stored, the request's row map, score +
-    top-k over each sampled row's causal keys and attention over its selected
-    blocks. The whole batch's step is extrapolated from it by the ratio of
-    causal keys scored (scoring dominates the oracle's time).
-    Returns (seconds per sample step, description, rows in the batch, scale).
-    """
+def _oracle_request(spec_name: str, fmt: str, b: int):
+    """The oracle's resident cache of request b (setup, untimed): the pool's
+    planes with the request's tokens stored, its source rows and step inputs."""
     import numpy as np
 
     from nvfp4_block_sparse_m3s_gb300 import workloads as W
@@ -180,64 +182,175 @@ def oracle_sample(spec_name: str, reps: int, fmt: str = "nvfp4"):
 
     wl = W.make(spec_name, with_cache_src=False)
     s = wl.spec
-    b = s.batch - 1
     L = int(wl.seq_len[b])
     t0, t1 = int(wl.tok_off[b]), int(wl.tok_off[b + 1])
-    nb = (L + 127) // 128
     qb = int(wl.cu_q[b + 1] - wl.cu_q[b])
     r0 = int(wl.cu_q[b])
-    nsamp = min(qb, 8)
-    sample = sorted({int(round(i * (qb - 1) / max(1, nsamp - 1))) for i in range(nsamp)} | {qb - 1})
     mx = fmt == "mxfp4"
-    kc, ks = O.new_planes(wl.num_pages, s.hkv, mx=mx)
-    vc, vs = O.new_planes(wl.num_pages, s.hkv, mx=mx)
-    ic, is_ = O.new_planes(wl.num_pages, 1, mx=mx)
+    planes = {}
     srcs = {}
-    for name, h, c, sc in (("k", s.hkv, kc, ks), ("v", s.hkv, vc, vs), ("ik", 1, ic, is_)):
+    for name, h in (("k", s.hkv), ("v", s.hkv), ("ik", 1)):
+        c, sc = O.new_planes(wl.num_pages, h, mx=mx)
         src = W.bf16_tensor(s.seed, name, (wl.ntok, h, 128), s.n_out, s.out_factor, rows=(t0, t1))
-        srcs[name] = src
-        O.nvfp4_store(src, wl.slot_all[t0:t1], c, sc)          # the resident cache (setup)
+        O.nvfp4_store(src, wl.slot_all[t0:t1], c, sc)          # the resident cache
+        planes[name], srcs[name] = (c, sc), src
+    new = wl.new_tok[(wl.new_tok >= t0) & (wl.new_tok < t1)] - t0   # this step's rows of b
+    return {"wl": wl, "b": b, "L": L, "t0": t0, "qb": qb, "r0": r0, "planes": planes,
+            "srcs": srcs, "new": new}
+
+
+def _oracle_step(st, rows):
+    """One timed oracle step of request ``st`` restricted to its local rows
+    ``rows``: their new K / V / index-K rows stored, the request's row map,
+    score + top-k and attention for those rows. Returns (seconds, causal keys)."""
+    import numpy as np
+
+    from oracle import m3s_oracle as O
+
+    wl, b, qb, r0, t0 = st["wl"], st["b"], st["qb"], st["r0"], st["t0"]
+    s = wl.spec
+    (kc, ks), (vc, vs), (ic, is_) = st["planes"]["k"], st["planes"]["v"], st["planes"]["ik"]
     cu = np.array([0, qb], dtype=np.int32)
-    seq = np.array([L], dtype=np.int32)
+    seq = np.array([st["L"]], dtype=np.int32)
     bt = wl.block_table[b: b + 1]
-    new = wl.new_tok[(wl.new_tok >= t0) & (wl.new_tok < t1)] - t0    # this step's rows of b
-    new = new[np.array(sample)] if len(new) == qb else new
+    new = st["new"]
+    new = new[np.array(rows)] if len(new) == qb else new
     q_idx, wgt, q = wl.q_idx[r0: r0 + qb], wl.w[r0: r0 + qb], wl.q[r0: r0 + qb]
-    times = []
+    t = time.perf_counter()
+    for name, (c, sc) in st["planes"].items():
+        O.nvfp4_store(st["srcs"][name][new], wl.slot_all[t0 + new], c, sc)
+    rr, rl = O.decode_rows(cu, seq, qb)
+    ids, _, _ = O.index_score_topk(q_idx, wgt, ic, is_, bt, rr, rl, s.topk, rows=rows)
+    O.sparse_attention(q, s.hkv, kc, ks, vc, vs, bt, rr, rl, ids, SM_SCALE, rows=rows)
+    dt = time.perf_counter() - t
+    return dt, int(sum(int(rl[r]) for r in rows))
+
+
+def _spread(n_all: int, n: int):
+    """At most n indices in [0, n_all), evenly spaced, the last one included."""
+    n = max(1, min(n, n_all))
+    return sorted({int(round(i * (n_all - 1) / max(1, n - 1))) for i in range(n)} | {n_all - 1})
+
+
+def _batch_keys(spec_name: str) -> float:
+    import numpy as np
+
+    from nvfp4_block_sparse_m3s_gb300 import workloads as W
+    from oracle import m3s_oracle as O
+
+    wl = W.make(spec_name, with_cache_src=False)
+    _, rl = O.decode_rows(wl.cu_q, wl.seq_len, wl.spec.rows)
+    return float(np.sum(rl.astype(np.float64)))
+
+
+def oracle_sample(spec_name: str, reps: int, fmt: str = "nvfp4"):
+    """Time the oracle's step for a bounded sample of the workload, on one core.
+
+    The sample is the last request's step restricted to at most 8 of its
+    rows, evenly spaced and always including its last row. The whole batch's
+    step is extrapolated from it by the ratio of causal keys scored (scoring
+    dominates the oracle's time).
+    Returns (seconds per sample step, description, rows in the batch, scale).
+    """
+    from nvfp4_block_sparse_m3s_gb300 import workloads as W
+
+    spec = W.SPECS[spec_name]
+    b = spec.batch - 1
+    st = _oracle_request(spec_name, fmt, b)
+    sample = _spread(st["qb"], 8)
+    times, keys = [], 0
     for _ in range(reps):
-        t = time.perf_counter()
-        for name, c, sc in (("k", kc, ks), ("v", vc, vs), ("ik", ic, is_)):
-            O.nvfp4_store(srcs[name][new], wl.slot_all[t0 + new], c, sc)
-        rr, rl = O.decode_rows(cu, seq, qb)
-        ids, _, _ = O.index_score_topk(q_idx, wgt, ic, is_, bt, rr, rl, s.topk, rows=sample)
-        O.sparse_attention(q, s.hkv, kc, ks, vc, vs, bt, rr, rl, ids, SM_SCALE, rows=sample)
-        times.append(time.perf_counter() - t)
-    t_sample = min(times)
-    _, rl_all = O.decode_rows(wl.cu_q, wl.seq_len, s.rows)
-    keys_all = float(np.sum(rl_all.astype(np.float64)))
-    keys_sample = float(sum(int(rl[r]) for r in sample))
-    scale = keys_all / keys_sample
-    desc = (f"oracle step of {len(sample)} of the {qb} row(s) of request {b} ({L} cached tokens),"
-            f" timed {reps}x (best), scaled by causal keys x{scale:.2f} to the batch of"
-            f" {s.rows} rows")
-    return t_sample, desc, s.rows, scale
+        dt, keys = _oracle_step(st, sample)
+        times.append(dt)
+    scale = _batch_keys(spec_name) / keys
+    desc = (f"oracle step of {len(sample)} of the {st['qb']} row(s) of request {b} ({st['L']} cached"
+            f" tokens), timed {reps}x (best), scaled by causal keys x{scale:.2f} to the batch of"
+            f" {spec.rows} rows")
+    return min(times), desc, spec.rows, scale
+
+
+def oracle_units(spec_name: str, n: int):
+    """A sample of the workload cut into at most n units of work, one per
+    process: one request per unit (up to 8 of its rows, evenly spaced) while the
+    batch has at least n requests, else the last request's rows spread over
+    the units (two rows each)."""
+    from nvfp4_block_sparse_m3s_gb300 import workloads as W
+
+    spec = W.SPECS[spec_name]
+    B = spec.batch
+    if B >= n or spec.q_rows[-1] < 2:
+        return [(b, _spread(spec.q_rows[b], 8)) for b in range(max(0, B - n), B)]
+    rows = _spread(spec.q_rows[-1], 2 * n)
+    return [(B - 1, rows[i::n]) for i in range(n) if rows[i::n]]
+
+
+def _oracle_unit_proc(spec_name, fmt, b, rows, barrier, out_q):
+    """One process of the multi-core oracle leg: set up, wait for the others,
+    time its unit."""
+    st = _oracle_request(spec_name, fmt, b)
+    barrier.wait(timeout=900)
+    dt, keys = _oracle_step(st, rows)
+    out_q.put((b, len(rows), dt, keys))
+
+
+def oracle_multicore(spec_name: str, procs: int, fmt: str = "nvfp4"):
+    """The oracle on several host cores: the units of ``oracle_units`` each in
+    their own process (spawned, one BLAS thread each), set up in parallel, then
+    timed together after a barrier. The parallel time is the slowest unit's; the
+    batch is extrapolated from the sampled units by causal keys."""
+    import multiprocessing as mp
+
+    units = oracle_units(spec_name, procs)
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(len(units))
+    out_q = ctx.Queue()
+    ps = [ctx.Process(target=_oracle_unit_proc, args=(spec_name, fmt, b, rows, barrier, out_q))
+          for b, rows in units]
+    for p in ps:
+        p.start()
+    res = [out_q.get(timeout=1800) for _ in ps]
+    for p in ps:
+        p.join()
+    t_par = max(r[2] for r in res)
+    keys = sum(r[3] for r in res)
+    nrows = sum(r[1] for r in res)
+    scale = _batch_keys(spec_name) / keys
+    desc = (f"{len(units)} processes, one unit each ({nrows} sampled rows over "
+            f"{len(set(r[0] for r in res))} request(s)), timed together after a barrier: the "
+            f"slowest unit's time, scaled by causal keys x{scale:.2f} to the batch")
+    return t_par, desc, len(units), scale
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def run_oracle_leg(args):
-    t, desc, rows, scale = oracle_sample(args.workload, args.oracle_reps, args.cache_format)
+    from nvfp4_block_sparse_m3s_gb300 import workloads as W
+    rows = W.SPECS[args.workload].rows
+    if args.oracle_procs > 1:
+        t, desc, cores, scale = oracle_multicore(args.workload, args.oracle_procs, args.cache_format)
+    else:
+        t, desc, _, scale = oracle_sample(args.workload, args.oracle_reps, args.cache_format)
+        cores = 1
     print(json.dumps({"seconds_per_sample": t, "sample": desc, "rows": rows, "scale": scale,
-                      "value": rows / (t * scale), "cores": 1}))
+                      "value": rows / (t * scale), "cores": cores}))
 
 
-def cpu_baseline(workload: str, reps: int = 2, fmt: str = "nvfp4"):
+def cpu_baseline(workload: str, reps: int = 2, fmt: str = "nvfp4", procs: int = 1):
+    """The oracle leg in a child process (one BLAS thread per process)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload",
-                        workload, "--oracle-reps", str(reps), "--cache-format", fmt],
-                       capture_output=True, text=True, env=env, timeout=900)
+                        workload, "--oracle-reps", str(reps), "--cache-format", fmt,
+                        "--oracle-procs", str(procs)],
+                       capture_output=True, text=True, env=env, timeout=1800)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1] if r.stderr.strip() else "failed"}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["value"], "unit": "rows/s", "cores": 1, "kind": "oracle",
+    return {"value": d["value"], "unit": "rows/s", "cores": d["cores"], "kind": "oracle",
             "sample": d["sample"]}
 
 
@@ -350,24 +463,20 @@ class Clocks:
                 "source": "NVML, 2 ms sampling during the timed region"}
 
 
-def run_ours(args):
+def measure_workload(name, args, dev, world):
+    """One workload on this rank's GPU: its cache made resident by our store
+    (untimed), then the step timed as one CUDA graph, the scorer and the
+    attention timed from the same graph with event nodes around them, one graph
+    per phase for the breakdown, and the step end to end from pinned host
+    memory, both replayed as one graph and called eagerly through the C ABI.
+    Returns the workload's figures; frees its device memory on return."""
     import numpy as np
     import torch
-    import torch.distributed as dist
 
     from nvfp4_block_sparse_m3s_gb300 import binding as M
     from nvfp4_block_sparse_m3s_gb300 import workloads as W
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    M.load()
-
-    spec = W.SPECS[args.workload]
+    spec = W.SPECS[name]
     wl = W.make(spec)
     s = wl.spec
     R = s.rows
@@ -388,6 +497,7 @@ def run_ours(args):
         t = bf16(src)
         M.m3s_nvfp4_store(t, slot_all, c, sc, err)
         del t
+    del slot_all
     torch.cuda.synchronize()
     new = wl.new_tok
     host_in = {
@@ -415,13 +525,10 @@ def run_ours(args):
     # The step's inputs live in one device buffer (each tensor at a 256-byte
     # aligned offset) mirrored by one pinned host buffer, so the end-to-end run
     # moves them with a single host-to-device copy; the outputs likewise.
-    def pack_layout(arrays):
-        offs, total = {}, 0
-        for k, v in arrays.items():
-            offs[k] = total
-            total += (v.nbytes + 255) // 256 * 256
-        return offs, total
-    in_off, in_bytes = pack_layout(host_in)
+    in_off, in_bytes = {}, 0
+    for k, v in host_in.items():
+        in_off[k] = in_bytes
+        in_bytes += (v.nbytes + 255) // 256 * 256
     dev_in = torch.zeros(in_bytes, dtype=torch.uint8, device=dev)
     pin_in = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
     d = {}
@@ -452,18 +559,20 @@ def run_ours(args):
         n = int(np.prod(shape)) * es
         return dev_out[out_off[k]: out_off[k] + n].view(dt).view(shape)
     ids = out_view("ids")
-    bscores = torch.empty((R, bt_stride), dtype=torch.float32, device=dev)
     out = out_view("out")
+    bscores = torch.empty((R, bt_stride), dtype=torch.float32, device=dev)
     lse = torch.empty((R, s.hq), dtype=torch.float32, device=dev)
-    ws_v = torch.empty(max(16, M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, R, B, bt_stride, 0, 0,
+    # workspaces (zeroed once at allocation)
+    ws_i = torch.zeros(max(16, M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, R, B, bt_stride, 0, 0,
+                                                     s.hi, s.topk, 1)),
+                       dtype=torch.uint8, device=dev)
+    ws_v = torch.zeros(max(16, M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, R, B, bt_stride, 0, 0,
                                                      s.hi, s.topk, max(s.q_rows))),
                        dtype=torch.uint8, device=dev)
-    ws_a = torch.empty(max(16, M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, R, B, bt_stride, s.hq,
+    ws_a = torch.zeros(max(16, M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, R, B, bt_stride, s.hq,
                                                      s.hkv, 0, s.topk)),
                        dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    ev_s0, ev_s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-
     side = torch.cuda.Stream(device=dev)
 
     def pre():
@@ -490,28 +599,31 @@ def run_ours(args):
 
     q_in = d["q"] if write_path == "store" else q_n
     qidx_in = d["q_idx"] if write_path == "store" else qidx_n
+    topk_pair = getattr(args, "topk_path", "fused") == "pair"
 
     def score():
         if fused:
             M.m3s_verify_score_topk(qidx_in, d["w"], ic, is_, bt, d["cu_q"], row_len,
                                     max(s.q_rows), s.topk, ids, ws_v, err)
-        else:
+        elif topk_pair:
             M.m3s_index_block_scores(qidx_in, d["w"], ic, is_, bt, row_req, row_len, bscores, err)
+        else:
+            M.m3s_index_score_topk(qidx_in, d["w"], ic, is_, bt, row_req, row_len, s.topk, ids,
+                                   None, ws_i, err)
 
     def topk():
-        if not fused:
-            M.m3s_block_topk(bscores, row_req, row_len, B, bt_stride, s.topk, ids)
+        M.m3s_block_topk(bscores, row_req, row_len, B, bt_stride, s.topk, ids)
 
     def attn():
         M.m3s_sparse_attention(q_in, s.hkv, kc, ks, vc, vs, bt, row_req, row_len, ids, SM_SCALE,
                                out, lse, ws_a, err)
 
     # eager warm-up (sets kernel attributes), then the whole step as one CUDA
-    # graph (the timed step), and the same step with the scorer bracketed by two
-    # event-record nodes (an event node between two kernels breaks their
-    # programmatic-launch overlap, so this copy times the scorer and not the
-    # step); one graph per phase is kept for the per-phase breakdown
-    phases = [pre, score, topk, attn] if not fused else [pre, score, attn]
+    # graph (the timed step), and the same step with event-record nodes around
+    # the scorer and around the attention (an event node between two kernels
+    # breaks their programmatic-launch overlap, so this copy times those two
+    # kernels and not the step); one graph per phase for the breakdown
+    phases = [pre, score, topk, attn] if (topk_pair and not fused) else [pre, score, attn]
     for _ in range(2):
         for fn in phases:
             fn()
@@ -524,7 +636,7 @@ def run_ours(args):
             fn()
         graphs.append(g)
     try:
-        sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        sev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
     except TypeError:   # a torch without event-record nodes in graphs
         sev = None
     whole = whole_ev = None
@@ -535,12 +647,16 @@ def run_ours(args):
                 fn()
         whole_ev = torch.cuda.CUDAGraph()
         with torch.cuda.graph(whole_ev, stream=cap):
-            for j, fn in enumerate(phases):
-                if j == 1:
+            for fn in phases:
+                if fn is score:
                     sev[0].record()
+                if fn is attn:
+                    sev[2].record()
                 fn()
-                if j == 1:
+                if fn is score:
                     sev[1].record()
+                if fn is attn:
+                    sev[3].record()
     torch.cuda.synchronize()
 
     def step(phase_events=None):
@@ -555,9 +671,10 @@ def run_ours(args):
         if phase_events:
             phase_events[-1].record(stream)
 
-    # batched store (or quantise-at-write; staged: + the store), row map, scorer,
-    # top-k, attention
-    launches_per_step = 5 + (1 if write_path == "staged" else 0)
+    # our kernels per step: store (or quantise-at-write; staged: + the store), row
+    # map, the scorer call's kernels, attention
+    launches_per_step = 3 + (1 if write_path == "staged" else 0) + SCORE_CALL_LAUNCHES[
+        "verify" if fused else ("pair" if topk_pair else "index")]
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -568,7 +685,8 @@ def run_ours(args):
         flush_buf.fill_(1)
         flush_buf.max()
 
-    for _ in range(max(3, args.warmup)):
+    warm = max(3, args.warmup)
+    for _ in range(warm):
         step()
         flush()
     torch.cuda.synchronize()
@@ -582,8 +700,8 @@ def run_ours(args):
         sel = ids_h[req_h == b]
         distinct += len(set(int(x) for x in sel.ravel() if x >= 0))
     keys = int(np.sum(host_in["seq_len"].astype(np.int64)))
-    nb_rows = int(np.sum((row_len.cpu().numpy().astype(np.int64) + 127) // 128))
-    score_bytes = keys * rec_bytes + R * s.hi * (256 + 4) + nb_rows * 4
+    rl = row_len.cpu().numpy().astype(np.int64)
+    score_bytes = keys * rec_bytes + R * s.hi * (256 + 4) + R * s.topk * 4
     attn_bytes = distinct * 128 * 2 * rec_bytes * s.hkv + R * s.hq * 256 * 2
     store_bytes = R * (2 * s.hkv + 1) * (256 + rec_bytes)
     if write_path != "store":   # the queries read and written back normalised / rotated
@@ -591,6 +709,7 @@ def run_ours(args):
     step_bytes = score_bytes + attn_bytes + store_bytes + R * 8
 
     # ---- timed region (device time, per step, L2 flushed between steps) ----
+    import torch.distributed as dist
     clocks = Clocks(dev)
     if world > 1:
         dist.barrier()
@@ -598,41 +717,27 @@ def run_ours(args):
     clocks.start()
     pev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
            for _ in range(args.steps)]
-    sev_ms, ms_ev = [], []
-    if whole is not None:
-        # one graph launch per step
-        for i in range(args.steps):
-            flush()
-            pev[i][0].record(stream)
-            step()
-            pev[i][-1].record(stream)
-        # the scorer's duration: the step graph with the two event nodes; the
-        # in-graph events are re-recorded by every replay, so each step is read
-        # back before the next one
-        for i in range(args.steps):
-            flush()
-            ev_s0.record(stream)
-            whole_ev.replay()
-            ev_s1.record(stream)
-            torch.cuda.synchronize()
-            sev_ms.append(sev[0].elapsed_time(sev[1]))
-            ms_ev.append(ev_s0.elapsed_time(ev_s1))
-    else:
-        for i in range(args.steps):
-            flush()
-            step(pev[i])
+    for i in range(args.steps):
+        flush()
+        pev[i][0].record(stream)
+        step()
+        pev[i][-1].record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
     ms = sum(e[0].elapsed_time(e[-1]) for e in pev) / args.steps
-    if whole is not None:
-        score_ms = sum(sev_ms) / args.steps
-    else:
-        score_ms = sum(e[1].elapsed_time(e[2]) for e in pev) / args.steps
-    ms, score_ms = max_over_ranks([ms, score_ms], dev)
-    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
-
+    # the scorer's and the attention's durations: the step graph with event
+    # nodes; the in-graph events are re-recorded by every replay, so each step
+    # is read back before the next one
+    score_l, attn_l = [], []
+    if whole_ev is not None:
+        for i in range(args.steps):
+            flush()
+            whole_ev.replay()
+            torch.cuda.synchronize()
+            score_l.append(sev[0].elapsed_time(sev[1]))
+            attn_l.append(sev[2].elapsed_time(sev[3]))
     # per-phase breakdown (one graph per phase, events between them; not the
     # headline: the graph boundaries add launch gaps the whole-step graph has not)
     ph_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
@@ -643,6 +748,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     phase_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in ph_ev) / args.steps
                 for j in range(len(phases))]
+    if not score_l:
+        score_l = [sum(e[phases.index(score)].elapsed_time(e[phases.index(score) + 1]) for e in ph_ev) / args.steps]
+        attn_l = [phase_ms[phases.index(attn)]]
+    score_ms = sum(score_l) / len(score_l)
+    attn_ms = sum(attn_l) / len(attn_l)
+    ms, score_ms, attn_ms = max_over_ranks([ms, score_ms, attn_ms], dev)
+    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
 
     # ---- end to end through the public API with host buffers ----
     # (every step's inputs from pinned host memory in one copy, its outputs back
@@ -651,9 +763,8 @@ def run_ours(args):
     h2d, d2h = in_bytes, out_bytes
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
-    # the copy in, the step and the copy out as one graph (one launch per step,
-    # as a serving loop would replay it); eager copies around the step graph
-    # where graphs are not available
+    # (a) the copy in, the step and the copy out as one graph (one launch per
+    # step, as a serving loop would replay it)
     e2e_graph = None
     if whole is not None:
         try:
@@ -663,13 +774,12 @@ def run_ours(args):
                 for fn in phases:
                     fn()
                 pin_out.copy_(dev_out, non_blocking=True)
-            for _ in range(max(3, args.warmup)):
+            for _ in range(warm):
                 e2e_graph.replay()
             torch.cuda.synchronize()
         except RuntimeError:
             e2e_graph = None
             torch.cuda.synchronize()
-
     for i in range(args.steps):
         flush()
         e2e_ev[i][0].record(stream)
@@ -682,12 +792,29 @@ def run_ours(args):
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
-    e2e_ms, = max_over_ranks([e2e_ms], dev)
+    # (b) eager: every step calls the C-ABI entry points afresh through the
+    # binding (host validation, tensor-map encode, launch), between the two
+    # copies; the GPU is idle when the first event is recorded (host sync after
+    # the flush), so the host's call overhead is inside the interval
+    eager_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        torch.cuda.synchronize()
+        eager_ev[i][0].record(stream)
+        dev_in.copy_(pin_in, non_blocking=True)
+        for fn in phases:
+            fn()
+        pin_out.copy_(dev_out, non_blocking=True)
+        eager_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    eager_ms = sum(a.elapsed_time(b) for a, b in eager_ev) / args.steps
+    e2e_ms, eager_ms = max_over_ranks([e2e_ms, eager_ms], dev)
+    assert int(err.item()) == 0, f"device error bits {int(err.item())}"
 
     hbm_peak, tc_peak, src = peaks()
     # the scorer's binding roofline: bytes at the HBM peak against f16 tensor-core
     # flops (every causal key x index head x 128-dim dot product) at the dense peak
-    rl = row_len.cpu().numpy().astype(np.int64)
     score_flops = float(np.sum(rl)) * s.hi * 128 * 2
     t_hbm = score_bytes / (hbm_peak * 1e9)
     t_tc = score_flops / (tc_peak * 1e12)
@@ -699,45 +826,110 @@ def run_ours(args):
         bound, unit, peak = "hbm", "GB/s", hbm_peak
         achieved = score_bytes / (score_ms * 1e-3) / 1e9
         peak_name = "hbm_gbs"
+    psrc = (lambda nm: f"measured (MEASURED_PEAKS.json {nm})" if src == "measured" else "fallback")
+    score_kernel = ("score_kernel<8> (m3s_verify_score_topk)" if fused else
+                    ("score_decode_kernel (m3s_index_block_scores)" if topk_pair else
+                     "score_decode_kernel (m3s_index_score_topk, top-k merged inside)"))
+    attn_gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
+    return {
+        "name": s.name,
+        "config": dict(workload_config(s, keys, args.cache_format), write_path=write_path),
+        "rows": R,
+        "ms_per_step": ms,
+        "rows_per_s": job_rows_per_s(world, R, ms),
+        "achieved_gbs_step": world * step_bytes / (ms * 1e-3) / 1e9,
+        "algorithmic_bytes_per_step": step_bytes,
+        "scorer": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                   "frac": achieved / peak,
+                   "traffic": ncu_traffic(s.name + ("-mxfp4" if mx else ""),
+                                          "score_kernel" if fused else "score_decode_kernel"),
+                   "kernel": score_kernel, "kernel_ms": score_ms, "bytes_per_launch": score_bytes,
+                   "flops_per_launch": score_flops,
+                   "hbm_gbs_achieved": score_bytes / (score_ms * 1e-3) / 1e9,
+                   "peak_source": psrc(peak_name)},
+        "attention": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
+                      "frac": attn_gbs / hbm_peak, "kernel": "attention_kernel (m3s_sparse_attention)",
+                      "kernel_ms": attn_ms, "bytes_per_launch": attn_bytes,
+                      "peak_source": psrc("hbm_gbs")},
+        "e2e": {"value": job_rows_per_s(world, R, e2e_ms), "unit": "rows/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "copies": ("pinned host <-> device, nodes of the step's graph" if e2e_graph is not None
+                           else "pinned host <-> device, stream copies around the step graph")},
+        "e2e_eager": {"value": job_rows_per_s(world, R, eager_ms), "unit": "rows/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "how": "every step calls the C-ABI entry points afresh between the pinned-host "
+                             "copies; timed from an idle GPU, so host call overhead is included"},
+        "gpu_launches": launches_per_step * args.steps,
+        "step_graph": "one graph per step" if whole is not None else "one graph per phase",
+        "phases_ms_separate_graphs": {fn.__name__: round(v, 5) for fn, v in zip(phases, phase_ms)},
+        "clocks": clk,
+        "warmup": warm,
+    }
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    M.load()
+
+    names = [args.workload]
+    if not args.no_per_workload:
+        names += [n for n in ("tiny", "decode", "verify", "skewed", "prefill") if n != args.workload]
+    res = {}
+    for n in names:
+        res[n] = measure_workload(n, args, dev, world)
+        torch.cuda.empty_cache()
+    h = res[args.workload]
+    mx = args.cache_format == "mxfp4"
     line = {
         "metric": METRIC,
-        "value": job_rows_per_s(world, R, ms),
+        "value": h["rows_per_s"],
         "unit": "rows/s",
         "n_gpus": world,
         "steps": args.steps,
-        "warmup": max(3, args.warmup),
-        "ms_per_step": ms,
+        "warmup": h["warmup"],
+        "ms_per_step": h["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f16/bf16" if mx else "f16",
         "data": "synthetic",
-        "config": dict(workload_config(s, keys, args.cache_format), write_path=write_path),
-        "achieved_gbs_step": world * step_bytes / (ms * 1e-3) / 1e9,
-        "algorithmic_bytes_per_step": step_bytes,
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak,
-                     "traffic": ncu_traffic(s.name + ("-mxfp4" if mx else ""),
-                                            "score_kernel" if fused else "score_decode_kernel"),
-                     "kernel": ("score_kernel<8> + topk (m3s_verify_score_topk)" if fused
-                                else "score_decode_kernel (m3s_index_block_scores)"),
-                     "kernel_ms": score_ms, "bytes_per_launch": score_bytes,
-                     "flops_per_launch": score_flops,
-                     "hbm_gbs_achieved": score_bytes / (score_ms * 1e-3) / 1e9,
-                     "peak_source": (f"measured (MEASURED_PEAKS.json {peak_name})"
-                                     if src == "measured" else "fallback")},
-        "e2e": {"value": job_rows_per_s(world, R, e2e_ms), "unit": "rows/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "copies": ("pinned host <-> device, nodes of the step's graph" if e2e_graph is not None
-                           else "pinned host <-> device, stream copies around the step graph")},
-        "gpu_launches": launches_per_step * args.steps,
-        "step_graph": "one graph per step" if whole is not None else "one graph per phase",
-        "ms_per_step_scorer_timed": (sum(ms_ev) / len(ms_ev)) if ms_ev else None,
-        "phases_ms_separate_graphs": {fn.__name__: round(v, 5) for fn, v in zip(phases, phase_ms)},
-        "clocks": clk,
+        "config": h["config"],
+        "achieved_gbs_step": h["achieved_gbs_step"],
+        "algorithmic_bytes_per_step": h["algorithmic_bytes_per_step"],
+        "roofline": h["scorer"],
+        "attention_roofline": h["attention"],
+        "e2e": h["e2e"],
+        "e2e_eager": h["e2e_eager"],
+        "gpu_launches": h["gpu_launches"],
+        "step_graph": h["step_graph"],
+        "phases_ms_separate_graphs": h["phases_ms_separate_graphs"],
+        "clocks": h["clocks"],
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, fmt=args.cache_format)
+        procs = host_cores()
+        for n in names:
+            res[n]["cpu_baseline"] = cpu_baseline(n, fmt=args.cache_format)
+            res[n]["cpu_baseline_multicore"] = cpu_baseline(n, reps=1, fmt=args.cache_format,
+                                                            procs=procs)
+        line["cpu_baseline"] = res[args.workload]["cpu_baseline"]
+        line["cpu_baseline_multicore"] = res[args.workload]["cpu_baseline_multicore"]
+    if len(names) > 1:
+        keep = ("config", "rows", "ms_per_step", "rows_per_s", "achieved_gbs_step",
+                "algorithmic_bytes_per_step", "scorer", "attention", "e2e", "e2e_eager",
+                "phases_ms_separate_graphs", "clocks", "cpu_baseline", "cpu_baseline_multicore")
+        line["per_workload"] = {n: {k: res[n][k] for k in keep if k in res[n]}
+                                for n in names if n != args.workload}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

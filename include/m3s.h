@@ -30,6 +30,16 @@
  *    of a call is enqueued on it, in order.
  *  - Alignment: plane, tensor and workspace pointers must be 16-byte aligned;
  *    the BF16 row stride of the store must be a multiple of 8 elements.
+ *  - Queries (q, q_idx) may hold any finite BF16 value. The tensor-core
+ *    products take f16 operands, so each (row, head) of the queries is scaled
+ *    by a power of two 2^-e before its conversion (e = the exponent of the
+ *    head's largest magnitude minus 15, so it lands in [2^15, 2^16)) and the
+ *    scale is undone exactly in fp32: scores as 2^e_ref times a sum whose
+ *    weights carry 2^(e_h - e_ref) (e_ref the row's largest e_h), attention
+ *    logits through a per-head logit scale. Elements below 2^-29 of their
+ *    head's largest round as f16 subnormals (below 2^-40 they vanish); a weight
+ *    whose w_h 2^(e_h - e_ref) falls below fp32's normal range rounds. Results
+ *    beyond fp32's range (a block score or logit above ~3.4e38) overflow.
  */
 #ifndef M3S_H_
 #define M3S_H_
@@ -53,7 +63,7 @@ extern "C" {
 #define M3S_DEVERR_BLOCK_ID 2 /* attention: a top-k id >= the row's block count or the table width */
 #define M3S_DEVERR_PAGE 4     /* a block-table entry outside [0, num_pages) (block skipped) */
 #define M3S_DEVERR_ROW 8      /* a row's request outside [0, B) or its length beyond the table */
-#define M3S_DEVERR_QRANGE 16  /* a query element beyond +-65504 (the fp16 operand range) */
+#define M3S_DEVERR_QRANGE 16  /* a query element that is inf or NaN */
 #define M3S_DEVERR_TIMEOUT 32 /* a bounded wait for an asynchronous copy gave up (kernel returned) */
 
 /* ---- limits of this build ---- */
@@ -274,13 +284,14 @@ int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* 
  * engine plugin whose device memory is budgeted once at start-up.
  * The block-score scratch is a file-scope device array of
  * M3S_STATIC_SCRATCH_BYTES (4 MiB), one per device; the call allocates
- * nothing. R * max(bt_stride, 1) * 4 bytes above that size returns
- * M3S_ERR_WORKSPACE before any launch. The first call on a device looks the
- * array up (cudaGetSymbolAddress, which also loads the library's device
- * module) and should come before any stream capture; later calls reuse the
- * cached address. Nothing in the scratch needs to start at zero. Every call
- * on a device shares the one scratch: calls that overlap on the GPU (e.g. on
- * two unordered streams) race and may return wrong ids.
+ * nothing. Limits, checked before any launch: R above 8192 returns
+ * M3S_ERR_UNSUPPORTED (as for m3s_index_score_topk); R * max(bt_stride, 1) * 4
+ * bytes above the scratch size returns M3S_ERR_WORKSPACE. Every call looks the
+ * array's address up in the current context (cudaGetSymbolAddress); the first
+ * call on a device also loads the library's device module and should come
+ * before any stream capture. Nothing in the scratch needs to start at zero.
+ * Every call on a device shares the one scratch: calls that overlap on the GPU
+ * (e.g. on two unordered streams) race and may return wrong ids.
  */
 #define M3S_STATIC_SCRATCH_BYTES (4u << 20)
 int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t Hi,
@@ -329,8 +340,9 @@ int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
  * their block once per occurrence.
  * k and v share one format (NVFP4 or MXFP4; mixed formats return
  * M3S_ERR_UNSUPPORTED, as the pages' startup refuses mixing them: #2744,
- * Follow-up: MXFP4 caches). The products are fp16 x fp16 (q is converted, see
- * M3S_DEVERR_QRANGE): NVFP4 K/V dequantise exactly to fp16; MXFP4 K is scaled
+ * Follow-up: MXFP4 caches). The products are fp16 x fp16 (q is scaled per head
+ * into f16's range, see the conventions above): NVFP4 K/V dequantise exactly
+ * to fp16; MXFP4 K is scaled
  * per token by its largest exponent and V per 32-dim group by the largest
  * exponent of the row's selected tokens so far, the factors re-applied in
  * fp32, which is exact while the exponents so normalised span at most 23.

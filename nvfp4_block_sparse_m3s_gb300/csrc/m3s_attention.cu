@@ -184,16 +184,37 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     }
     if (lane == 0) sm.nblocks = n;
   }
+  // Heads g and g + 8 are scaled by 2^-e before their f16 conversion (e from
+  // the head's largest magnitude, over the four lanes t that hold its 128 dims)
+  // and their logits by sm_scale log2(e) 2^e, which undoes it.
   uint32_t qa[8][4];
-  bool qbad = false;
+  float lsc0, lsc1;   // per-head logit scales (log2 units)
+  {
+    unsigned m0 = 0u, m1 = 0u;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    qa[j][0] = bf16x2_to_f16x2(qr[j][0].x, qbad);
-    qa[j][1] = bf16x2_to_f16x2(qr[j][1].x, qbad);
-    qa[j][2] = bf16x2_to_f16x2(qr[j][0].y, qbad);
-    qa[j][3] = bf16x2_to_f16x2(qr[j][1].y, qbad);
+    for (int j = 0; j < 8; ++j) {
+      m0 = max(m0, max(bf16x2_absmax_bits(qr[j][0].x), bf16x2_absmax_bits(qr[j][0].y)));
+      m1 = max(m1, max(bf16x2_absmax_bits(qr[j][1].x), bf16x2_absmax_bits(qr[j][1].y)));
+    }
+#pragma unroll
+    for (int o = 1; o < 4; o <<= 1) {
+      m0 = max(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = max(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
+    if ((m0 >= kBf16InfBits || m1 >= kBf16InfBits) && t == 0) raise(a.err, M3S_DEVERR_QRANGE);
+    const int e0 = m0 ? q_scale_exp(min(m0, kBf16InfBits - 1)) : 0;
+    const int e1 = m1 ? q_scale_exp(min(m1, kBf16InfBits - 1)) : 0;
+    const QScale sc0 = q_scale(e0), sc1 = q_scale(e1);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      qa[j][0] = bf16x2_to_f16x2_scaled(qr[j][0].x, sc0);
+      qa[j][1] = bf16x2_to_f16x2_scaled(qr[j][1].x, sc1);
+      qa[j][2] = bf16x2_to_f16x2_scaled(qr[j][0].y, sc0);
+      qa[j][3] = bf16x2_to_f16x2_scaled(qr[j][1].y, sc1);
+    }
+    lsc0 = a.scale_log2 * exp2i_f32(e0);
+    lsc1 = a.scale_log2 * exp2i_f32(e1);
   }
-  if (qbad) raise(a.err, M3S_DEVERR_QRANGE);
   __syncthreads();
   const int nblocks = sm.nblocks;
 
@@ -274,8 +295,8 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const bool live = tk + e < ntok;
-          sacc[c][e] = live ? sacc[c][e] * a.scale_log2 : -INFINITY;
-          sacc[c][2 + e] = live ? sacc[c][2 + e] * a.scale_log2 : -INFINITY;
+          sacc[c][e] = live ? sacc[c][e] * lsc0 : -INFINITY;
+          sacc[c][2 + e] = live ? sacc[c][2 + e] * lsc1 : -INFINITY;
           mx0 = fmaxf(mx0, sacc[c][e]);
           mx1 = fmaxf(mx1, sacc[c][2 + e]);
         }

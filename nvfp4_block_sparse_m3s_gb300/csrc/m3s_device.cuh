@@ -173,14 +173,62 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
 }
 
-// BF16 pair (low element in the low half) -> f16x2, with a range flag.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t two, bool& out_of_range) {
-  const float a = __uint_as_float(two << 16);
-  const float b = __uint_as_float(two & 0xFFFF0000u);
-  out_of_range |= !(fabsf(a) <= 65504.f) || !(fabsf(b) <= 65504.f);
+// ---- queries: BF16 -> f16 under a per-(row, head) power-of-two scale -------
+//
+// BF16 spans 2^-133 .. 2^128, f16 only 2^-24 .. 65504. A query head (128
+// elements) is therefore multiplied by 2^-e before its conversion, with e
+// chosen from the head's largest magnitude so that it lands in [2^15, 2^16):
+// every element within 2^-29 of the largest converts exactly (an f16 normal
+// holds BF16's 8 significant bits), smaller ones round as f16 subnormals or
+// vanish (below 2^-40 of the largest). The readers undo the scale exactly in
+// fp32: d_true = 2^e * d_scaled (ReLU and softmax logits commute with it).
+
+// The largest magnitude of a BF16 pair, as 15-bit magnitude bits (which order
+// like the values).
+__device__ __forceinline__ uint32_t bf16x2_absmax_bits(uint32_t two) {
+  return max(two & 0x7FFFu, (two >> 16) & 0x7FFFu);
+}
+
+// A head with no nonzero element has no scale exponent.
+constexpr int kQNoExp = -100000;
+
+// Scale exponent e of a head whose largest magnitude has bits m (0 < m <
+// 0x7F80): the exponent of m's leading bit, minus 15.
+__device__ __forceinline__ int q_scale_exp(uint32_t m) {
+  const int E = static_cast<int>(m >> 7);
+  const int lead = E > 0 ? E - 127 : (31 - __clz(static_cast<int>(m))) - 133;  // subnormal: mantissa's leading bit
+  return lead - 15;
+}
+
+// 2^k as fp32 for any k (a subnormal below -126, 0 below -149, +inf above 127).
+__device__ __forceinline__ float exp2i_f32(int k) {
+  if (k > 127) return __uint_as_float(0x7F800000u);
+  if (k >= -126) return __uint_as_float(static_cast<uint32_t>(k + 127) << 23);
+  return k >= -149 ? __uint_as_float(1u << (k + 149)) : 0.f;
+}
+
+// The two factors whose product is 2^-e (each an exact fp32 power of two; the
+// second is 1 unless -e > 127).
+struct QScale {
+  float s1, s2;
+};
+__device__ __forceinline__ QScale q_scale(int e) {
+  const int k = -e, k1 = min(k, 127);
+  return QScale{exp2i_f32(k1), exp2i_f32(k - k1)};
+}
+
+// BF16 pair (low element in the low half) * 2^-e -> f16x2. The two products are
+// exact (powers of two, no overflow: the head's largest element lands below
+// 2^16); the conversion is exact for f16 normals.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t two, QScale s) {
+  const float a = (__uint_as_float(two << 16) * s.s1) * s.s2;
+  const float b = (__uint_as_float(two & 0xFFFF0000u) * s.s1) * s.s2;
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
+
+// Magnitude bits at or above this are inf or NaN (reported, never scaled).
+constexpr uint32_t kBf16InfBits = 0x7F80u;
 
 // f32 -> BF16 bits, round to nearest even (finite inputs; NaN kept quiet).
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {

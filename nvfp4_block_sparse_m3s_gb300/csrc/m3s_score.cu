@@ -27,7 +27,6 @@
 // A slots and accumulators from one role to the next, so no role waits on a
 // round trip of another.
 #include <cstring>
-#include <mutex>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -115,7 +114,9 @@ struct __align__(1024) ScoreSmem {
   uint64_t afull[Cfg<QT>::kNA], aempty[Cfg<QT>::kNA];
   uint64_t dfull[Cfg<QT>::kND], dempty[Cfg<QT>::kND];
   uint32_t blkmax[Cfg<QT>::kND][4][QT];  // order-preserving bits of per-warp maxima
-  float wsm[QT * 16];
+  float wsm[QT * 16];                    // weights times 2^(e_h - e_ref) of their row
+  int qexp[Cfg<QT>::kN];                 // per (row, head): the query scale exponent e_h
+  float rowscale[QT];                    // per row: 2^e_ref, applied to its block maxima
   int lensm[QT];
   uint32_t tmem_base;
   int qbad;
@@ -212,29 +213,50 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
     const TileInfo<QT> ti = tile_info<QT>(a, tile, false);
     const int32_t* bt_row = a.block_table + static_cast<size_t>(ti.req) * a.bt_stride;
 
-    // ---- stage the tile's queries (the B operand), weights and lengths ----
+    // ---- stage the tile's queries (the B operand), weights and lengths. Each
+    // (row, head) is scaled by 2^-e_h before its f16 conversion (its largest
+    // magnitude from the 16 lanes of a half-warp, which hold its 16 chunks: both
+    // loop bounds are multiples of 32, so whole warps iterate together) ----
     for (int e = tid; e < C::kN * 16; e += C::kThreads) {
       const int n = e >> 4, kc = e & 15;
       const int rho = n >> 4, h = n & 15;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (rho < ti.nrows && h < a.Hi) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(
+      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+      if (rho < ti.nrows && h < a.Hi)
+        raw = *reinterpret_cast<const uint4*>(
             a.q_idx + (static_cast<size_t>(ti.row0 + rho) * a.Hi + h) * kHeadDim + 8 * kc);
-        bool bad = false;
-        v.x = bf16x2_to_f16x2(raw.x, bad);
-        v.y = bf16x2_to_f16x2(raw.y, bad);
-        v.z = bf16x2_to_f16x2(raw.z, bad);
-        v.w = bf16x2_to_f16x2(raw.w, bad);
-        if (bad) sm.qbad = 1;
+      unsigned m = max(max(bf16x2_absmax_bits(raw.x), bf16x2_absmax_bits(raw.y)),
+                       max(bf16x2_absmax_bits(raw.z), bf16x2_absmax_bits(raw.w)));
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (m >= kBf16InfBits) sm.qbad = 1;
+      const int eh = m ? q_scale_exp(min(m, kBf16InfBits - 1)) : kQNoExp;
+      if (m) {
+        const QScale sc = q_scale(eh);
+        v.x = bf16x2_to_f16x2_scaled(raw.x, sc);
+        v.y = bf16x2_to_f16x2_scaled(raw.y, sc);
+        v.z = bf16x2_to_f16x2_scaled(raw.z, sc);
+        v.w = bf16x2_to_f16x2_scaled(raw.w, sc);
       }
       *reinterpret_cast<uint4*>(sm.bq + bq_offset<QT>(n, kc)) = v;
-    }
-    for (int e = tid; e < QT * 16; e += C::kThreads) {
-      const int rho = e >> 4, h = e & 15;
-      sm.wsm[e] = (rho < ti.nrows && h < a.Hi) ? a.w[static_cast<size_t>(ti.row0 + rho) * a.Hi + h] : 0.f;
+      if (kc == 0) sm.qexp[n] = eh;
     }
     if (tid < QT) sm.lensm[tid] = tid < ti.nrows ? a.row_len[ti.row0 + tid] : 0;
     fence_proxy_async();  // the queries are read by the tensor core (async proxy)
+    __syncthreads();
+    // score = 2^e_ref * sum_h (w_h 2^(e_h - e_ref)) ReLU(scaled dot product), per
+    // row e_ref = the largest e_h over its contributing heads (the row's 16 heads
+    // are a half-warp; QT * 16 is a multiple of 32)
+    for (int e = tid; e < QT * 16; e += C::kThreads) {
+      const int rho = e >> 4, h = e & 15;
+      const float wv = (rho < ti.nrows && h < a.Hi) ? a.w[static_cast<size_t>(ti.row0 + rho) * a.Hi + h] : 0.f;
+      const int eh = wv != 0.f ? sm.qexp[e] : kQNoExp;
+      int eref = eh;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) eref = max(eref, __shfl_xor_sync(0xffffffffu, eref, o));
+      sm.wsm[e] = eh == kQNoExp ? 0.f : wv * exp2i_f32(max(eh - eref, -150));
+      if (h == 0) sm.rowscale[rho] = eref == kQNoExp ? 1.f : exp2i_f32(eref);
+    }
     __syncthreads();
 
     if (warp == 0) {
@@ -299,6 +321,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       int rlen[QT];
 #pragma unroll
       for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
+      const float rscale = sm.rowscale[etid < QT ? etid : 0];   // this thread's row's 2^e_ref
       PageWindow pw;
       for (int j = ((ep - g0) % C::kNEpi + C::kNEpi) % C::kNEpi; j < nseg; j += C::kNEpi) {
         const int g = g0 + j, ds = g % C::kND, ud = g / C::kND;
@@ -373,7 +396,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
               uint32_t mk = 0;
 #pragma unroll
               for (int q = 0; q < 4; ++q) mk = max(mk, sm.blkmax[ds][q][rho]);
-              m = from_ordered_bits(mk);
+              m = from_ordered_bits(mk) * rscale;
             }
             a.bscores[static_cast<size_t>(ti.row0 + rho) * a.bs_stride + blk] = m;
           }
@@ -799,10 +822,11 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
 // it cannot size a workspace per call. Those callers get a scratch whose
 // size is fixed when the library is built.
 //
-// The host side looks the array's address up once per device
-// (cudaGetSymbolAddress); that first call per device also loads the module
-// that holds the array, so it should come before any stream capture. Later
-// calls only read the cached address. Nothing in the scratch has to start at
+// The host side looks the array's address up on every call
+// (cudaGetSymbolAddress, with the caller's device current), so the address is
+// always the one of the current context, also after a cudaDeviceReset. The
+// first call on a device also loads the module that holds the array, so it
+// should come before any stream capture. Nothing in the scratch has to start at
 // zero: the scorer writes every block score that the top-k reads (each block
 // below the row's block count, -inf for a skipped page). All calls share one
 // scratch per device, so two calls that overlap on the GPU (different
@@ -816,22 +840,16 @@ static_assert(M3S_STATIC_SCRATCH_BYTES % 256 == 0, "static scratch size");
 
 static __device__ __align__(256) float g_static_block_scores[kStaticScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mutex;
-float* g_static_addr[kMaxDevices] = {};
-
-// The array's address on the current device, looked up on the first call for
-// that device. Returns nullptr when the lookup fails.
+// The array's address in the current context (nullptr when the lookup fails).
+// Not cached: a cached address would dangle after cudaDeviceReset or under
+// another context of the same device.
 float* static_scratch() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_static_mutex);
-  if (!g_static_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_block_scores) != cudaSuccess) return nullptr;
-    g_static_addr[dev] = static_cast<float*>(p);
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_block_scores) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_static_addr[dev];
+  return static_cast<float*>(p);
 }
 
 }  // namespace

@@ -60,7 +60,9 @@ struct __align__(16) DecodeSmem {
   uint8_t stage[kWarps][kStages][kStageBytes];
   uint64_t bar[kWarps][kStages];
   uint2 qfrag[kQFragWords];
-  float w[16];
+  float w[16];           // the row's weights times 2^(e_h - e_ref)
+  unsigned qmax[2][16];  // per head: the largest query magnitude's BF16 bits (by segment parity)
+  float escale;          // 2^e_ref: the row's block maxima are scaled back by it
   int len;
   int qbad;
 };
@@ -99,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
 
   if (tid < kWarps * kStages) mbar_init(&sm.bar[tid / kStages][tid % kStages], 1);
   if (tid == 0) sm.qbad = 0;
+  if (tid < 32) (&sm.qmax[0][0])[tid] = 0u;
   mbar_fence_init();
   __syncthreads();
   pdl_trigger();
@@ -115,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
   bool aborted = false;
 
   int pos = lo;
+  int par = 0;   // parity of this CTA's segment count (selects the qmax buffer)
   while (pos < hi) {
     while (pre[tile + 1] <= pos) ++tile;
     const int seg_lo = pos - pre[tile];
@@ -125,12 +129,15 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     // the loads go out first, so their round trip overlaps the block-table
     // fetch of the first copies below ----
     uint2 qraw = make_uint2(0u, 0u);
+    int hq = -1;   // the head of this thread's query word (-1: none)
     {
       const int ln = tid & 31, c = (tid >> 5) & 1, j = tid >> 6;
       const int h = 8 * c + (ln >> 2), tt = ln & 3;
-      if (ti.nrows && h < a.Hi)
+      if (ti.nrows && h < a.Hi) {
         qraw = *reinterpret_cast<const uint2*>(
             a.q_idx + (static_cast<size_t>(ti.row0) * a.Hi + h) * kHeadDim + 32 * tt + 4 * j);
+        hq = h;
+      }
     }
     const float wrow = (tid < 16 && ti.nrows && tid < a.Hi) ? a.w[static_cast<size_t>(ti.row0) * a.Hi + tid] : 0.f;
     const int lrow = (tid == 0 && ti.nrows) ? a.row_len[ti.row0] : 0;
@@ -192,22 +199,45 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     if (nhalf > 0) issue(0);
     if (nhalf > 1) issue(1);
 
-    // ---- the queries to fp16 in fragment order (the previous segment's
-    // readers are past the first barrier) ----
+    // ---- the queries to fp16 in fragment order, each head scaled by 2^-e_h
+    // (its largest magnitude taken over the CTA with shared-memory atomics);
+    // the previous segment's readers are past the first barrier ----
+    if (hq >= 0) {
+      const unsigned m = max(bf16x2_absmax_bits(qraw.x), bf16x2_absmax_bits(qraw.y));
+      if (m) atomicMax(&sm.qmax[par][hq], m);
+    }
     __syncthreads();
+    if (tid < 16) sm.qmax[par ^ 1][tid] = 0u;   // the next segment's (its last readers are done)
     {
-      bool bad = false;
-      uint2 v;
-      v.x = bf16x2_to_f16x2(qraw.x, bad);
-      v.y = bf16x2_to_f16x2(qraw.y, bad);
-      if (bad) sm.qbad = 1;
+      uint2 v = make_uint2(0u, 0u);
+      if (hq >= 0) {
+        const unsigned m = sm.qmax[par][hq];
+        if (m >= kBf16InfBits) sm.qbad = 1;
+        if (m) {
+          const QScale sc = q_scale(q_scale_exp(min(m, kBf16InfBits - 1)));
+          v.x = bf16x2_to_f16x2_scaled(qraw.x, sc);
+          v.y = bf16x2_to_f16x2_scaled(qraw.y, sc);
+        }
+      }
       sm.qfrag[tid] = v;
     }
-    if (tid < 16) sm.w[tid] = wrow;
+    if (warp == 0) {
+      // score = 2^e_ref * sum_h (w_h 2^(e_h - e_ref)) ReLU(scaled dot product),
+      // e_ref the largest e_h over the heads that contribute
+      int eh = kQNoExp;
+      if (lane < 16 && ti.nrows && lane < a.Hi) {
+        const unsigned m = sm.qmax[par][lane];
+        if (m && wrow != 0.f) eh = q_scale_exp(min(m, kBf16InfBits - 1));
+      }
+      const int eref = __reduce_max_sync(0xffffffffu, eh);
+      if (lane < 16) sm.w[lane] = eh == kQNoExp ? 0.f : wrow * exp2i_f32(max(eh - eref, -150));
+      if (lane == 0) sm.escale = eref == kQNoExp ? 1.f : exp2i_f32(eref);
+    }
     if (tid == 0) sm.len = lrow;
     __syncthreads();
 
     const float w0 = sm.w[2 * t], w1 = sm.w[2 * t + 1], w2 = sm.w[8 + 2 * t], w3 = sm.w[9 + 2 * t];
+    const float escale = sm.escale;
     const int rlen = sm.len;
     uint32_t qa[8][2][2];
 #pragma unroll
@@ -330,13 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
         if (lane == 0 && ti.nrows && blk * kPage < rlen)
-          a.bscores[static_cast<size_t>(ti.row0) * a.bs_stride + blk] = m;
+          a.bscores[static_cast<size_t>(ti.row0) * a.bs_stride + blk] = m * escale;
       }
       __syncwarp();
       if (hh + 2 < nhalf) issue(hh + 2);
     }
     pos = pre[tile] + seg_hi;
     ++tile;
+    par ^= 1;
   }
   __syncthreads();
   if (tid == 0 && sm.qbad) raise(a.err, M3S_DEVERR_QRANGE);

@@ -544,6 +544,33 @@ def norm_rope_rows(bits: np.ndarray, weight, cos, sin, rotary_dim: int, eps: flo
     return f32_to_bf16_bits(y)
 
 
+def norm_rope_rows_f64(bits: np.ndarray, weight, cos, sin, rotary_dim: int, eps: float) -> np.ndarray:
+    """The normalised, rotated rows [T, H, 128] of BF16 rows ``bits`` in float64,
+    unrounded: the definition itself, with no float32 step and no order of
+    summation (the sum of squares is math.fsum's, exact then rounded once).
+
+      - RMSNorm (``weight`` [128] given): y = x / sqrt(mean(x^2) + eps) * weight;
+      - RoPE (``cos``/``sin`` [T, rotary_dim / 2] given), rotate-half on the first
+        rotary_dim dims: o_i = y_i c - y_j s, o_j = y_j c + y_i s (j = i + rd/2).
+    """
+    x = bf16_to_f64(bits)
+    T, H, D = x.shape
+    assert D == HEAD_DIM
+    if weight is not None:
+        ss = np.array([[math.fsum(v * v for v in x[t, h]) for h in range(H)] for t in range(T)])
+        y = x / np.sqrt(ss / HEAD_DIM + float(eps))[..., None] * np.asarray(weight, np.float64)
+    else:
+        y = x.copy()
+    if cos is not None:
+        h = rotary_dim // 2
+        c = np.asarray(cos, np.float64)[:, None, :h]
+        s = np.asarray(sin, np.float64)[:, None, :h]
+        y1, y2 = y[..., :h].copy(), y[..., h:rotary_dim].copy()
+        y[..., :h] = y1 * c - y2 * s
+        y[..., h:rotary_dim] = y2 * c + y1 * s
+    return y
+
+
 def qk_norm_rope_store(jobs, slot_mapping, cos, sin, rotary_dim: int, eps: float) -> int:
     """The fused write: each job is (src bits [T, H, 128], weight [128] or None,
     rope: bool, destination), the destination either a (codes, scales) plane

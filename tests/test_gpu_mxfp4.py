@@ -131,8 +131,9 @@ def test_mx_step_small_vs_oracle(lib, case):
 def test_mx_extreme_scales_stay_exact(lib):
     """Keys whose four groups span a wide exponent range, K near the smallest E8M0
     exponents and V near the largest, V growing 2^4 per block (the running V
-    reference rises block by block): the scorer and the attention, both exact
-    while the exponents they normalise against span <= 23, match the oracle."""
+    reference rises block by block), index queries at 2^-100 and attention
+    queries at 2^110: the scorer and the attention, both exact while the
+    exponents they normalise against span <= 23, match the oracle."""
     rng = np.random.default_rng(17)
     L, hi, hq = 700, 16, 16
     nb = (L + 127) // 128
@@ -148,9 +149,10 @@ def test_mx_extreme_scales_stay_exact(lib):
     kv = W.f32_to_bf16_bits((rng.standard_normal((L, 1, 128)) * 2.0 ** -120).astype(np.float32))
     vgrow = 2.0 ** (100 + 4 * (np.arange(L) // 128))[:, None, None]
     vv = W.f32_to_bf16_bits((rng.standard_normal((L, 1, 128)) * vgrow).astype(np.float32))
-    q_idx = W.f32_to_bf16_bits(rng.standard_normal((1, hi, 128)).astype(np.float32))
+    # queries at both ends of the BF16 range (the kernels scale each head into f16's)
+    q_idx = W.f32_to_bf16_bits(rng.standard_normal((1, hi, 128)).astype(np.float32) * np.float32(2.0 ** -100))
     w = rng.random((1, hi)).astype(np.float32)
-    q = W.f32_to_bf16_bits(rng.standard_normal((1, hq, 128)).astype(np.float32))
+    q = W.f32_to_bf16_bits(rng.standard_normal((1, hq, 128)).astype(np.float32) * np.float32(2.0 ** 110))
     bt = np.zeros((1, nb), dtype=np.int32)
     bt[0] = rng.permutation(P)[:nb]
     slots = (bt[0][np.arange(L) // 128].astype(np.int64) * 128 + np.arange(L) % 128)

@@ -103,3 +103,42 @@ def test_quantise_at_write_bad_slot_reported(lib):
     keep = slots < P * 128
     O.nvfp4_store(src[keep], slots[keep], rc, rs)
     assert np.array_equal(c.cpu().numpy(), rc) and np.array_equal(s.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_fused_planes_checked_without_the_kernels_reduction_order(lib, fmt):
+    """The check of the fused write that does not lean on the oracle restating the
+    kernel's float32 steps: (1) the same call in its BF16-rows mode gives the rows
+    the kernel quantises, and the oracle's own store of those rows equals the fused
+    planes bit for bit; (2) those rows lie within BF16 rounding (plus a float32
+    allowance) of the unrounded fp64 RMSNorm and rotation, and almost all of them
+    are exactly the fp64 value rounded to BF16."""
+    mx = fmt == "mxfp4"
+    T, P, rd, eps = 300, 4, 64, 1e-6
+    ref, dev, (src, wts, cos, sin, slots, _) = _case(71, T, P, rd, mx, mx)
+    cos_d, sin_d = torch.from_numpy(cos).cuda(), torch.from_numpy(sin).cuda()
+    for n, w, rope in (("k", wts["k"], True), ("v", None, False), ("ik", wts["ik"], True)):
+        H = src[n].shape[1]
+        rows = torch.zeros((T, H, 128), dtype=torch.bfloat16, device="cuda")
+        M.m3s_qk_norm_rope_store([(bf16_dev(src[n]), None if w is None else torch.from_numpy(w).cuda(),
+                                   rope, rows)], None, cos_d, sin_d, rd, eps)
+        torch.cuda.synchronize()
+        gpu_rows = rows.view(torch.int16).cpu().numpy().view(np.uint16)
+        c, sc = O.new_planes(P, H, mx=mx)
+        assert O.nvfp4_store(gpu_rows, slots, c, sc) == 0
+        assert np.array_equal(dev[n][0].cpu().numpy(), c), n
+        assert np.array_equal(dev[n][1].cpu().numpy(), sc), n
+        exact = O.norm_rope_rows_f64(src[n], w, cos if rope else None, sin if rope else None, rd, eps)
+        # float32 allowance: relative to the terms each output is made of
+        y = O.norm_rope_rows_f64(src[n], w, None, None, rd, eps)
+        mag = np.abs(y).copy()
+        if rope:
+            h = rd // 2
+            c32, s32 = np.abs(cos[:, None, :h].astype(np.float64)), np.abs(sin[:, None, :h].astype(np.float64))
+            mag[..., :h] = np.abs(y[..., :h]) * c32 + np.abs(y[..., h:rd]) * s32
+            mag[..., h:rd] = np.abs(y[..., h:rd]) * c32 + np.abs(y[..., :h]) * s32
+        got = O.bf16_to_f64(gpu_rows)
+        assert np.all(np.abs(got - exact) <= 2.0 ** -8 * np.abs(exact) + 2.0 ** -16 * mag), n
+        nearest = O.f32_to_bf16_bits(exact.astype(np.float32))
+        same = float(np.mean(nearest == gpu_rows))
+        assert same >= 0.99, (n, same)

@@ -662,6 +662,27 @@ def test_norm_rope_against_torch_rms_norm_and_complex_rotation():
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6)
 
 
+def test_norm_rope_f64_against_torch_rms_norm_and_complex_rotation():
+    """The unrounded float64 rows equal torch's rms_norm (fp64) followed by the
+    rotation written as a complex product, to fp64 rounding; with neither step
+    the rows come back exactly."""
+    rng = np.random.default_rng(16)
+    T, H, r = 5, 2, 48
+    x = W.f32_to_bf16_bits((rng.standard_normal((T, H, 128)) * 2.0 ** rng.integers(-30, 30, (T, H, 1)))
+                           .astype(np.float32))
+    w = (rng.random(128) + 0.5).astype(np.float32)
+    cos, sin = _rope_tables(T, r // 2)
+    got = O.norm_rope_rows_f64(x, w, cos, sin, r, 1e-6)
+    xt = torch.from_numpy(O.bf16_to_f64(x))
+    nt = torch.nn.functional.rms_norm(xt, (128,), torch.from_numpy(w.astype(np.float64)), eps=1e-6)
+    rot = torch.complex(nt[..., : r // 2], nt[..., r // 2: r]) * torch.complex(
+        torch.from_numpy(cos.astype(np.float64))[:, None, :], torch.from_numpy(sin.astype(np.float64))[:, None, :])
+    ref = torch.cat([rot.real, rot.imag, nt[..., r:]], -1).numpy()
+    mag = np.abs(nt.numpy()).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(got - ref) <= 1e-13 * mag)
+    assert np.array_equal(O.norm_rope_rows_f64(x, None, None, None, 0, 1e-6), O.bf16_to_f64(x))
+
+
 def test_norm_rope_special_cases():
     """No norm and no rotation give the rows back bit for bit; angle 0 is the
     identity; a zero row stays zero; a constant row of c with unit weights
