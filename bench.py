@@ -140,7 +140,7 @@ def job_rows_per_s(world: int, rows_per_rank: int, ms: float) -> float:
 
 
 #: kernels each way of running score + top-k launches per call
-SCORE_CALL_LAUNCHES = {"verify": 2, "index": 2, "pair": 2}
+SCORE_CALL_LAUNCHES = {"verify": 1, "index": 1, "pair": 2}
 
 #: bytes per token and head of a K, V or index-K record
 RECORD_BYTES = {"nvfp4": 72, "mxfp4": 68}

@@ -116,9 +116,17 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
  *   R rows, B requests, max_blocks = block-table width (bt_stride), Hq / Hkv
  *   q and KV heads, Hi index heads, topk, max_q = the largest rows-per-request
  *   the verify call will see (the cu_q differences).
- * Index / verify: R * max_blocks fp32 block scores (index: 0 when the caller
- * passes its own block_scores). Attention: 0 (its split-K partials are merged
- * on chip); its ws arguments are accepted and ignored.
+ * Index / verify (0 when topk is 0): the streaming top-k's state, sized by
+ * the tiles of query rows the call scores (index: one tile per row, ntiles = R;
+ * verify: tiles of up to 8 rows of one request, ntiles = B * ceil(max_q / 8)):
+ * one 4-byte ticket per tile (rounded up to 256 bytes), then candidate lists
+ * of topk 8-byte keys for (ntiles + 255) slots of 1 (index) or 8 (verify)
+ * rows. The workspace must read zero when it is first used (zero it once after
+ * allocating it); every call leaves it that way again, so it can be reused
+ * call after call, graph replays included. A call that raised
+ * M3S_DEVERR_TIMEOUT may leave tickets set: zero the workspace again after one.
+ * Attention: 0 (its split-K partials are merged on chip); its ws arguments
+ * are accepted and ignored.
  */
 size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int32_t Hq,
                            int32_t Hkv, int32_t Hi, int32_t topk, int32_t max_q);
@@ -244,10 +252,16 @@ int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int3
  *   idx_k.num_heads == 1, block_table int32 [B][bt_stride] (logical block ->
  *   physical page), row_req / row_len from m3s_decode_rows,
  *   topk_ids int32 [R][topk] (topk <= 64),
- *   block_scores fp32 [R][bt_stride] or NULL: when given, receives every
+ *   block_scores fp32 [R][bt_stride] or NULL: when given, also receives every
  *   row's block scores (entries past the row's block count are left as is).
  * Rows with row_req < 0 or row_len <= 0 produce -1 ids. Needs
- * ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, ...).
+ * ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, ...), zeroed before
+ * its first use (see there).
+ * One launch: the scorer keeps a running top-k per warp as it streams the
+ * keys (#2744, Fused verify top-k: a streaming top-k per chunk, then a merge),
+ * each CTA leaves its share of a row as topk candidate keys in the workspace,
+ * and the CTA that scores a row's last block merges the row's candidates into
+ * its ids; the block-score matrix is never written unless asked for.
  */
 int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                          m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
@@ -311,7 +325,10 @@ int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t H
  *   row_len int32 [R] their causal lengths (m3s_decode_rows),
  *   max_q >= every cu_q[b+1]-cu_q[b] (sizes the request-row tiling).
  * Other arguments as for m3s_index_score_topk (the index plane NVFP4 or MXFP4,
- * with the same exactness).
+ * with the same exactness). One launch, the top-k streamed and merged inside
+ * it as for m3s_index_score_topk; rows past cu_q[B] get -1 ids. Needs
+ * ws_bytes >= m3s_workspace_bytes(M3S_OP_VERIFY_SCORE_TOPK, ...), zeroed before
+ * its first use.
  */
 int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                           m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,

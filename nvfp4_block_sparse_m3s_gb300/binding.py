@@ -233,13 +233,13 @@ def m3s_index_score_topk(q_idx, w, codes, scales, block_table, row_req, row_len,
     B, bt_stride = block_table.shape
     if topk_ids is None:
         topk_ids = torch.empty((R, topk), dtype=torch.int32, device=q_idx.device)
-    if ws is None and block_scores is None:
+    if ws is None:   # zeroed once, as the call requires (each call leaves it so)
         nb = m3s_workspace_bytes(OP_INDEX_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk)
-        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
     rc = load().m3s_index_score_topk(
         _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride,
         _ptr(row_req), _ptr(row_len), R, B, topk, init_blocks, local_blocks, _ptr(topk_ids),
-        _ptr(block_scores), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        _ptr(block_scores), _ptr(ws), ws.numel() * ws.element_size(),
         _ptr(err), _stream(stream))
     _check(rc, "m3s_index_score_topk")
     return topk_ids
@@ -294,9 +294,9 @@ def m3s_verify_score_topk(q_idx, w, codes, scales, block_table, cu_q, row_len, m
     B, bt_stride = block_table.shape
     if topk_ids is None:
         topk_ids = torch.empty((R, topk), dtype=torch.int32, device=q_idx.device)
-    if ws is None:
+    if ws is None:   # zeroed once, as the call requires (each call leaves it so)
         nb = m3s_workspace_bytes(OP_VERIFY_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, max_q)
-        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
     rc = load().m3s_verify_score_topk(
         _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride, _ptr(cu_q),
         _ptr(row_len), B, R, max_q, topk, init_blocks, local_blocks, _ptr(topk_ids), _ptr(ws),

@@ -1,7 +1,7 @@
 // Host-side entry points that launch nothing: workspace sizing and version.
 #include <cuda_runtime.h>
 
-#include "../../include/m3s.h"
+#include "m3s_score_common.cuh"
 
 namespace {
 size_t round16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
@@ -9,15 +9,17 @@ size_t round16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
 
 extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int32_t Hq,
                                       int32_t Hkv, int32_t Hi, int32_t topk, int32_t max_q) {
-  (void)B;
   (void)Hi;
-  (void)max_q;
-  if (R <= 0) return 0;
+  (void)max_blocks;
+  (void)Hq;
+  (void)Hkv;
+  if (R <= 0 || topk <= 0) return 0;
   switch (op) {
-    case M3S_OP_INDEX_SCORE_TOPK:
-    case M3S_OP_VERIFY_SCORE_TOPK: {
-      const size_t stride = max_blocks > 0 ? static_cast<size_t>(max_blocks) : 1;
-      return round16(static_cast<size_t>(R) * stride * sizeof(float));
+    case M3S_OP_INDEX_SCORE_TOPK:   // one tile per row
+      return round16(m3s::topk_ws_bytes(R, 1, topk));
+    case M3S_OP_VERIFY_SCORE_TOPK: {   // tiles of up to 8 rows of one request
+      const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;
+      return round16(m3s::topk_ws_bytes(B > 0 ? B * cpr : 0, 8, topk));
     }
     case M3S_OP_SPARSE_ATTENTION:
       // split-K partials are combined inside a thread-block cluster: no workspace

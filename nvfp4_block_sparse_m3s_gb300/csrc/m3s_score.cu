@@ -26,6 +26,7 @@
 // the ReLU-weighted head sum and the block maximum. mbarriers hand stages,
 // A slots and accumulators from one role to the next, so no role waits on a
 // round trip of another.
+#include <cstddef>
 #include <cstring>
 
 #include <cuda.h>
@@ -56,21 +57,10 @@ constexpr int kStageBytes = kPageCodeBytes + kPageScaleBytes;  // one block: 921
 // segment (about 5 us, some 7 blocks, on the verify batch), so a CTA whose
 // range spans two tiles is given that many fewer blocks.
 constexpr int kTileSetUp = 7;
-
-// Block position of cost position x, where tile t spans [pre[t] + c t,
-// pre[t + 1] + c (t + 1)) in cost space: its first c units are its set-up, the
-// rest one unit per block. Monotone, so consecutive cost ranges give
-// contiguous, disjoint block ranges covering every block.
-__device__ __forceinline__ int tile_cost_to_block(const int* pre, int ntiles, long long x, int c) {
-  if (x >= pre[ntiles] + static_cast<long long>(c) * ntiles) return pre[ntiles];
-  int l = 0, h = ntiles;   // pc(l) <= x < pc(h)
-  while (h - l > 1) {
-    const int m = (l + h) >> 1;
-    if (pre[m] + static_cast<long long>(c) * m <= x) l = m; else h = m;
-  }
-  const long long o = x - (pre[l] + static_cast<long long>(c) * l);
-  return pre[l] + static_cast<int>(o > c ? o - c : 0);
-}
+// With the streaming top-k a segment's end also merges its candidates and
+// arrives on the tile's ticket (and the last CTA of a tile merges it): charged
+// as 3 more blocks.
+constexpr int kTileSetUpStreaming = 10;
 
 // Roles and resources. Warp 0: producer (bulk copies); warps 1 .. kND: MMA
 // issuers, one per accumulator slot (block g -> issuer g % kND, so one issuer's
@@ -114,7 +104,10 @@ struct __align__(1024) ScoreSmem {
   uint64_t afull[Cfg<QT>::kNA], aempty[Cfg<QT>::kNA];
   uint64_t dfull[Cfg<QT>::kND], dempty[Cfg<QT>::kND];
   uint32_t blkmax[Cfg<QT>::kND][4][QT];  // order-preserving bits of per-warp maxima
-  float wsm[QT * 16];                    // weights times 2^(e_h - e_ref) of their row
+  unsigned long long elist[Cfg<QT>::kNEpi][QT][64];   // per epilogue warpgroup and row: running top-k
+  int vslot[kMaxGrid + 32];                   // candidate slots of a tile being merged
+  int fin;
+  alignas(16) float wsm[QT * 16];        // weights times 2^(e_h - e_ref) of their row (read as float4)
   int qexp[Cfg<QT>::kN];                 // per (row, head): the query scale exponent e_h
   float rowscale[QT];                    // per row: 2^e_ref, applied to its block maxima
   int lensm[QT];
@@ -123,9 +116,12 @@ struct __align__(1024) ScoreSmem {
   int abort;
 };
 
+static_assert(offsetof(ScoreSmem<8>, wsm) % 16 == 0, "the epilogue reads the weights as float4");
+static_assert(offsetof(ScoreSmem<8>, elist) % 8 == 0 && offsetof(ScoreSmem<8>, full) % 8 == 0, "8-byte members");
+
 template <int QT>
 size_t score_smem_bytes(int ntiles) {
-  return sizeof(ScoreSmem<QT>) + (ntiles + 1) * 4 + 1024;  // + alignment slack
+  return sizeof(ScoreSmem<QT>) + TileLayout::bytes(ntiles) + 1024;  // + alignment slack
 }
 
 // B layout: core matrix (8 rows x 8 f16 = 128 B) for K-chunk kc (dims 8kc ..
@@ -161,7 +157,10 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   ScoreSmem<QT>& sm = *reinterpret_cast<ScoreSmem<QT>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  int* pre = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(ScoreSmem<QT>));
+  TileLayout L;
+  L.bind(reinterpret_cast<uint8_t*>(&sm) + sizeof(ScoreSmem<QT>), a.ntiles,
+         a.cand ? kTileSetUpStreaming : kTileSetUp);
+  const int* pre = L.pre;
   __shared__ int red[C::kWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -183,6 +182,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
   if (tid == 0) {
     sm.qbad = 0;
     sm.abort = 0;
+    sm.fin = 0;
   }
   if (warp == 0) tmem_alloc(&sm.tmem_base, C::kTmemCols);
   mbar_fence_init();
@@ -190,16 +190,19 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  pdl_trigger();
+  // with the streaming top-k the next kernel is let launch only when this CTA's
+  // blocks are scored (its waiting CTAs slowed the step when launched early)
+  if (!a.cand) pdl_trigger();
   pdl_wait();
 
   // ---- exclusive prefix of block counts over tiles, then this CTA's range ----
-  tile_prefix<QT>(a, pre, red, C::kThreads);
+  tile_prefix<QT>(a, L, red, C::kThreads);
   const int ntiles = a.ntiles;
-  const long long cost = pre[ntiles] + static_cast<long long>(kTileSetUp) * ntiles;
-  const int lo = tile_cost_to_block(pre, ntiles, cost * blockIdx.x / gridDim.x, kTileSetUp);
-  const int hi = tile_cost_to_block(pre, ntiles, cost * (blockIdx.x + 1) / gridDim.x, kTileSetUp);
+  if (a.cand) write_unscored_rows<QT>(a, L, C::kThreads);
+  const int2 range = L.cta_range(blockIdx.x);
+  const int lo = range.x, hi = range.y;
   int tile = tile_at(pre, ntiles, lo);
+  if (a.cand && lo >= hi) pdl_trigger();   // no blocks
 
   int g0 = 0;               // sequence number of the segment's first block in this CTA
   bool mma_issued = false;  // MMA thread: a commit may still be outstanding
@@ -242,6 +245,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       if (kc == 0) sm.qexp[n] = eh;
     }
     if (tid < QT) sm.lensm[tid] = tid < ti.nrows ? a.row_len[ti.row0 + tid] : 0;
+    for (int e = tid; e < C::kNEpi * QT * 64; e += C::kThreads) (&sm.elist[0][0][0])[e] = 0ull;
     fence_proxy_async();  // the queries are read by the tensor core (async proxy)
     __syncthreads();
     // score = 2^e_ref * sum_h (w_h 2^(e_h - e_ref)) ReLU(scaled dot product), per
@@ -321,7 +325,16 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       int rlen[QT];
 #pragma unroll
       for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
-      const float rscale = sm.rowscale[etid < QT ? etid : 0];   // this thread's row's 2^e_ref
+      // Streaming top-k: warp wq keeps the lists of rows 2 wq and 2 wq + 1 (lanes 0
+      // and 1 compute their block maxima). A list takes its first topk keys as
+      // they come, is sorted once full, and from then on a key enters only above
+      // the list's k-th (a warp-uniform register compare; then one warp insert).
+      static_assert(QT <= 8, "two rows a warp of the warpgroup");
+      const int my_row = 2 * wq + (lane & 1);
+      const float rscale = sm.rowscale[my_row];   // lanes 0 and 1: their row's 2^e_ref
+      const int nbr = (sm.lensm[my_row] + kPage - 1) / kPage;   // its blocks (forced-block rule)
+      int lcnt = 0;                  // lanes 0 and 1: keys their row's list holds
+      unsigned long long lkth = 0ull;  // and its k-th key once full
       PageWindow pw;
       for (int j = ((ep - g0) % C::kNEpi + C::kNEpi) % C::kNEpi; j < nseg; j += C::kNEpi) {
         const int g = g0 + j, ds = g % C::kND, ud = g / C::kND;
@@ -388,17 +401,60 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
         }
         named_bar_sync(1 + ep, 128);
         if (*reinterpret_cast<volatile int*>(&sm.abort)) break;  // uniform: read after the barrier
-        if (etid < QT) {
-          const int rho = etid;
-          if (rho < ti.nrows && blk * kPage < rlen[rho]) {
+        {
+          // lanes 0 and 1: their row's block key; mode 1 = the list just filled
+          // (sort it once), 2 = the key enters the full list (a warp insert)
+          int mode = 0;
+          unsigned long long key = 0ull;
+          if (lane < 2 && my_row < ti.nrows && blk * kPage < sm.lensm[my_row]) {
             float m = -INFINITY;
             if (page >= 0 && page < a.num_pages) {
               uint32_t mk = 0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) mk = max(mk, sm.blkmax[ds][q][rho]);
+              for (int q = 0; q < 4; ++q) mk = max(mk, sm.blkmax[ds][q][my_row]);
               m = from_ordered_bits(mk) * rscale;
             }
-            a.bscores[static_cast<size_t>(ti.row0 + rho) * a.bs_stride + blk] = m;
+            if (a.bscores) a.bscores[static_cast<size_t>(ti.row0 + my_row) * a.bs_stride + blk] = m;
+            if (a.cand) {
+              key = select_key(m, blk, nbr, a.init_blocks, a.local_blocks);
+              if (lcnt < a.topk) {   // filling: append
+                sm.elist[ep][my_row][lcnt] = key;
+                if (++lcnt == a.topk) mode = 1;
+              } else if (key > lkth) {
+                mode = 2;
+              }
+            }
+          }
+          unsigned need = __ballot_sync(0xffffffffu, mode != 0) & 3u;
+          while (need) {   // (warp-uniform; rare once the lists are full)
+            const int h = __ffs(need) - 1;
+            need &= need - 1;
+            const int md = __shfl_sync(0xffffffffu, mode, h);
+            unsigned long long* lst = &sm.elist[ep][2 * wq + h][0];
+            __syncwarp();   // lane h's append is visible
+            WarpTopk t = warp_load(lst, 64, lane);
+            if (md == 1) {
+              warp_sort_desc(t, a.topk, lane);
+            } else {
+              t.kth = __shfl_sync(0xffffffffu, lkth, h);
+              t.insert(__shfl_sync(0xffffffffu, key, h), a.topk, lane);
+            }
+            warp_store(t, lst, 64, lane);
+            const unsigned long long nk = __shfl_sync(0xffffffffu, a.topk > 32 ? t.b : t.a, (a.topk - 1) & 31);
+            if (lane == h) lkth = nk;
+          }
+        }
+      }
+      if (a.cand) {   // lists that never filled: sorted for the segment's merge
+        const unsigned part = __ballot_sync(0xffffffffu, lane < 2 && lcnt > 0 && lcnt < a.topk) & 3u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if ((part >> h) & 1u) {
+            unsigned long long* lst = &sm.elist[ep][2 * wq + h][0];
+            __syncwarp();
+            WarpTopk t = warp_load(lst, 64, lane);
+            warp_sort_desc(t, a.topk, lane);
+            warp_store(t, lst, 64, lane);
           }
         }
       }
@@ -458,6 +514,19 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       }
     }
     __syncthreads();  // every role is done with this segment (and its queries)
+    if (a.cand && pre[tile] + seg_hi >= hi) pdl_trigger();   // this CTA's blocks are scored
+    if (a.cand) {
+      // the segment's candidates: per row, the epilogue warpgroups' lists merged
+      // into slot tile + CTA; then the tile's ticket (the last CTA merges the tile)
+      if (warp < ti.nrows) {   // a warp a row: its two warpgroups' lists, one pairwise merge
+        WarpTopk x = warp_load(&sm.elist[0][warp][0], 64, lane);
+        warp_merge2(x, warp_load(&sm.elist[1][warp][0], 64, lane), a.topk, lane);
+        write_keys(x, a.topk, a.cand + (static_cast<size_t>(tile + blockIdx.x) * QT + warp) * a.topk, lane);
+      }
+      __syncthreads();
+      tile_finish<QT>(a, L, tile, nseg, reinterpret_cast<unsigned long long*>(&sm.stage[0][0]),
+                      static_cast<int>(sizeof(sm.stage) / 8), sm.vslot, &sm.fin, C::kThreads);
+    }
     g0 += nseg;
     pos = pre[tile] + seg_hi;
     ++tile;
@@ -648,9 +717,24 @@ int sm_count() {
   return n;
 }
 
+int grid_size() { return min(sm_count(), kMaxGrid); }
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The streaming top-k's workspace (sized by m3s_workspace_bytes): the tiles'
+// tickets, then the candidate lists.
+void bind_topk_workspace(ScoreArgs& a, void* ws, int ntiles, int topk, int init_blocks, int local_blocks,
+                         int32_t* ids, int qt = 1) {
+  (void)qt;
+  a.ticket = static_cast<unsigned*>(ws);
+  a.cand = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + topk_ticket_bytes(ntiles));
+  a.topk = topk;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  a.ids = ids;
+}
 
 size_t topk_smem(int bt_stride, int* keys_out) {
   const int k = bt_stride < 12288 ? bt_stride : 12288;
@@ -669,7 +753,7 @@ int launch_score(const ScoreArgs& a, cudaStream_t st) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
-  return launch_kernel(kernel, dim3(sm_count()), dim3(Cfg<QT>::kThreads), smem, st, 0, a,
+  return launch_kernel(kernel, dim3(grid_size()), dim3(Cfg<QT>::kThreads), smem, st, 0, a,
                        map) == cudaSuccess
              ? M3S_OK
              : M3S_ERR_LAUNCH;
@@ -756,24 +840,15 @@ extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32
   if (!row_req || !row_len || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
   if (R > kMaxTiles) return M3S_ERR_UNSUPPORTED;
   if (topk == 0) return M3S_OK;
+  if (ws_bytes < m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, 1))
+    return M3S_ERR_WORKSPACE;
+  if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
   const int stride = bt_stride > 0 ? bt_stride : 1;
-  float* bs = block_scores;
-  if (!bs) {
-    if (ws_bytes < m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, 1))
-      return M3S_ERR_WORKSPACE;
-    if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
-    bs = static_cast<float*>(ws);
-  }
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (B > 0) {
-    ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-                row_req, nullptr, row_len, R, B, R, 1, bs, stride, err,
-                idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
-    rc = launch_score_decode(a, st);
-    if (rc != M3S_OK) return rc;
-  }
-  return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, init_blocks, local_blocks,
-                     topk_ids, st);
+  ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
+              row_req, nullptr, row_len, R, B, R, 1, block_scores, stride, err,
+              idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
+  bind_topk_workspace(a, ws, R, topk, init_blocks, local_blocks, topk_ids);
+  return launch_score_decode(a, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
@@ -787,29 +862,18 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
   int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk_ids);
   if (rc != M3S_OK || R == 0) return rc;
   if (!cu_q || !row_len || max_q < 0 || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
-  if (topk == 0 || B == 0) {
-    if (topk > 0) {
-      // no requests: every row is padding
-      return launch_topk(nullptr, 1, nullptr, row_len, R, 0, bt_stride, topk, 0, 0, topk_ids,
-                         static_cast<cudaStream_t>(stream));
-    }
-    return M3S_OK;
-  }
+  if (topk == 0) return M3S_OK;
   const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;
-  const long long ntiles = static_cast<long long>(B) * cpr;
+  const long long ntiles = static_cast<long long>(B) * cpr;   // B == 0: every row is padding
   if (ntiles > kMaxTiles) return M3S_ERR_UNSUPPORTED;
   if (ws_bytes < m3s_workspace_bytes(M3S_OP_VERIFY_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, max_q))
     return M3S_ERR_WORKSPACE;
   if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
-  float* bs = static_cast<float*>(ws);
   ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-              nullptr, cu_q, row_len, R, B, static_cast<int>(ntiles), cpr, bs, bt_stride, err,
+              nullptr, cu_q, row_len, R, B, static_cast<int>(ntiles), cpr, nullptr, bt_stride, err,
               idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  rc = launch_score<8>(a, st);
-  if (rc != M3S_OK) return rc;
-  return launch_topk(bs, bt_stride, nullptr, row_len, R, B, bt_stride, topk, init_blocks,
-                     local_blocks, topk_ids, st);
+  bind_topk_workspace(a, ws, static_cast<int>(ntiles), topk, init_blocks, local_blocks, topk_ids, 8);
+  return launch_score<8>(a, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------

@@ -47,6 +47,7 @@ constexpr int kHalfScaleBytes = kHalfKeys * kScaleBytes;      // 512
 constexpr int kStageBytes = kHalfCodeBytes + kHalfScaleBytes; // 4608
 constexpr int kQFragWords = 8 * 2 * 32;                       // k-steps x n-tiles x lanes (uint2)
 constexpr int kSegCost = 6;                                   // set-up of a row segment, in blocks
+constexpr int kSegCostStreaming = 14;   // ... plus its candidates' merge and ticket (streaming top-k)
 static_assert(kQFragWords == kThreads, "one query fragment word per thread");
 
 // MXFP4 factors of one warp's current half: per key the fp16x2 factor of each
@@ -63,24 +64,12 @@ struct __align__(16) DecodeSmem {
   float w[16];           // the row's weights times 2^(e_h - e_ref)
   unsigned qmax[2][16];  // per head: the largest query magnitude's BF16 bits (by segment parity)
   float escale;          // 2^e_ref: the row's block maxima are scaled back by it
+  unsigned long long wlist[kWarps][64];   // the warps' top-k lists at a segment's end
+  int vslot[kMaxGrid + 32];   // candidate slots of a tile being merged
+  int fin;
   int len;
   int qbad;
 };
-
-// Block position of cost position x, where tile t spans [pre[t] + c t,
-// pre[t + 1] + c (t + 1)) in cost space: its first c units are its set-up (the
-// tile's first block), the rest one unit per block. Monotone, so consecutive
-// cost ranges give contiguous, disjoint block ranges covering every block.
-__device__ __forceinline__ int cost_to_block(const int* pre, int ntiles, long long x, int c) {
-  if (x >= pre[ntiles] + static_cast<long long>(c) * ntiles) return pre[ntiles];
-  int l = 0, h = ntiles;   // pc(l) <= x < pc(h)
-  while (h - l > 1) {
-    const int m = (l + h) >> 1;
-    if (pre[m] + static_cast<long long>(c) * m <= x) l = m; else h = m;
-  }
-  const long long o = x - (pre[l] + static_cast<long long>(c) * l);
-  return pre[l] + static_cast<int>(o > c ? o - c : 0);
-}
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -93,26 +82,38 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
   MxScratch& mxs = *reinterpret_cast<MxScratch*>(smem_raw + sizeof(DecodeSmem));   // MX only
-  int* pre = reinterpret_cast<int*>(smem_raw + sizeof(DecodeSmem) + (MX ? sizeof(MxScratch) : 0));
+  TileLayout L;
+  L.bind(smem_raw + sizeof(DecodeSmem) + (MX ? sizeof(MxScratch) : 0), a.ntiles,
+         a.cand ? kSegCostStreaming : kSegCost);
+  const int* pre = L.pre;
   __shared__ int red[kWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
 
   if (tid < kWarps * kStages) mbar_init(&sm.bar[tid / kStages][tid % kStages], 1);
-  if (tid == 0) sm.qbad = 0;
+  if (tid == 0) {
+    sm.qbad = 0;
+    sm.fin = 0;
+  }
   if (tid < 32) (&sm.qmax[0][0])[tid] = 0u;
   mbar_fence_init();
   __syncthreads();
-  pdl_trigger();
+  // The next kernel may launch once every CTA has signalled. Its CTAs then wait
+  // for this grid on SMs this grid has freed; with the streaming top-k the grid
+  // ends with a few CTAs merging candidates, so those signal only when their
+  // blocks are scored (early waiting CTAs of the next kernel were measured to
+  // slow the step down).
+  if (!a.cand) pdl_trigger();
   pdl_wait();
 
-  tile_prefix<1>(a, pre, red, kThreads);
+  tile_prefix<1>(a, L, red, kThreads);
   const int ntiles = a.ntiles;
-  const long long C = pre[ntiles] + static_cast<long long>(kSegCost) * ntiles;
-  const int lo = cost_to_block(pre, ntiles, C * blockIdx.x / gridDim.x, kSegCost);
-  const int hi = cost_to_block(pre, ntiles, C * (blockIdx.x + 1) / gridDim.x, kSegCost);
+  if (a.cand) write_unscored_rows<1>(a, L, kThreads);
+  const int2 range = L.cta_range(blockIdx.x);
+  const int lo = range.x, hi = range.y;
   int tile = tile_at(pre, ntiles, lo);
+  if (a.cand && lo >= hi) pdl_trigger();   // no blocks
 
   uint32_t phase_bits = 0;  // per-stage mbarrier parity of this warp
   bool aborted = false;
@@ -239,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     const float w0 = sm.w[2 * t], w1 = sm.w[2 * t + 1], w2 = sm.w[8 + 2 * t], w3 = sm.w[9 + 2 * t];
     const float escale = sm.escale;
     const int rlen = sm.len;
+    const int nbr = (rlen + kPage - 1) / kPage;   // the row's blocks (forced-block rule)
+    WarpTopk list;   // this warp's running top-k of the segment's blocks
+    list.clear();
     uint32_t qa[8][2][2];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
@@ -359,11 +363,28 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        if (lane == 0 && ti.nrows && blk * kPage < rlen)
-          a.bscores[static_cast<size_t>(ti.row0) * a.bs_stride + blk] = m * escale;
+        if (ti.nrows && blk * kPage < rlen) {   // warp-uniform
+          const float sc = m * escale;
+          if (a.bscores && lane == 0) a.bscores[static_cast<size_t>(ti.row0) * a.bs_stride + blk] = sc;
+          if (a.cand) list.insert(select_key(sc, blk, nbr, a.init_blocks, a.local_blocks), a.topk, lane);
+        }
       }
       __syncwarp();
       if (hh + 2 < nhalf) issue(hh + 2);
+    }
+    if (a.cand && pre[tile] + seg_hi >= hi) pdl_trigger();   // this CTA's blocks are scored
+    if (a.cand) {
+      // the segment's candidates: the 16 warps' lists merged by warp 0 into
+      // slot tile + CTA; then the tile's ticket (the last CTA merges the tile)
+      for (int half = kWarps / 2; half >= 1; half >>= 1) {   // a tree of pairwise merges
+        if (warp >= half && warp < 2 * half) warp_store(list, &sm.wlist[warp][0], 64, lane);
+        __syncthreads();
+        if (warp < half) warp_merge2(list, warp_load(&sm.wlist[warp + half][0], 64, lane), a.topk, lane);
+      }
+      if (warp == 0) write_keys(list, a.topk, a.cand + static_cast<size_t>(tile + blockIdx.x) * a.topk, lane);
+      __syncthreads();
+      tile_finish<1>(a, L, tile, seg_hi - seg_lo, reinterpret_cast<unsigned long long*>(&sm.stage[0][0][0]),
+                     static_cast<int>(sizeof(sm.stage) / 8), sm.vslot, &sm.fin, kThreads);
     }
     pos = pre[tile] + seg_hi;
     ++tile;
@@ -376,13 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
 }  // namespace
 
 int launch_score_decode(const ScoreArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(DecodeSmem) + (a.mx ? sizeof(MxScratch) : 0) + (a.ntiles + 1) * 4 + 16;
+  const size_t smem = sizeof(DecodeSmem) + (a.mx ? sizeof(MxScratch) : 0) + TileLayout::bytes(a.ntiles) + 16;
   if (smem > 227 * 1024) return M3S_ERR_UNSUPPORTED;
   const auto kernel = a.mx ? score_decode_kernel<true> : score_decode_kernel<false>;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return M3S_ERR_LAUNCH;
-  return launch_kernel(kernel, dim3(sm_count()), dim3(kThreads), smem, st, 0, a) ==
+  return launch_kernel(kernel, dim3(grid_size()), dim3(kThreads), smem, st, 0, a) ==
                  cudaSuccess
              ? M3S_OK
              : M3S_ERR_LAUNCH;

@@ -42,7 +42,15 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_workspace_sizes(lib):
     from nvfp4_block_sparse_m3s_gb300 import binding as M
-    assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600) == 8 * 3600 * 4
+    # streaming top-k: a ticket per tile (256-byte rounded), then candidate lists for
+    # ntiles + 255 slots (at most 256 CTAs) of rows-per-tile x topk 8-byte keys
+    assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600, 0, 0, 16, 16) == \
+        256 + (8 + 255) * 1 * 16 * 8
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 128, 16, 1600, 0, 0, 16, 16, 8) == \
+        256 + (16 + 255) * 8 * 16 * 8
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 8192, 1, 2112, 0, 0, 16, 16, 8192) == \
+        4096 + (1024 + 255) * 8 * 16 * 8
+    assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600, 0, 0, 16, 0) == 0   # no top-k
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 0, 8, 3600) == 0
     # attention merges its split-K partials on chip (thread-block cluster): no workspace
     assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == 0
