@@ -47,9 +47,10 @@ def parse():
     ap.add_argument("--no-per-workload", action="store_true",
                     help="measure the headline workload only (default: all five, the others "
                          "reported under per_workload)")
-    ap.add_argument("--topk-path", choices=["fused", "pair"], default="fused",
-                    help="decode rows: fused = m3s_index_score_topk (the top-k merged inside the "
-                         "scorer); pair = m3s_index_block_scores then m3s_block_topk")
+    ap.add_argument("--topk-path", choices=["call", "pair"], default="pair",
+                    help="decode rows: pair = m3s_index_block_scores then m3s_block_topk (the "
+                         "kernels m3s_index_score_topk runs for up to 256 rows, the scorer timed "
+                         "alone); call = m3s_index_score_topk itself")
     ap.add_argument("--cache-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="K / V / index-K record format")
     ap.add_argument("--write-path", choices=["store", "fused", "staged"], default="store",
@@ -139,8 +140,10 @@ def job_rows_per_s(world: int, rows_per_rank: int, ms: float) -> float:
     return world * rows_per_rank / (ms * 1e-3)
 
 
-#: kernels each way of running score + top-k launches per call
-SCORE_CALL_LAUNCHES = {"verify": 1, "index": 1, "pair": 2}
+#: the scorers' CTA bound: a score + top-k call with more query tiles than this
+#: streams its top-k inside the scorer (one launch), else it launches the scorer
+#: and then the top-k
+MAX_GRID = 256
 
 #: bytes per token and head of a K, V or index-K record
 RECORD_BYTES = {"nvfp4": 72, "mxfp4": 68}
@@ -599,7 +602,7 @@ def measure_workload(name, args, dev, world):
 
     q_in = d["q"] if write_path == "store" else q_n
     qidx_in = d["q_idx"] if write_path == "store" else qidx_n
-    topk_pair = getattr(args, "topk_path", "fused") == "pair"
+    topk_pair = getattr(args, "topk_path", "pair") == "pair"
 
     def score():
         if fused:
@@ -673,8 +676,9 @@ def measure_workload(name, args, dev, world):
 
     # our kernels per step: store (or quantise-at-write; staged: + the store), row
     # map, the scorer call's kernels, attention
-    launches_per_step = 3 + (1 if write_path == "staged" else 0) + SCORE_CALL_LAUNCHES[
-        "verify" if fused else ("pair" if topk_pair else "index")]
+    ntiles = B * ((max(s.q_rows) + 7) // 8) if fused else R
+    streams = (fused or not topk_pair) and ntiles > MAX_GRID
+    launches_per_step = 3 + (1 if write_path == "staged" else 0) + (1 if streams else 2)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -827,9 +831,11 @@ def measure_workload(name, args, dev, world):
         achieved = score_bytes / (score_ms * 1e-3) / 1e9
         peak_name = "hbm_gbs"
     psrc = (lambda nm: f"measured (MEASURED_PEAKS.json {nm})" if src == "measured" else "fallback")
-    score_kernel = ("score_kernel<8> (m3s_verify_score_topk)" if fused else
+    score_kernel = (("score_kernel<8> (m3s_verify_score_topk, top-k streamed inside)" if streams else
+                     "score_kernel<8> + topk_kernel (m3s_verify_score_topk)") if fused else
                     ("score_decode_kernel (m3s_index_block_scores)" if topk_pair else
-                     "score_decode_kernel (m3s_index_score_topk, top-k merged inside)"))
+                     ("score_decode_kernel (m3s_index_score_topk, top-k streamed inside)" if streams else
+                      "score_decode_kernel + topk_kernel (m3s_index_score_topk)")))
     attn_gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
     return {
         "name": s.name,

@@ -116,15 +116,19 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
  *   R rows, B requests, max_blocks = block-table width (bt_stride), Hq / Hkv
  *   q and KV heads, Hi index heads, topk, max_q = the largest rows-per-request
  *   the verify call will see (the cu_q differences).
- * Index / verify (0 when topk is 0): the streaming top-k's state, sized by
- * the tiles of query rows the call scores (index: one tile per row, ntiles = R;
- * verify: tiles of up to 8 rows of one request, ntiles = B * ceil(max_q / 8)):
- * one 4-byte ticket per tile (rounded up to 256 bytes), then candidate lists
- * of topk 8-byte keys for (ntiles + 255) slots of 1 (index) or 8 (verify)
- * rows. The workspace must read zero when it is first used (zero it once after
- * allocating it); every call leaves it that way again, so it can be reused
- * call after call, graph replays included. A call that raised
- * M3S_DEVERR_TIMEOUT may leave tickets set: zero the workspace again after one.
+ * Index / verify (0 when topk is 0), by the tiles of query rows the call
+ * scores (index: one tile per row, ntiles = R; verify: tiles of up to 8 rows
+ * of one request, ntiles = B * ceil(max_q / 8)):
+ *  - ntiles <= 256: the block scores, R * max_blocks fp32 (the call launches the
+ *    scorer, then the top-k);
+ *  - ntiles > 256: the streaming top-k's state (one launch): one 4-byte ticket
+ *    per tile (rounded up to 256 bytes), then candidate lists of topk 8-byte
+ *    keys for (ntiles + 255) slots of 1 (index) or 8 (verify) rows, then
+ *    (verify) a score scratch of 256 x 8 x max_blocks fp32. This workspace must
+ *    read zero when it is first used (zero it once after allocating it); every
+ *    call leaves it that way again, so it can be reused call after call, graph
+ *    replays included. A call that raised M3S_DEVERR_TIMEOUT may leave tickets
+ *    set: zero the workspace again after one.
  * Attention: 0 (its split-K partials are merged on chip); its ws arguments
  * are accepted and ignored.
  */
@@ -255,13 +259,17 @@ int m3s_decode_rows(const int32_t* cu_q, const int32_t* seq_len, int32_t B, int3
  *   block_scores fp32 [R][bt_stride] or NULL: when given, also receives every
  *   row's block scores (entries past the row's block count are left as is).
  * Rows with row_req < 0 or row_len <= 0 produce -1 ids. Needs
- * ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, ...), zeroed before
- * its first use (see there).
- * One launch: the scorer keeps a running top-k per warp as it streams the
- * keys (#2744, Fused verify top-k: a streaming top-k per chunk, then a merge),
- * each CTA leaves its share of a row as topk candidate keys in the workspace,
- * and the CTA that scores a row's last block merges the row's candidates into
- * its ids; the block-score matrix is never written unless asked for.
+ * ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, ...) (for up to 256
+ * rows none when block_scores is given: the scores go there), zeroed before
+ * its first use when R > 256 (see there).
+ * Two forms, by the number of rows. Above 256 rows (more than the scorer runs
+ * CTAs) the top-k streams inside the scorer (#2744, Fused verify top-k: a
+ * streaming top-k per chunk, then a merge): each warp keeps a running top-k as
+ * it scores, each CTA leaves its share of a row as topk candidate keys in the
+ * workspace, and the CTA that scores a row's last block merges the row's
+ * candidates into its ids; one launch, no block-score matrix. Up to 256 rows
+ * every row ends with the launch and those merges would form its tail: the
+ * scorer writes the block scores and a second launch selects.
  */
 int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                          m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,
@@ -325,10 +333,12 @@ int m3s_index_score_topk_static(const uint16_t* q_idx, const float* w, int32_t H
  *   row_len int32 [R] their causal lengths (m3s_decode_rows),
  *   max_q >= every cu_q[b+1]-cu_q[b] (sizes the request-row tiling).
  * Other arguments as for m3s_index_score_topk (the index plane NVFP4 or MXFP4,
- * with the same exactness). One launch, the top-k streamed and merged inside
- * it as for m3s_index_score_topk; rows past cu_q[B] get -1 ids. Needs
- * ws_bytes >= m3s_workspace_bytes(M3S_OP_VERIFY_SCORE_TOPK, ...), zeroed before
- * its first use.
+ * with the same exactness); rows past cu_q[B] get -1 ids. As for
+ * m3s_index_score_topk, more than 256 tiles stream the top-k inside the scorer
+ * (one launch; the epilogue leaves each row's block maxima in a per-CTA score
+ * scratch, one warp a row selects at its segment's end), else block scores and
+ * a second launch. Needs ws_bytes >= m3s_workspace_bytes(M3S_OP_VERIFY_SCORE_TOPK,
+ * ...), zeroed before its first use in the streaming form.
  */
 int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                           m3s_fp4_plane idx_k, const int32_t* block_table, int32_t bt_stride,

@@ -10,16 +10,15 @@ size_t round16(size_t n) { return (n + 15) & ~static_cast<size_t>(15); }
 extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_blocks, int32_t Hq,
                                       int32_t Hkv, int32_t Hi, int32_t topk, int32_t max_q) {
   (void)Hi;
-  (void)max_blocks;
   (void)Hq;
   (void)Hkv;
   if (R <= 0 || topk <= 0) return 0;
   switch (op) {
     case M3S_OP_INDEX_SCORE_TOPK:   // one tile per row
-      return round16(m3s::topk_ws_bytes(R, 1, topk));
+      return round16(m3s::score_topk_ws_bytes(R, 1, R, max_blocks, topk));
     case M3S_OP_VERIFY_SCORE_TOPK: {   // tiles of up to 8 rows of one request
       const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;
-      return round16(m3s::topk_ws_bytes(B > 0 ? B * cpr : 0, 8, topk));
+      return round16(m3s::score_topk_ws_bytes(B > 0 ? static_cast<long long>(B) * cpr : 0, 8, R, max_blocks, topk));
     }
     case M3S_OP_SPARSE_ATTENTION:
       // split-K partials are combined inside a thread-block cluster: no workspace

@@ -66,7 +66,10 @@ constexpr int kTileSetUpStreaming = 10;
 // issuers, one per accumulator slot (block g -> issuer g % kND, so one issuer's
 // commits overlap the other's MMAs); warps 1 + kND .. kND + 4 kNEpi: epilogue
 // warpgroups (block g -> g % kNEpi, which owns accumulator slot g % kND); then
-// kNDQ dequantising warpgroups.
+// kNDQ dequantising warpgroups. With the streaming top-k the epilogue (the
+// busiest role) only stores each row's block maximum into the CTA's score
+// scratch (L2-resident, reused every segment); at the segment's end one warp
+// per row selects the row's top-k from it.
 // Tensor memory: kNA A slots of 64 columns (128 keys x 128 f16) and kND
 // accumulator slots of N = 16 * QT f32 columns.
 template <int QT>
@@ -103,8 +106,10 @@ struct __align__(1024) ScoreSmem {
   uint64_t full[Cfg<QT>::kNS], empty[Cfg<QT>::kNS];
   uint64_t afull[Cfg<QT>::kNA], aempty[Cfg<QT>::kNA];
   uint64_t dfull[Cfg<QT>::kND], dempty[Cfg<QT>::kND];
-  uint32_t blkmax[Cfg<QT>::kND][4][QT];  // order-preserving bits of per-warp maxima
-  unsigned long long elist[Cfg<QT>::kNEpi][QT][64];   // per epilogue warpgroup and row: running top-k
+  // order-preserving bits of per-warp block maxima, by accumulator slot and by the
+  // parity of the warpgroup's block count: a buffer is written again only after
+  // the warpgroup's next barrier, which its reader passes first
+  uint32_t blkmax[Cfg<QT>::kND][2][4][QT];
   int vslot[kMaxGrid + 32];                   // candidate slots of a tile being merged
   int fin;
   alignas(16) float wsm[QT * 16];        // weights times 2^(e_h - e_ref) of their row (read as float4)
@@ -117,7 +122,7 @@ struct __align__(1024) ScoreSmem {
 };
 
 static_assert(offsetof(ScoreSmem<8>, wsm) % 16 == 0, "the epilogue reads the weights as float4");
-static_assert(offsetof(ScoreSmem<8>, elist) % 8 == 0 && offsetof(ScoreSmem<8>, full) % 8 == 0, "8-byte members");
+static_assert(offsetof(ScoreSmem<8>, full) % 8 == 0, "8-byte members");
 
 template <int QT>
 size_t score_smem_bytes(int ntiles) {
@@ -245,7 +250,6 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       if (kc == 0) sm.qexp[n] = eh;
     }
     if (tid < QT) sm.lensm[tid] = tid < ti.nrows ? a.row_len[ti.row0 + tid] : 0;
-    for (int e = tid; e < C::kNEpi * QT * 64; e += C::kThreads) (&sm.elist[0][0][0])[e] = 0ull;
     fence_proxy_async();  // the queries are read by the tensor core (async proxy)
     __syncthreads();
     // score = 2^e_ref * sum_h (w_h 2^(e_h - e_ref)) ReLU(scaled dot product), per
@@ -325,16 +329,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       int rlen[QT];
 #pragma unroll
       for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
-      // Streaming top-k: warp wq keeps the lists of rows 2 wq and 2 wq + 1 (lanes 0
-      // and 1 compute their block maxima). A list takes its first topk keys as
-      // they come, is sorted once full, and from then on a key enters only above
-      // the list's k-th (a warp-uniform register compare; then one warp insert).
-      static_assert(QT <= 8, "two rows a warp of the warpgroup");
-      const int my_row = 2 * wq + (lane & 1);
-      const float rscale = sm.rowscale[my_row];   // lanes 0 and 1: their row's 2^e_ref
-      const int nbr = (sm.lensm[my_row] + kPage - 1) / kPage;   // its blocks (forced-block rule)
-      int lcnt = 0;                  // lanes 0 and 1: keys their row's list holds
-      unsigned long long lkth = 0ull;  // and its k-th key once full
+      const float rscale = sm.rowscale[etid < QT ? etid : 0];   // this thread's row's 2^e_ref
       PageWindow pw;
       for (int j = ((ep - g0) % C::kNEpi + C::kNEpi) % C::kNEpi; j < nseg; j += C::kNEpi) {
         const int g = g0 + j, ds = g % C::kND, ud = g / C::kND;
@@ -397,64 +392,26 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
         for (int rho = 0; rho < QT; ++rho) {
           const uint32_t key = ordered_bits(tok < rlen[rho] ? sc[rho] : -INFINITY);
           const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-          if (lane == 0) sm.blkmax[ds][wq][rho] = mx;
+          if (lane == 0) sm.blkmax[ds][ud & 1][wq][rho] = mx;
         }
         named_bar_sync(1 + ep, 128);
         if (*reinterpret_cast<volatile int*>(&sm.abort)) break;  // uniform: read after the barrier
         {
-          // lanes 0 and 1: their row's block key; mode 1 = the list just filled
-          // (sort it once), 2 = the key enters the full list (a warp insert)
-          int mode = 0;
-          unsigned long long key = 0ull;
-          if (lane < 2 && my_row < ti.nrows && blk * kPage < sm.lensm[my_row]) {
+          // rows: threads 0 .. QT-1 of the warpgroup (its first warp's lanes)
+          // take their block maxima right after the barrier
+          if (etid < QT) {
+            const int rho = etid;
             float m = -INFINITY;
-            if (page >= 0 && page < a.num_pages) {
-              uint32_t mk = 0;
+            if (rho < ti.nrows && blk * kPage < rlen[rho]) {
+              if (page >= 0 && page < a.num_pages) {
+                uint32_t mk = 0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) mk = max(mk, sm.blkmax[ds][q][my_row]);
-              m = from_ordered_bits(mk) * rscale;
-            }
-            if (a.bscores) a.bscores[static_cast<size_t>(ti.row0 + my_row) * a.bs_stride + blk] = m;
-            if (a.cand) {
-              key = select_key(m, blk, nbr, a.init_blocks, a.local_blocks);
-              if (lcnt < a.topk) {   // filling: append
-                sm.elist[ep][my_row][lcnt] = key;
-                if (++lcnt == a.topk) mode = 1;
-              } else if (key > lkth) {
-                mode = 2;
+                for (int q = 0; q < 4; ++q) mk = max(mk, sm.blkmax[ds][ud & 1][q][rho]);
+                m = from_ordered_bits(mk) * rscale;
               }
+              if (a.bscores) a.bscores[static_cast<size_t>(ti.row0 + rho) * a.bs_stride + blk] = m;
             }
-          }
-          unsigned need = __ballot_sync(0xffffffffu, mode != 0) & 3u;
-          while (need) {   // (warp-uniform; rare once the lists are full)
-            const int h = __ffs(need) - 1;
-            need &= need - 1;
-            const int md = __shfl_sync(0xffffffffu, mode, h);
-            unsigned long long* lst = &sm.elist[ep][2 * wq + h][0];
-            __syncwarp();   // lane h's append is visible
-            WarpTopk t = warp_load(lst, 64, lane);
-            if (md == 1) {
-              warp_sort_desc(t, a.topk, lane);
-            } else {
-              t.kth = __shfl_sync(0xffffffffu, lkth, h);
-              t.insert(__shfl_sync(0xffffffffu, key, h), a.topk, lane);
-            }
-            warp_store(t, lst, 64, lane);
-            const unsigned long long nk = __shfl_sync(0xffffffffu, a.topk > 32 ? t.b : t.a, (a.topk - 1) & 31);
-            if (lane == h) lkth = nk;
-          }
-        }
-      }
-      if (a.cand) {   // lists that never filled: sorted for the segment's merge
-        const unsigned part = __ballot_sync(0xffffffffu, lane < 2 && lcnt > 0 && lcnt < a.topk) & 3u;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if ((part >> h) & 1u) {
-            unsigned long long* lst = &sm.elist[ep][2 * wq + h][0];
-            __syncwarp();
-            WarpTopk t = warp_load(lst, 64, lane);
-            warp_sort_desc(t, a.topk, lane);
-            warp_store(t, lst, 64, lane);
+            if (a.cand) a.seg_scores[(static_cast<size_t>(blockIdx.x) * QT + rho) * a.bt_stride + j] = m;
           }
         }
       }
@@ -516,12 +473,31 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
     __syncthreads();  // every role is done with this segment (and its queries)
     if (a.cand && pre[tile] + seg_hi >= hi) pdl_trigger();   // this CTA's blocks are scored
     if (a.cand) {
-      // the segment's candidates: per row, the epilogue warpgroups' lists merged
-      // into slot tile + CTA; then the tile's ticket (the last CTA merges the tile)
-      if (warp < ti.nrows) {   // a warp a row: its two warpgroups' lists, one pairwise merge
-        WarpTopk x = warp_load(&sm.elist[0][warp][0], 64, lane);
-        warp_merge2(x, warp_load(&sm.elist[1][warp][0], 64, lane), a.topk, lane);
-        write_keys(x, a.topk, a.cand + (static_cast<size_t>(tile + blockIdx.x) * QT + warp) * a.topk, lane);
+      // the segment's candidates: warp rho takes row rho's block maxima from the
+      // CTA's score scratch 32 at a time and keeps their top-k (a key enters
+      // only above the list's k-th), into slot tile + CTA; then the tile's
+      // ticket (the last CTA of the tile merges it)
+      if (warp < ti.nrows) {
+        const int rho = warp;
+        const int rl_r = sm.lensm[rho];
+        const int nbr = (rl_r + kPage - 1) / kPage;
+        const float* row_sc = a.seg_scores + (static_cast<size_t>(blockIdx.x) * QT + rho) * a.bt_stride;
+        WarpTopk list;
+        list.clear();
+        for (int j0 = 0; j0 < nseg; j0 += 32) {
+          const int j = j0 + lane;
+          const int blk = seg_lo + j;
+          unsigned long long key = 0ull;
+          if (j < nseg && blk * kPage < rl_r)
+            key = select_key(__ldcg(row_sc + j), blk, nbr, a.init_blocks, a.local_blocks);
+          unsigned over = __ballot_sync(0xffffffffu, key > list.kth);
+          while (over) {   // ascending lanes: each key is inserted in turn
+            const int l = __ffs(over) - 1;
+            over &= over - 1;
+            list.insert(__shfl_sync(0xffffffffu, key, l), a.topk, lane);
+          }
+        }
+        write_keys(list, a.topk, a.cand + (static_cast<size_t>(tile + blockIdx.x) * QT + rho) * a.topk, lane);
       }
       __syncthreads();
       tile_finish<QT>(a, L, tile, nseg, reinterpret_cast<unsigned long long*>(&sm.stage[0][0]),
@@ -726,8 +702,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // The streaming top-k's workspace (sized by m3s_workspace_bytes): the tiles'
 // tickets, then the candidate lists.
 void bind_topk_workspace(ScoreArgs& a, void* ws, int ntiles, int topk, int init_blocks, int local_blocks,
-                         int32_t* ids, int qt = 1) {
-  (void)qt;
+                         int32_t* ids) {
   a.ticket = static_cast<unsigned*>(ws);
   a.cand = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + topk_ticket_bytes(ntiles));
   a.topk = topk;
@@ -840,15 +815,28 @@ extern "C" int m3s_index_score_topk(const uint16_t* q_idx, const float* w, int32
   if (!row_req || !row_len || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
   if (R > kMaxTiles) return M3S_ERR_UNSUPPORTED;
   if (topk == 0) return M3S_OK;
-  if (ws_bytes < m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, 1))
-    return M3S_ERR_WORKSPACE;
-  if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
   const int stride = bt_stride > 0 ? bt_stride : 1;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool streams = topk_streams(R);
+  if (streams || !block_scores) {
+    if (ws_bytes < m3s_workspace_bytes(M3S_OP_INDEX_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, 1))
+      return M3S_ERR_WORKSPACE;
+    if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
+  }
+  float* bs = block_scores ? block_scores : static_cast<float*>(ws);
   ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-              row_req, nullptr, row_len, R, B, R, 1, block_scores, stride, err,
+              row_req, nullptr, row_len, R, B, R, 1, streams ? block_scores : bs, stride, err,
               idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
-  bind_topk_workspace(a, ws, R, topk, init_blocks, local_blocks, topk_ids);
-  return launch_score_decode(a, static_cast<cudaStream_t>(stream));
+  if (streams) {
+    bind_topk_workspace(a, ws, R, topk, init_blocks, local_blocks, topk_ids);
+    return launch_score_decode(a, st);
+  }
+  if (B > 0) {   // two launches: block scores, then the top-k
+    rc = launch_score_decode(a, st);
+    if (rc != M3S_OK) return rc;
+  }
+  return launch_topk(bs, stride, row_req, row_len, R, B, bt_stride, topk, init_blocks, local_blocks,
+                     topk_ids, st);
 }
 
 extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
@@ -869,11 +857,25 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
   if (ws_bytes < m3s_workspace_bytes(M3S_OP_VERIFY_SCORE_TOPK, R, B, bt_stride, 0, 0, Hi, topk, max_q))
     return M3S_ERR_WORKSPACE;
   if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool streams = topk_streams(ntiles);
+  const int stride = bt_stride > 0 ? bt_stride : 1;
   ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
-              nullptr, cu_q, row_len, R, B, static_cast<int>(ntiles), cpr, nullptr, bt_stride, err,
+              nullptr, cu_q, row_len, R, B, static_cast<int>(ntiles), cpr,
+              streams ? nullptr : static_cast<float*>(ws), stride, err,
               idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
-  bind_topk_workspace(a, ws, static_cast<int>(ntiles), topk, init_blocks, local_blocks, topk_ids, 8);
-  return launch_score<8>(a, static_cast<cudaStream_t>(stream));
+  if (streams) {
+    bind_topk_workspace(a, ws, static_cast<int>(ntiles), topk, init_blocks, local_blocks, topk_ids);
+    a.seg_scores = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(a.cand) +
+                                            topk_cand_bytes(static_cast<int>(ntiles), 8, topk));
+    return launch_score<8>(a, st);
+  }
+  if (ntiles > 0) {   // two launches: block scores, then the top-k (rows past cu_q[B]: -1)
+    rc = launch_score<8>(a, st);
+    if (rc != M3S_OK) return rc;
+  }
+  return launch_topk(static_cast<float*>(ws), stride, nullptr, row_len, R, B, bt_stride, topk, init_blocks,
+                     local_blocks, topk_ids, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -37,6 +37,7 @@ struct ScoreArgs {
   int32_t* ids;               // [R][topk] output ids, or nullptr when keys_out is given
   unsigned long long* keys_out;  // [R][topk] merged keys (candidate output), or nullptr
   const int32_t* blk_base;    // per request: global id of the call's block 0 (or nullptr)
+  float* seg_scores;          // verify path: per CTA, [QT][bt_stride] block maxima of its segment
 };
 
 template <int QT>
@@ -593,12 +594,35 @@ __device__ void tile_finish(const ScoreArgs& a, const TileLayout& L, int t, int 
 }
 
 // Streaming top-k workspace: a ticket per tile (rounded up to 256 bytes), then
-// candidate lists for ntiles + kMaxGrid - 1 slots of qt rows x topk keys.
+// candidate lists for ntiles + kMaxGrid - 1 slots of qt rows x topk keys, then
+// (multi-row tiles) each CTA's segment score scratch, qt rows x bt_stride fp32.
 __host__ __device__ constexpr size_t topk_ticket_bytes(int ntiles) {
   return (static_cast<size_t>(ntiles) * 4 + 255) & ~static_cast<size_t>(255);
 }
-__host__ __device__ constexpr size_t topk_ws_bytes(int ntiles, int qt, int topk) {
-  return topk_ticket_bytes(ntiles) + static_cast<size_t>(ntiles + kMaxGrid - 1) * qt * topk * 8;
+__host__ __device__ constexpr size_t topk_cand_bytes(int ntiles, int qt, int topk) {
+  return static_cast<size_t>(ntiles + kMaxGrid - 1) * qt * topk * 8;
+}
+__host__ __device__ constexpr size_t topk_ws_bytes(int ntiles, int qt, int topk, int bt_stride = 0) {
+  return topk_ticket_bytes(ntiles) + topk_cand_bytes(ntiles, qt, topk) +
+         (qt > 1 ? static_cast<size_t>(kMaxGrid) * qt * (bt_stride > 0 ? bt_stride : 1) * 4 : 0);
+}
+
+// Which form a score + top-k call takes. With more tiles than CTAs can run,
+// tiles finish throughout the launch and each tile's candidate merge overlaps
+// other tiles' scoring: the top-k streams inside the scorer (one launch, no
+// block-score matrix). With at most kMaxGrid tiles every tile ends with the
+// launch and the merges form its tail; there the block scores go to the
+// workspace and a second launch selects (it starts while the scorer ends).
+// Measured on the decode batches (1-8 rows) and the 16 x 8 verify batch, the
+// two-launch form was the faster one; on the 8192-row prefill chunk (1024
+// tiles), streaming.
+__host__ __device__ constexpr bool topk_streams(long long ntiles) { return ntiles > kMaxGrid; }
+
+// Workspace bytes of a score + top-k call: the streaming state, or the block
+// scores (rows x bt_stride fp32) of the two-launch form.
+__host__ __device__ constexpr size_t score_topk_ws_bytes(long long ntiles, int qt, int R, int bt_stride, int topk) {
+  return topk_streams(ntiles) ? topk_ws_bytes(static_cast<int>(ntiles), qt, topk, bt_stride)
+                              : static_cast<size_t>(R) * (bt_stride > 0 ? bt_stride : 1) * 4;
 }
 
 int sm_count();

@@ -42,14 +42,18 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_workspace_sizes(lib):
     from nvfp4_block_sparse_m3s_gb300 import binding as M
-    # streaming top-k: a ticket per tile (256-byte rounded), then candidate lists for
-    # ntiles + 255 slots (at most 256 CTAs) of rows-per-tile x topk 8-byte keys
-    assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600, 0, 0, 16, 16) == \
-        256 + (8 + 255) * 1 * 16 * 8
+    # up to 256 tiles (index: a tile per row; verify: up to 8 rows of one request):
+    # two launches, the block scores (rows x bt_stride fp32) in the workspace
+    assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600, 0, 0, 16, 16) == 8 * 3600 * 4
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 128, 16, 1600, 0, 0, 16, 16, 8) == \
-        256 + (16 + 255) * 8 * 16 * 8
+        128 * 1600 * 4
+    # more tiles: the streaming top-k's state, a ticket per tile (256-byte rounded),
+    # candidate lists for ntiles + 255 slots of rows-per-tile x topk 8-byte keys and
+    # (verify) each CTA's segment score scratch (8 rows x bt_stride fp32)
+    assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 300, 300, 24, 0, 0, 16, 16) == \
+        1280 + (300 + 255) * 1 * 16 * 8
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 8192, 1, 2112, 0, 0, 16, 16, 8192) == \
-        4096 + (1024 + 255) * 8 * 16 * 8
+        4096 + (1024 + 255) * 8 * 16 * 8 + 256 * 8 * 2112 * 4
     assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600, 0, 0, 16, 0) == 0   # no top-k
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 0, 8, 3600) == 0
     # attention merges its split-K partials on chip (thread-block cluster): no workspace
