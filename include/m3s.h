@@ -109,6 +109,7 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
 #define M3S_OP_INDEX_SCORE_TOPK 1
 #define M3S_OP_VERIFY_SCORE_TOPK 2
 #define M3S_OP_SPARSE_ATTENTION 3
+#define M3S_OP_INDEX_CANDIDATES 4
 
 /*
  * Workspace bytes an op needs (device memory the caller provides as `ws`).
@@ -295,6 +296,46 @@ int m3s_index_block_scores(const uint16_t* q_idx, const float* w, int32_t Hi,
 int m3s_block_topk(const float* block_scores, int32_t bs_stride, const int32_t* row_req,
                    const int32_t* row_len, int32_t R, int32_t B, int32_t bt_stride, int32_t topk,
                    int32_t init_blocks, int32_t local_blocks, int32_t* topk_ids, void* stream);
+
+/*
+ * Indexer context parallelism. #2744, review thread on the unused page-16
+ * tables: with indexer CP one request's index keys are split over ranks; each
+ * rank scores its share and the ranks' candidate keys are merged
+ * (merge_candidate_keys) into the top-k. (The pages' engine refuses CP
+ * together with the FP4 index at startup; this library does not.)
+ *
+ * Candidate keys, uint64, larger = better, 0 = an empty slot:
+ *   a scored block:  high word = the fp32 block score's order-preserving bits
+ *                    (x >= 0: bits | 0x80000000, x < 0: ~bits, -0 as +0),
+ *                    low word = 0xFFFFFFFF - block id (ties to the lower id);
+ *   a forced init block:  0xFFFFFFFF : 0xFFFFFFFF - id;
+ *   a forced local block: 0xFFFFFFFE : id.
+ *
+ * m3s_index_score_candidates: the rows' top-k over a slice of each request's
+ * blocks, as candidate keys cand_keys uint64 [R][topk] (descending, 0-padded),
+ * with the request's block ids and token positions: request b's slice holds
+ * its blocks blk_begin[b] .. blk_begin[b] + blk_count[b] - 1 (int32 [B],
+ * device), local block j at block_table[b][j] of this slice's table; row r
+ * (length row_len[r], the whole request's causal length) scores the slice's
+ * tokens below row_len[r]. Forced blocks are placed by the row's own block
+ * count. Other arguments as for m3s_index_score_topk. One launch (the
+ * streaming form); ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_CANDIDATES,
+ * ...), zeroed before its first use (every call leaves it zeroed).
+ *
+ * m3s_merge_candidates: the top-k ids of each row from n_lists ranks' candidate
+ * keys (cand_keys uint64 [n_lists][R][topk], each row's list descending),
+ * ascending and -1 padded, as m3s_index_score_topk returns them; n_lists <= 256.
+ * Merging every slice's candidates gives the unsplit call's ids: each block of
+ * a row's top-k is among its own slice's top-k.
+ */
+int m3s_index_score_candidates(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_fp4_plane idx_k,
+                               const int32_t* block_table, int32_t bt_stride, const int32_t* blk_begin,
+                               const int32_t* blk_count, const int32_t* row_req, const int32_t* row_len,
+                               int32_t R, int32_t B, int32_t topk, int32_t init_blocks,
+                               int32_t local_blocks, uint64_t* cand_keys, void* ws, size_t ws_bytes,
+                               int32_t* err, void* stream);
+int m3s_merge_candidates(const uint64_t* cand_keys, int32_t n_lists, int32_t R, int32_t topk,
+                         int32_t* topk_ids, void* stream);
 
 /*
  * m3s_index_score_topk without a caller workspace. The pages have no

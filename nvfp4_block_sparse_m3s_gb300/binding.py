@@ -23,7 +23,7 @@ STATUS = {1: "M3S_ERR_INVALID", 2: "M3S_ERR_UNSUPPORTED", 3: "M3S_ERR_WORKSPACE"
           4: "M3S_ERR_LAUNCH"}
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_PAGE, DEVERR_ROW, DEVERR_QRANGE, DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16, 32
-OP_INDEX_SCORE_TOPK, OP_VERIFY_SCORE_TOPK, OP_SPARSE_ATTENTION = 1, 2, 3
+OP_INDEX_SCORE_TOPK, OP_VERIFY_SCORE_TOPK, OP_SPARSE_ATTENTION, OP_INDEX_CANDIDATES = 1, 2, 3, 4
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 HEAD_DIM = PAGE = 128
 
@@ -76,6 +76,9 @@ _SIGS = {
                                              _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "m3s_sparse_attention": (ctypes.c_int, [_P, _I32, _I32, Plane, Plane, _P, _I32, _I32, _P, _P,
                                             _P, _I32, _I32, _F32, _P, _P, _P, _SZ, _P, _P]),
+    "m3s_index_score_candidates": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _P, _P, _I32,
+                                                  _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
+    "m3s_merge_candidates": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P]),
     "m3s_version": (ctypes.c_char_p, []),
 }
 
@@ -330,3 +333,37 @@ def m3s_sparse_attention(q, hkv: int, k_codes, k_scales, v_codes, v_scales, bloc
         _stream(stream))
     _check(rc, "m3s_sparse_attention")
     return out
+
+
+def m3s_index_score_candidates(q_idx, w, codes, scales, block_table, blk_begin, blk_count, row_req,
+                               row_len, topk: int, cand_keys=None, ws=None, err=None, stream=None,
+                               init_blocks: int = 0, local_blocks: int = 0):
+    """A slice's candidate keys, int64 [R, topk] (the uint64 keys' bits)."""
+    _index_inputs(q_idx, w, block_table, row_req, row_len, blk_begin, blk_count)
+    R, Hi = q_idx.shape[0], q_idx.shape[1]
+    B, bt_stride = block_table.shape
+    if cand_keys is None:
+        cand_keys = torch.empty((R, topk), dtype=torch.int64, device=q_idx.device)
+    if cand_keys.dtype != torch.int64 or not cand_keys.is_contiguous():
+        raise TypeError("cand_keys must be a contiguous int64 tensor [R, topk]")
+    if ws is None:   # zeroed once, as the call requires (each call leaves it so)
+        nb = m3s_workspace_bytes(OP_INDEX_CANDIDATES, R, B, bt_stride, 0, 0, Hi, topk)
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device=q_idx.device)
+    rc = load().m3s_index_score_candidates(
+        _ptr(q_idx), _ptr(w), Hi, plane(codes, scales), _ptr(block_table), bt_stride, _ptr(blk_begin),
+        _ptr(blk_count), _ptr(row_req), _ptr(row_len), R, B, topk, init_blocks, local_blocks,
+        _ptr(cand_keys), _ptr(ws), ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
+    _check(rc, "m3s_index_score_candidates")
+    return cand_keys
+
+
+def m3s_merge_candidates(cand_keys, topk_ids=None, stream=None):
+    """cand_keys int64 [n_lists, R, topk] -> topk_ids int32 [R, topk]."""
+    if cand_keys.dtype != torch.int64 or cand_keys.dim() != 3 or not cand_keys.is_contiguous():
+        raise TypeError("cand_keys must be a contiguous int64 tensor [n_lists, R, topk]")
+    n, R, topk = cand_keys.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((R, topk), dtype=torch.int32, device=cand_keys.device)
+    rc = load().m3s_merge_candidates(_ptr(cand_keys), n, R, topk, _ptr(topk_ids), _stream(stream))
+    _check(rc, "m3s_merge_candidates")
+    return topk_ids

@@ -879,6 +879,77 @@ extern "C" int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int3
 }
 
 // ---------------------------------------------------------------------------
+// Indexer context parallelism: a slice's candidates, and their merge.
+// ---------------------------------------------------------------------------
+namespace m3s {
+namespace {
+
+// One warp per row: the k best keys of the n_lists ranks' lists (list i of row r
+// at cand + (i * R + r) * topk), as ids ascending (-1 padded).
+__global__ void __launch_bounds__(256) merge_candidates_kernel(const unsigned long long* __restrict__ cand,
+                                                               int n_lists, int R, int topk,
+                                                               int32_t* __restrict__ ids) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= R) return;   // (warp-uniform)
+  WarpTopk sel;
+  warp_merge<true>(cand + static_cast<size_t>(r) * topk, nullptr, R * topk, n_lists, topk, topk, lane, sel);
+  write_ids(sel, topk, ids + static_cast<size_t>(r) * topk, lane);
+}
+
+}  // namespace
+}  // namespace m3s
+
+extern "C" int m3s_index_score_candidates(const uint16_t* q_idx, const float* w, int32_t Hi,
+                                          m3s_fp4_plane idx_k, const int32_t* block_table,
+                                          int32_t bt_stride, const int32_t* blk_begin,
+                                          const int32_t* blk_count, const int32_t* row_req,
+                                          const int32_t* row_len, int32_t R, int32_t B, int32_t topk,
+                                          int32_t init_blocks, int32_t local_blocks,
+                                          uint64_t* cand_keys, void* ws, size_t ws_bytes, int32_t* err,
+                                          void* stream) {
+  using namespace m3s;
+  int32_t dummy = 0;
+  int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, &dummy);
+  if (rc != M3S_OK || R == 0) return rc;
+  if (!row_req || !row_len || !cand_keys || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
+  if (B > 0 && (!blk_begin || !blk_count)) return M3S_ERR_INVALID;
+  if (R > kMaxTiles) return M3S_ERR_UNSUPPORTED;
+  if (topk == 0) return M3S_OK;
+  if (ws_bytes < m3s_workspace_bytes(M3S_OP_INDEX_CANDIDATES, R, B, bt_stride, 0, 0, Hi, topk, 1))
+    return M3S_ERR_WORKSPACE;
+  if (!ws || !aligned16(ws) || (reinterpret_cast<uintptr_t>(cand_keys) & 7u)) return M3S_ERR_INVALID;
+  ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
+              row_req, nullptr, row_len, R, B, R, 1, nullptr, bt_stride > 0 ? bt_stride : 1, err,
+              idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
+  bind_topk_workspace(a, ws, R, topk, init_blocks, local_blocks, nullptr);
+  a.keys_out = reinterpret_cast<unsigned long long*>(cand_keys);
+  a.blk_base = blk_begin;
+  a.blk_count = blk_count;
+  return launch_score_decode(a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int m3s_merge_candidates(const uint64_t* cand_keys, int32_t n_lists, int32_t R, int32_t topk,
+                                    int32_t* topk_ids, void* stream) {
+  using namespace m3s;
+  if (n_lists < 0 || R < 0 || topk < 0) return M3S_ERR_INVALID;
+  if (topk > M3S_MAX_TOPK || n_lists > kMaxGrid) return M3S_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(R) * topk > INT32_MAX) return M3S_ERR_UNSUPPORTED;   // list stride is int
+  if (R == 0 || topk == 0) return M3S_OK;
+  if (!topk_ids || (n_lists > 0 && !cand_keys) || (reinterpret_cast<uintptr_t>(cand_keys) & 7u))
+    return M3S_ERR_INVALID;
+  const int rows_per_cta = 8;
+  return launch_kernel(merge_candidates_kernel, dim3((R + rows_per_cta - 1) / rows_per_cta),
+                       dim3(32 * rows_per_cta), 0, static_cast<cudaStream_t>(stream), 0,
+                       reinterpret_cast<const unsigned long long*>(cand_keys), n_lists, R, topk, topk_ids) ==
+                 cudaSuccess
+             ? M3S_OK
+             : M3S_ERR_LAUNCH;
+}
+
+// ---------------------------------------------------------------------------
 // m3s_index_score_topk_static: m3s_index_score_topk with its block-score
 // scratch in a file-scope device array instead of a caller workspace.
 //

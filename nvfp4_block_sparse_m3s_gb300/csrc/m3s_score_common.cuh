@@ -36,7 +36,8 @@ struct ScoreArgs {
   int topk, init_blocks, local_blocks;
   int32_t* ids;               // [R][topk] output ids, or nullptr when keys_out is given
   unsigned long long* keys_out;  // [R][topk] merged keys (candidate output), or nullptr
-  const int32_t* blk_base;    // per request: global id of the call's block 0 (or nullptr)
+  const int32_t* blk_base;    // per request: the request's id of the call's block 0 (or nullptr)
+  const int32_t* blk_count;   // per request: blocks of the call's slice (with blk_base)
   float* seg_scores;          // verify path: per CTA, [QT][bt_stride] block maxima of its segment
 };
 
@@ -56,6 +57,15 @@ __device__ TileInfo<QT> tile_info(const ScoreArgs& a, int t, bool report) {
     ti.len = a.row_len[t];
     if (ti.req < 0 || ti.len <= 0) { ti.len = 0; return ti; }
     ti.nrows = 1;
+    if (a.blk_base && ti.req < a.B) {   // a slice of the request's blocks: its causal part
+      const int base = a.blk_base[ti.req], cnt = max(a.blk_count[ti.req], 0);
+      ti.len = min(max(ti.len - base * kPage, 0), cnt * kPage);
+      if (base < 0 || ti.len <= 0) {   // nothing of this row in the slice
+        ti.nrows = 0;
+        ti.len = 0;
+        return ti;
+      }
+    }
   } else {
     const int b = t / a.cpr, j = t % a.cpr;
     const int c0 = a.cu_q[b], qb = a.cu_q[b + 1] - c0;

@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     const float escale = sm.escale;
     const int rlen = sm.len;
     const int nbr = (rlen + kPage - 1) / kPage;   // the row's blocks (forced-block rule)
+    // a slice of the request's blocks (context parallelism): local block j is the
+    // request's block j + boff, and token positions and ids are the request's
+    const int boff = (a.blk_base && ti.nrows) ? a.blk_base[ti.req] : 0;
     WarpTopk list;   // this warp's running top-k of the segment's blocks
     list.clear();
     uint32_t qa[8][2][2];
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
             p0 *= fa;
             p1 *= fb;
           }
-          const int tok0 = blk * kPage + half * kHalfKeys + key0;
+          const int tok0 = (blk + boff) * kPage + half * kHalfKeys + key0;
           if (tok0 < rlen) best = fmaxf(best, p0);
           if (tok0 + 8 < rlen) best = fmaxf(best, p1);
         }
@@ -363,10 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        if (ti.nrows && blk * kPage < rlen) {   // warp-uniform
+        if (ti.nrows && (blk + boff) * kPage < rlen) {   // warp-uniform
           const float sc = m * escale;
           if (a.bscores && lane == 0) a.bscores[static_cast<size_t>(ti.row0) * a.bs_stride + blk] = sc;
-          if (a.cand) list.insert(select_key(sc, blk, nbr, a.init_blocks, a.local_blocks), a.topk, lane);
+          if (a.cand) list.insert(select_key(sc, blk + boff, nbr, a.init_blocks, a.local_blocks), a.topk, lane);
         }
       }
       __syncwarp();

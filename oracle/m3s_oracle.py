@@ -369,6 +369,52 @@ def topk_ids(bscore: np.ndarray, k: int, init_blocks: int = 0, local_blocks: int
     return out
 
 
+def rank_records(bscore: np.ndarray, ids, nb: int, init_blocks: int = 0, local_blocks: int = 0) -> list:
+    """The order topk_ids selects by, as sortable records (class, in-class value, id):
+    a record ranks higher with a larger class, then a larger in-class value, then a
+    lower id. Init blocks (class 2) by lower id, local blocks (class 1) by higher id,
+    scored blocks (class 0) by score; ``nb`` is the row's block count (the forced
+    blocks are the row's first and last ones)."""
+    out = []
+    for i in ids:
+        i = int(i)
+        if i < init_blocks:
+            out.append((2, -float(i), i))
+        elif i >= nb - local_blocks:
+            out.append((1, float(i), i))
+        else:
+            out.append((0, float(bscore[i]), i))
+    return out
+
+
+def _best_first(records):
+    return sorted(records, key=lambda rec: (-rec[0], -rec[1], rec[2]))
+
+
+def slice_candidates(bscore: np.ndarray, lo: int, hi: int, k: int, init_blocks: int = 0,
+                     local_blocks: int = 0) -> list:
+    """Indexer context parallelism ("[MiniMax-M3.1] FP4 index cache and NVFP4 sparse KV
+    cache" (#2744), review thread on the unused page-16 tables: the indexer-CP decode path
+    merges per-rank candidate keys): the candidates of the rank that holds blocks
+    [lo, hi) of a row whose block scores are ``bscore`` -- the k best of its blocks in
+    the order topk_ids uses (forced blocks by the row's own block count), best first,
+    as rank_records."""
+    nb = len(bscore)
+    recs = rank_records(bscore, range(max(0, lo), min(hi, nb)), nb, init_blocks, local_blocks)
+    return _best_first(recs)[:k]
+
+
+def merge_candidates(lists, k: int) -> np.ndarray:
+    """The k best of the union of the ranks' candidate lists (rank_records), as
+    topk_ids returns them: ids ascending, padded with -1. Because every block of
+    the row's top k is among its own rank's k best, this equals the top k of the
+    whole row."""
+    union = _best_first([rec for lst in lists for rec in lst])[:k]
+    out = np.full(k, -1, dtype=np.int32)
+    out[: len(union)] = np.sort([rec[2] for rec in union]).astype(np.int32)
+    return out
+
+
 def index_score_topk(q_idx: np.ndarray, w: np.ndarray, idx_codes: np.ndarray,
                      idx_scales: np.ndarray, block_table: np.ndarray, row_req: np.ndarray,
                      row_len: np.ndarray, topk: int, rows=None, init_blocks: int = 0,

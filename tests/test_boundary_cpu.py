@@ -55,6 +55,11 @@ def test_workspace_sizes(lib):
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 8192, 1, 2112, 0, 0, 16, 16, 8192) == \
         4096 + (1024 + 255) * 8 * 16 * 8 + 256 * 8 * 2112 * 4
     assert M.m3s_workspace_bytes(M.OP_INDEX_SCORE_TOPK, 8, 8, 3600, 0, 0, 16, 0) == 0   # no top-k
+    # a slice's candidates: always the streaming state, whatever the row count
+    assert M.m3s_workspace_bytes(M.OP_INDEX_CANDIDATES, 8, 8, 3600, 0, 0, 16, 16) == \
+        256 + (8 + 255) * 1 * 16 * 8
+    assert M.m3s_workspace_bytes(M.OP_INDEX_CANDIDATES, 300, 300, 24, 0, 0, 16, 16) == \
+        1280 + (300 + 255) * 1 * 16 * 8
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 0, 8, 3600) == 0
     # attention merges its split-K partials on chip (thread-block cluster): no workspace
     assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == 0
@@ -78,6 +83,16 @@ def test_host_validation_rejects_before_launch(lib):
                                     None, None, 0, None, None) == M.ERR_UNSUPPORTED
     assert lib.m3s_index_score_topk(None, None, 16, P, None, 1, None, None, 1, 1, 65, 0, 0, None,
                                     None, None, 0, None, None) == M.ERR_UNSUPPORTED
+    # context parallelism: top-k beyond the build, more lists than the merge takes,
+    # a slice without its begin / count arrays
+    assert lib.m3s_merge_candidates(None, 2, 4, 65, None, None) == M.ERR_UNSUPPORTED
+    assert lib.m3s_merge_candidates(None, 257, 4, 16, None, None) == M.ERR_UNSUPPORTED
+    assert lib.m3s_merge_candidates(None, 2, 4, 16, None, None) == M.ERR_INVALID
+    assert lib.m3s_merge_candidates(None, 2, 0, 16, None, None) == M.OK
+    fake_plane = M.Plane(ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21), 4, 1)
+    fk = ctypes.c_void_p(1 << 20)
+    assert lib.m3s_index_score_candidates(fk, fk, 16, fake_plane, fk, 4, None, None, fk, fk, 2, 2,
+                                          16, 0, 0, fk, fk, 1 << 20, None, None) == M.ERR_INVALID
     # forced block counts must not be negative
     fake = ctypes.c_void_p(1 << 20)
     assert lib.m3s_block_topk(fake, 8, fake, fake, 1, 1, 8, 4, -1, 0, fake, None) == M.ERR_INVALID

@@ -727,3 +727,40 @@ def test_quantise_at_write_equals_staging_then_store():
         O.nvfp4_store(staged, slots, rc, rs)
         assert np.array_equal(kc, rc) and np.array_equal(ks, rs)
         assert np.array_equal(qo, O.norm_rope_rows(q, None, cos, sin, 64, 1e-6))
+
+
+# --------------------------------------------------------------------------
+# Indexer context parallelism: per-rank candidates, then a merge (#2744, review
+# thread on the unused page-16 tables: merge_candidate_keys)
+# --------------------------------------------------------------------------
+
+def test_split_candidates_merge_to_the_unsplit_top_k():
+    """For any cut of a row's blocks into contiguous slices, merging each slice's k
+    best equals the row's top k (topk_ids, itself pinned by brute force): ties to
+    the lower id and forced init / local blocks included."""
+    rng = np.random.default_rng(40)
+    for trial in range(400):
+        nb = int(rng.integers(1, 90))
+        k = int(rng.integers(1, 20))
+        sc = rng.integers(0, 6, nb).astype(np.float64) if trial % 3 == 0 else rng.standard_normal(nb)
+        init = int(rng.integers(0, 4)) if trial % 2 else 0
+        local = int(rng.integers(0, 5)) if trial % 2 else 0
+        n = int(rng.integers(1, 6))
+        cuts = np.sort(rng.integers(0, nb + 1, n - 1))
+        bounds = [0, *cuts.tolist(), nb]
+        lists = [O.slice_candidates(sc, bounds[i], bounds[i + 1], k, init, local) for i in range(n)]
+        assert all(len(lst) <= k for lst in lists)
+        assert np.array_equal(O.merge_candidates(lists, k), O.topk_ids(sc, k, init, local)), trial
+
+
+def test_slice_candidates_special_cases():
+    """An empty slice has no candidates; a slice of at most k blocks keeps them all;
+    the whole row as one slice gives topk_ids' set, best first."""
+    sc = np.array([3.0, 1.0, 4.0, 1.0, 5.0])
+    assert O.slice_candidates(sc, 2, 2, 3) == []
+    assert sorted(r[2] for r in O.slice_candidates(sc, 1, 3, 5)) == [1, 2]
+    best = O.slice_candidates(sc, 0, 5, 3)
+    assert [r[2] for r in best] == [4, 2, 0]
+    assert np.array_equal(O.merge_candidates([best], 3), O.topk_ids(sc, 3))
+    # equal scores: the lower id first; forced: init (lower id first) above local
+    assert [r[2] for r in O.slice_candidates(np.zeros(6), 0, 6, 6, 1, 2)] == [0, 5, 4, 1, 2, 3]
