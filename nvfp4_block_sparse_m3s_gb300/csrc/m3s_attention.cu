@@ -8,10 +8,12 @@
 //
 // Split-K inside a thread-block cluster: the CTAs (split, kv head, row) of one
 // (kv head, row) form a cluster; each runs an online softmax over its share of
-// the row's blocks, leaves (m, l, o) in its shared memory, and cluster rank 0
-// combines the partials through distributed shared memory and writes the
+// the row's blocks, leaves (m, l, o) in its shared memory, and the cluster's
+// CTAs combine the partials through distributed shared memory and write the
 // output, so there is no second launch and no workspace round trip. Inside a
-// CTA the four warps take 32 tokens each of every 128-token block: S = Q K^T
+// CTA a group of four warps takes 32 tokens each of a 128-token block; a CTA
+// has one group, or two taking alternate blocks (each with its own two-stage
+// page ring) when the grid has at most one CTA per SM. S = Q K^T
 // with the q heads of the KV head as M (m16), then P V with P re-used from the
 // S accumulators as the A operand. K and V are dequantised from the
 // shared-memory copy of the page straight into mma fragments: K in a permuted
@@ -36,9 +38,7 @@
 namespace m3s {
 namespace {
 
-constexpr int kAttWarps = 4;
-constexpr int kAttThreads = kAttWarps * 32;  // == head_dim: one thread per output dim
-constexpr int kBlockBytes = 2 * (kPageCodeBytes + kPageScaleBytes);  // K and V: 18432
+constexpr int kAttMaxWarps = 8;
 
 struct AttnArgs {
   const uint16_t* q;
@@ -64,24 +64,45 @@ struct AttnArgs {
 constexpr int kMergeRow = kHeadDim + 4;
 __device__ __forceinline__ int merge_at(int head, int dim) { return head * kMergeRow + dim + (dim >> 5); }
 
-struct __align__(16) AttnSmem {
-  union {
-    uint8_t stage[2][kBlockBytes];
-    struct {
-      float o[kAttWarps][16 * kMergeRow];
-      float m[kAttWarps][16];
-      float l[kAttWarps][16];
-      float f[kAttWarps][16];   // exp2(m_warp - M) per warp and head
-    } merge;
-  };
+// The warps' partial outputs, merged after the block loop (over the page stages).
+template <int NW>
+struct AttnMerge {
+  float o[NW][16 * kMergeRow];
+  float m[NW][16];
+  float l[NW][16];
+  float f[NW][16];   // exp2(m_warp - M) per warp and head
+};
+
+// Dynamic shared memory: this part, then the page stages (K codes, K scales,
+// V codes, V scales of one page each), which the merge buffers reuse.
+struct __align__(16) AttnFixed {
+  uint4 qa[8][32];            // the q fragments (A operand) per k-step and lane
+  float lsc[16];              // per-head logit scales (log2 units)
   float cta_o[16][kHeadDim];  // this CTA's partial: sum p v, relative to cta_m (log2 units)
   float cta_m[16];
   float cta_l[16];
-  uint64_t bar[2];
+  uint64_t bar[4];            // two stages per warp group
   int page[M3S_MAX_TOPK];
   int ntok[M3S_MAX_TOPK];
   int nblocks;
 };
+constexpr size_t kAttFixedBytes = (sizeof(AttnFixed) + 127) / 128 * 128;
+
+// Named barrier over the n threads of barrier `id`, and the same with an OR
+// vote across them.
+__device__ __forceinline__ void bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool bar_or(bool p, int id, int n) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred a, b;\n setp.ne.u32 a, %1, 0;\n bar.red.or.pred b, %2, %3, a;\n"
+      " selp.u32 %0, 1, 0, b;\n}\n"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -94,29 +115,48 @@ __device__ __forceinline__ float pow2_f32_nonpos(int d) {
   return d >= -149 ? __uint_as_float(1u << (d + 149)) : 0.f;
 }
 
-template <bool MX>
-__global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a) {
+template <bool MX, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(const AttnArgs a) {
   // a page's K (or V) scale bytes, and where they sit in a stage
   constexpr int kPageScaleB = MX ? kMxPageScaleBytes : kPageScaleBytes;
   constexpr int kStageB = 2 * (kPageCodeBytes + kPageScaleB);
-  __shared__ AttnSmem sm;
+  constexpr int kThreads = NW * 32;
+  constexpr int kGroups = NW / 4;   // groups of four warps, each a two-stage ring
+  extern __shared__ __align__(128) uint8_t att_smem[];
+  AttnFixed& sm = *reinterpret_cast<AttnFixed*>(att_smem);
+  uint8_t* const stage0 = att_smem + kAttFixedBytes;
+  AttnMerge<NW>& mg = *reinterpret_cast<AttnMerge<NW>*>(stage0);
   const int split = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
+  const int gi = warp >> 2;   // this warp's group
 
   if (tid == 0) {
-    mbar_init(&sm.bar[0], 1);
-    mbar_init(&sm.bar[1], 1);
+    for (int i = 0; i < 2 * kGroups; ++i) mbar_init(&sm.bar[i], 1);
     mbar_fence_init();
+    // Before the wait, bring this row's q and a share of the block table into
+    // L2: no earlier kernel of the step writes the block table, and a q line a
+    // producer writes later is updated in L2, which every read below goes through.
+    if (split == 0)
+      bulk_prefetch_l2(a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G) * kHeadDim,
+                       static_cast<uint32_t>(a.G * kHeadDim * 2));
+    const size_t tb = static_cast<size_t>(a.B) * a.bt_stride * sizeof(int32_t);
+    const size_t nctas = static_cast<size_t>(gridDim.x) * gridDim.y * gridDim.z;
+    const size_t me = blockIdx.x + static_cast<size_t>(gridDim.x) * (blockIdx.y + static_cast<size_t>(gridDim.y) * blockIdx.z);
+    const size_t chunk = ((tb + nctas - 1) / nctas + 15) & ~static_cast<size_t>(15);
+    const size_t off = me * chunk;
+    if ((reinterpret_cast<uintptr_t>(a.block_table) & 15u) == 0 && off < tb) {
+      const size_t n = min(chunk, tb - off) & ~static_cast<size_t>(15);
+      if (n > 0) bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(a.block_table) + off, static_cast<uint32_t>(n));
+    }
   }
   pdl_trigger();
   pdl_wait();
   // q fragments (A operand, heads as rows) in the permuted head-dim order:
-  // k-step j covers dims 32t+4j .. 32t+4j+3 for thread t. Their loads go out
-  // first (they do not depend on the block list) and are converted after it, so
-  // warp 0's id, length and page loads do not wait behind them.
+  // k-step j covers dims 32t+4j .. 32t+4j+3 for thread t. Warp 1 loads and
+  // converts them into shared memory while warp 0 works out the block list.
   uint2 qr[8][2];
-  {
+  if (warp == 1) {
     const int h0 = g, h1 = g + 8;
     const uint16_t* q0 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h0) * kHeadDim + 32 * t;
     const uint16_t* q1 = a.q + (static_cast<size_t>(r) * a.Hq + kvh * a.G + h1) * kHeadDim + 32 * t;
@@ -130,10 +170,12 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   // The block list of this split: warp 0 reads the ids (together with the row's
   // request and length), checks them, looks the pages up in parallel and
   // compacts the valid ones; the lane that finds block 0 or 1 starts its copy.
+  // block i of the list goes to group i mod kGroups, as that group's
+  // (i / kGroups)-th block, into the group's stage 2 group + (that & 1)
   auto issue = [&](int i, int page) {
-    const int s = i & 1;
+    const int s = 2 * (i % kGroups) + ((i / kGroups) & 1);
     const size_t rec = static_cast<size_t>(page) * a.Hkv + kvh;
-    uint8_t* dst = sm.stage[s];
+    uint8_t* dst = stage0 + s * kStageB;
     fence_proxy_async();
     mbar_expect_tx(&sm.bar[s], kStageB);
     bulk_g2s(dst, a.kc + rec * kPageCodeBytes, kPageCodeBytes, &sm.bar[s]);
@@ -178,7 +220,7 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
         const int at = n + __popc(keep & ((1u << lane) - 1u));
         sm.page[at] = page;
         sm.ntok[at] = ntok;
-        if (at < 2) issue(at, page);
+        if (at < 2 * kGroups) issue(at, page);
       }
       n += __popc(keep);
     }
@@ -187,9 +229,7 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   // Heads g and g + 8 are scaled by 2^-e before their f16 conversion (e from
   // the head's largest magnitude, over the four lanes t that hold its 128 dims)
   // and their logits by sm_scale log2(e) 2^e, which undoes it.
-  uint32_t qa[8][4];
-  float lsc0, lsc1;   // per-head logit scales (log2 units)
-  {
+  if (warp == 1) {
     unsigned m0 = 0u, m1 = 0u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -206,17 +246,17 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     const int e1 = m1 ? q_scale_exp(min(m1, kBf16InfBits - 1)) : 0;
     const QScale sc0 = q_scale(e0), sc1 = q_scale(e1);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      qa[j][0] = bf16x2_to_f16x2_scaled(qr[j][0].x, sc0);
-      qa[j][1] = bf16x2_to_f16x2_scaled(qr[j][1].x, sc1);
-      qa[j][2] = bf16x2_to_f16x2_scaled(qr[j][0].y, sc0);
-      qa[j][3] = bf16x2_to_f16x2_scaled(qr[j][1].y, sc1);
+    for (int j = 0; j < 8; ++j)
+      sm.qa[j][lane] = make_uint4(bf16x2_to_f16x2_scaled(qr[j][0].x, sc0), bf16x2_to_f16x2_scaled(qr[j][1].x, sc1),
+                                  bf16x2_to_f16x2_scaled(qr[j][0].y, sc0), bf16x2_to_f16x2_scaled(qr[j][1].y, sc1));
+    if (t == 0) {
+      sm.lsc[g] = a.scale_log2 * exp2i_f32(e0);
+      sm.lsc[g + 8] = a.scale_log2 * exp2i_f32(e1);
     }
-    lsc0 = a.scale_log2 * exp2i_f32(e0);
-    lsc1 = a.scale_log2 * exp2i_f32(e1);
   }
   __syncthreads();
   const int nblocks = sm.nblocks;
+  const float lsc0 = sm.lsc[g], lsc1 = sm.lsc[g + 8];
 
 
   float o[16][4];
@@ -227,24 +267,26 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   uint32_t vref = 0;                     // MX: this warp's V reference exponent per group (bytes)
   bool aborted = false;
 
-  for (int i = 0; i < nblocks; ++i) {
-    const int s = i & 1;
-    const bool fail = !aborted && !mbar_wait(&sm.bar[s], (i >> 1) & 1);
-    // one decision for the whole CTA before any warp-collective work
-    if (__syncthreads_or(fail) && !aborted) {
+  // this group's blocks i = gi, gi + kGroups, ... (its k-th in stage 2 gi + (k & 1))
+  for (int i = gi, k = 0; i < nblocks; i += kGroups, ++k) {
+    const int s = 2 * gi + (k & 1);
+    const uint32_t par = static_cast<uint32_t>(k >> 1) & 1u;
+    const bool fail = !aborted && !mbar_wait(&sm.bar[s], par);
+    // one decision for the whole group before any warp-collective work
+    if (bar_or(fail, 1 + gi, 128) && !aborted) {
       aborted = true;
-      if (tid == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
-      // give the copies still in flight one more bounded wait before leaving
-      mbar_wait(&sm.bar[s], (i >> 1) & 1);
-      if (i + 1 < nblocks) mbar_wait(&sm.bar[s ^ 1], ((i + 1) >> 1) & 1);
+      if ((warp & 3) == 0 && lane == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
+      // give the group's copies still in flight one more bounded wait before leaving
+      mbar_wait(&sm.bar[s], par);
+      if (i + kGroups < nblocks) mbar_wait(&sm.bar[s ^ 1], static_cast<uint32_t>((k + 1) >> 1) & 1u);
     }
     if (!aborted) {
-      const uint8_t* kcs = sm.stage[s];
+      const uint8_t* kcs = stage0 + s * kStageB;
       const uint8_t* kss = kcs + kPageCodeBytes;
       const uint8_t* vcs = kss + kPageScaleB;
       const uint8_t* vss = vcs + kPageCodeBytes;
       const int ntok = sm.ntok[i];
-      const int tb = warp * 32;  // this warp's first token in the block
+      const int tb = (warp & 3) * 32;  // this warp's first token in the block
 
       // ---- S = Q K^T for 32 tokens (4 n8 tiles) ----
       float sacc[4][4];
@@ -261,10 +303,11 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
           const uint32_t sj = pow2_neg_f16x2(em - static_cast<int>((kw4 >> (8 * t)) & 0xFFu));
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
+            const uint4 qv = sm.qa[j][lane];
             const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
             const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
             const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
-            mma16816(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+            mma16816(sacc[c], qv.x, qv.y, qv.z, qv.w, b0, b1);
           }
           // columns 2t, 2t + 1 of this tile are the tokens decoded by lanes 8t, 8t + 4
           const float fk = pow2_f32(em - 127);
@@ -279,11 +322,12 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
           const uint32_t s0 = bcast_lo(sc), s1 = bcast_hi(sc);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
+            const uint4 qv = sm.qa[j][lane];
             const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
             const uint32_t sj = j < 4 ? s0 : s1;
             const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
             const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
-            mma16816(sacc[c], qa[j][0], qa[j][1], qa[j][2], qa[j][3], b0, b1);
+            mma16816(sacc[c], qv.x, qv.y, qv.z, qv.w, b0, b1);
           }
         }
       }
@@ -404,8 +448,9 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
         }
       }
     }
-    __syncthreads();  // every warp is done with stage s
-    if (tid == 0 && !aborted && i + 2 < nblocks) issue(i + 2, sm.page[i + 2]);
+    bar_sync(1 + gi, 128);  // every warp of the group is done with stage s
+    if ((warp & 3) == 0 && lane == 0 && !aborted && i + 2 * kGroups < nblocks)
+      issue(i + 2 * kGroups, sm.page[i + 2 * kGroups]);
   }
 
   if constexpr (MX) {   // undo the V reference: this thread's accumulators are group t
@@ -423,12 +468,12 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  __syncthreads();
+  __syncthreads();   // every group is done with its stages (all copies landed)
   if (t == 0) {
-    sm.merge.m[warp][g] = m0;
-    sm.merge.m[warp][g + 8] = m1;
-    sm.merge.l[warp][g] = l0;
-    sm.merge.l[warp][g + 8] = l1;
+    mg.m[warp][g] = m0;
+    mg.m[warp][g + 8] = m1;
+    mg.l[warp][g] = l0;
+    mg.l[warp][g + 8] = l1;
   }
   // o[2jj + odd][e]: head g (e < 2) or g+8, dim 16*(2t + (e&1)) + 2jj + odd
 #pragma unroll
@@ -439,7 +484,7 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
       for (int e = 0; e < 4; ++e) {
         const int head = e < 2 ? g : g + 8;
         const int dim = 16 * (2 * t + (e & 1)) + 2 * jj + odd;
-        sm.merge.o[warp][merge_at(head, dim)] = o[2 * jj + odd][e];
+        mg.o[warp][merge_at(head, dim)] = o[2 * jj + odd][e];
       }
   __syncthreads();
 
@@ -450,23 +495,23 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
     const int head = tid;
     float M = -INFINITY;
 #pragma unroll
-    for (int wv = 0; wv < kAttWarps; ++wv) M = fmaxf(M, sm.merge.m[wv][head]);
+    for (int wv = 0; wv < NW; ++wv) M = fmaxf(M, mg.m[wv][head]);
     float L = 0.f;
 #pragma unroll
-    for (int wv = 0; wv < kAttWarps; ++wv) {
-      const float f = M == -INFINITY ? 0.f : exp2f(sm.merge.m[wv][head] - M);
-      sm.merge.f[wv][head] = f;
-      L += f * sm.merge.l[wv][head];
+    for (int wv = 0; wv < NW; ++wv) {
+      const float f = M == -INFINITY ? 0.f : exp2f(mg.m[wv][head] - M);
+      mg.f[wv][head] = f;
+      L += f * mg.l[wv][head];
     }
     sm.cta_m[head] = M;
     sm.cta_l[head] = L;
   }
   __syncthreads();
-  for (int head = 0; head < 16; ++head) {
-    const int dim = tid;   // kAttThreads == kHeadDim
+  const int dim = tid & (kHeadDim - 1);   // thread = (head half, output dim)
+  for (int head = tid >> 7; head < 16; head += kThreads / kHeadDim) {
     float O = 0.f;
 #pragma unroll
-    for (int wv = 0; wv < kAttWarps; ++wv) O += sm.merge.f[wv][head] * sm.merge.o[wv][merge_at(head, dim)];
+    for (int wv = 0; wv < NW; ++wv) O += mg.f[wv][head] * mg.o[wv][merge_at(head, dim)];
     sm.cta_o[head][dim] = O;
   }
   namespace cg = cooperative_groups;
@@ -476,11 +521,10 @@ __global__ void __launch_bounds__(kAttThreads) attention_kernel(const AttnArgs a
   if (nrank > 1) cluster.sync(); else __syncthreads();
   // rank k merges heads k, k + nrank, ...: thread = dim, every partial read
   // once through distributed shared memory, all loads independent
-  const AttnSmem* peer[8];
+  const AttnFixed* peer[8];
 #pragma unroll
   for (int rk = 0; rk < 8; ++rk) peer[rk] = rk < nrank ? cluster.map_shared_rank(&sm, rk) : &sm;
-  for (int head = rank; head < G; head += nrank) {
-    const int dim = tid;  // kAttThreads == kHeadDim
+  for (int head = rank + nrank * (tid >> 7); head < G; head += nrank * (kThreads / kHeadDim)) {
     float mr[8], lr[8], orr[8];
 #pragma unroll
     for (int rk = 0; rk < 8; ++rk) {
@@ -519,18 +563,41 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
-// Split count: enough CTAs to cover the GPU twice, at most one block per split
-// and at most 8 splits (one portable thread-block cluster per (kv head, row)).
+int sm_count_cached() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+      n = v;
+    else
+      return 148;
+  }
+  return n;
+}
+
+// Split count: enough CTAs for four per SM (the one-group CTA's residency), at
+// most one block per split and at most 8 splits (one portable thread-block
+// cluster per (kv head, row)).
 int attention_splits(int R, int Hkv, int topk, int* ips) {
   if (topk <= 0) { *ips = 0; return 1; }
   const long long ctas = static_cast<long long>(R) * Hkv;
-  long long want = ctas > 0 ? (2 * 152 + ctas - 1) / ctas : 1;
+  const long long slots = 4ll * sm_count_cached();
+  long long want = ctas > 0 ? (slots + ctas - 1) / ctas : 1;
   if (want < 1) want = 1;
   if (want > 8) want = 8;
   if (want > topk) want = topk;
   const int per = static_cast<int>((topk + want - 1) / want);
   *ips = per;
   return (topk + per - 1) / per;
+}
+
+// Dynamic shared memory of a CTA of nw warps: the fixed part, then the page
+// stages (two per group of four warps) or the merge buffers, whichever is larger.
+size_t attention_smem(int nw, bool mx) {
+  const size_t stage = 2 * (kPageCodeBytes + static_cast<size_t>(mx ? kMxPageScaleBytes : kPageScaleBytes));
+  const size_t st = static_cast<size_t>(nw / 2) * stage;
+  const size_t mrg = nw == 8 ? sizeof(AttnMerge<8>) : sizeof(AttnMerge<4>);
+  return kAttFixedBytes + (st > mrg ? st : mrg);
 }
 
 }  // namespace m3s
@@ -566,9 +633,19 @@ extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, 
   AttnArgs a{q, Hq, Hkv, Hq / Hkv, k.codes, k.scales, v.codes, v.scales, k.num_pages, block_table,
              bt_stride, row_req, row_len, topk_ids, topk, R, B,
              sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err};
-  const auto kernel = k.format == M3S_FMT_MXFP4 ? attention_kernel<true> : attention_kernel<false>;
-  if (launch_kernel(kernel, dim3(nsplit, Hkv, R), dim3(kAttThreads), 0,
-                    static_cast<cudaStream_t>(stream), nsplit, a) != cudaSuccess)
+  // two warp groups when the grid has at most one CTA per SM (each SM then
+  // computes two of its blocks at once), else one (more CTAs resident per SM)
+  const bool mx = k.format == M3S_FMT_MXFP4;
+  const bool wide = static_cast<long long>(nsplit) * Hkv * R <= sm_count_cached();
+  const int nw = wide ? 8 : 4;
+  const auto kernel = mx ? (wide ? attention_kernel<true, 8> : attention_kernel<true, 4>)
+                         : (wide ? attention_kernel<false, 8> : attention_kernel<false, 4>);
+  const size_t smem = attention_smem(nw, mx);
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+      cudaSuccess)
+    return M3S_ERR_LAUNCH;
+  if (launch_kernel(kernel, dim3(nsplit, Hkv, R), dim3(nw * 32), smem, static_cast<cudaStream_t>(stream), nsplit,
+                    a) != cudaSuccess)
     return M3S_ERR_LAUNCH;
   return M3S_OK;
 }
