@@ -47,10 +47,12 @@ def parse():
     ap.add_argument("--no-per-workload", action="store_true",
                     help="measure the headline workload only (default: all five, the others "
                          "reported under per_workload)")
-    ap.add_argument("--topk-path", choices=["call", "pair"], default="pair",
-                    help="decode rows: pair = m3s_index_block_scores then m3s_block_topk (the "
-                         "kernels m3s_index_score_topk runs for up to 256 rows, the scorer timed "
-                         "alone); call = m3s_index_score_topk itself")
+    ap.add_argument("--topk-path", choices=["fused", "call", "pair"], default="fused",
+                    help="decode rows: fused = m3s_index_attention (the scorer leaves per-CTA "
+                         "candidates, the attention merges them: two launches); call = "
+                         "m3s_index_score_topk then m3s_sparse_attention; pair = "
+                         "m3s_index_block_scores, m3s_block_topk, m3s_sparse_attention. The scorer "
+                         "and the attention are timed alone through the pair calls either way")
     ap.add_argument("--cache-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="K / V / index-K record format")
     ap.add_argument("--write-path", choices=["store", "fused", "staged"], default="store",
@@ -575,15 +577,16 @@ def measure_workload(name, args, dev, world):
     ws_a = torch.zeros(max(16, M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, R, B, bt_stride, s.hq,
                                                      s.hkv, 0, s.topk)),
                        dtype=torch.uint8, device=dev)
+    ws_ia = torch.zeros(max(16, M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, R, B, bt_stride, s.hq,
+                                                      s.hkv, s.hi, s.topk)),
+                        dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    side = torch.cuda.Stream(device=dev)
 
     def pre():
-        # the row map runs on a parallel branch beside the batched store
-        cur = torch.cuda.current_stream()
-        side.wait_stream(cur)
-        with torch.cuda.stream(side):
-            M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
+        # the row map, then the batched store, chained on the stream (each
+        # launch overlaps its predecessor's tail through the programmatic
+        # dependency; a fork / join would cost a full graph edge)
+        M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
         if write_path == "store":
             M.m3s_nvfp4_store_batch([(d["k_new"], kc, ks), (d["v_new"], vc, vs),
                                      (d["ik_new"], ic, is_)], d["slots"], err)
@@ -598,21 +601,25 @@ def measure_workload(name, args, dev, world):
             if not fused_w:
                 M.m3s_nvfp4_store_batch([(staging["k_new"], kc, ks), (staging["v_new"], vc, vs),
                                          (staging["ik_new"], ic, is_)], d["slots"], err)
-        cur.wait_stream(side)
 
     q_in = d["q"] if write_path == "store" else q_n
     qidx_in = d["q_idx"] if write_path == "store" else qidx_n
-    topk_pair = getattr(args, "topk_path", "pair") == "pair"
+    path = getattr(args, "topk_path", "fused")
 
-    def score():
-        if fused:
-            M.m3s_verify_score_topk(qidx_in, d["w"], ic, is_, bt, d["cu_q"], row_len,
-                                    max(s.q_rows), s.topk, ids, ws_v, err)
-        elif topk_pair:
-            M.m3s_index_block_scores(qidx_in, d["w"], ic, is_, bt, row_req, row_len, bscores, err)
-        else:
-            M.m3s_index_score_topk(qidx_in, d["w"], ic, is_, bt, row_req, row_len, s.topk, ids,
-                                   None, ws_i, err)
+    def score():   # the verify rows' fused score + top-k
+        M.m3s_verify_score_topk(qidx_in, d["w"], ic, is_, bt, d["cu_q"], row_len,
+                                max(s.q_rows), s.topk, ids, ws_v, err)
+
+    def score_pair():
+        M.m3s_index_block_scores(qidx_in, d["w"], ic, is_, bt, row_req, row_len, bscores, err)
+
+    def score_call():
+        M.m3s_index_score_topk(qidx_in, d["w"], ic, is_, bt, row_req, row_len, s.topk, ids,
+                               None, ws_i, err)
+
+    def index_attention():
+        M.m3s_index_attention(qidx_in, d["w"], ic, is_, q_in, s.hkv, kc, ks, vc, vs, bt, row_req,
+                              row_len, s.topk, SM_SCALE, ids, out, lse, ws_ia, err)
 
     def topk():
         M.m3s_block_topk(bscores, row_req, row_len, B, bt_stride, s.topk, ids)
@@ -622,18 +629,30 @@ def measure_workload(name, args, dev, world):
                                out, lse, ws_a, err)
 
     # eager warm-up (sets kernel attributes), then the whole step as one CUDA
-    # graph (the timed step), and the same step with event-record nodes around
-    # the scorer and around the attention (an event node between two kernels
-    # breaks their programmatic-launch overlap, so this copy times those two
-    # kernels and not the step); one graph per phase for the breakdown
-    phases = [pre, score, topk, attn] if (topk_pair and not fused) else [pre, score, attn]
+    # graph (the timed step), and the same work as separate calls with
+    # event-record nodes around the scorer and around the attention (an event
+    # node between two kernels breaks their programmatic-launch overlap, so this
+    # copy times those two kernels and not the step); one graph per separate
+    # call for the breakdown
+    if fused:
+        phases = [pre, score, attn]
+        timing, score_fn = phases, score
+    elif path == "fused":
+        phases = [pre, index_attention]
+        timing, score_fn = [pre, score_pair, topk, attn], score_pair
+    elif path == "pair":
+        phases = [pre, score_pair, topk, attn]
+        timing, score_fn = phases, score_pair
+    else:
+        phases = [pre, score_call, attn]
+        timing, score_fn = phases, score_call
     for _ in range(2):
-        for fn in phases:
+        for fn in phases + timing:
             fn()
     torch.cuda.synchronize()
     cap = torch.cuda.Stream(device=dev)
     graphs = []
-    for fn in phases:
+    for fn in timing:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
             fn()
@@ -650,20 +669,20 @@ def measure_workload(name, args, dev, world):
                 fn()
         whole_ev = torch.cuda.CUDAGraph()
         with torch.cuda.graph(whole_ev, stream=cap):
-            for fn in phases:
-                if fn is score:
+            for fn in timing:
+                if fn is score_fn:
                     sev[0].record()
                 if fn is attn:
                     sev[2].record()
                 fn()
-                if fn is score:
+                if fn is score_fn:
                     sev[1].record()
                 if fn is attn:
                     sev[3].record()
     torch.cuda.synchronize()
 
     def step(phase_events=None):
-        # phase_events: len(phases)+1 events bracketing each phase's graph
+        # phase_events: len(timing)+1 events bracketing each separate call's graph
         if whole is not None and phase_events is None:
             whole.replay()
             return
@@ -675,10 +694,17 @@ def measure_workload(name, args, dev, world):
             phase_events[-1].record(stream)
 
     # our kernels per step: store (or quantise-at-write; staged: + the store), row
-    # map, the scorer call's kernels, attention
+    # map, then the scorer call's kernels and the attention (fused: the scorer and
+    # the attention, no top-k launch)
     ntiles = B * ((max(s.q_rows) + 7) // 8) if fused else R
-    streams = (fused or not topk_pair) and ntiles > MAX_GRID
-    launches_per_step = 3 + (1 if write_path == "staged" else 0) + (1 if streams else 2)
+    streams = (fused or path == "call") and ntiles > MAX_GRID
+    pre_launches = 2 + (1 if write_path == "staged" else 0)
+    if not fused and path == "fused":
+        launches_per_step = pre_launches + 2
+    elif not fused and path == "pair":
+        launches_per_step = pre_launches + 3
+    else:
+        launches_per_step = pre_launches + (1 if streams else 2) + 1
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -719,7 +745,7 @@ def measure_workload(name, args, dev, world):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
            for _ in range(args.steps)]
     for i in range(args.steps):
         flush()
@@ -744,17 +770,17 @@ def measure_workload(name, args, dev, world):
             attn_l.append(sev[2].elapsed_time(sev[3]))
     # per-phase breakdown (one graph per phase, events between them; not the
     # headline: the graph boundaries add launch gaps the whole-step graph has not)
-    ph_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+    ph_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(timing) + 1)]
              for _ in range(args.steps)]
     for i in range(args.steps):
         flush()
         step(ph_ev[i])
     torch.cuda.synchronize()
     phase_ms = [sum(e[j].elapsed_time(e[j + 1]) for e in ph_ev) / args.steps
-                for j in range(len(phases))]
+                for j in range(len(timing))]
     if not score_l:
-        score_l = [sum(e[phases.index(score)].elapsed_time(e[phases.index(score) + 1]) for e in ph_ev) / args.steps]
-        attn_l = [phase_ms[phases.index(attn)]]
+        score_l = [phase_ms[timing.index(score_fn)]]
+        attn_l = [phase_ms[timing.index(attn)]]
     score_ms = sum(score_l) / len(score_l)
     attn_ms = sum(attn_l) / len(attn_l)
     ms, score_ms, attn_ms = max_over_ranks([ms, score_ms, attn_ms], dev)
@@ -833,9 +859,9 @@ def measure_workload(name, args, dev, world):
     psrc = (lambda nm: f"measured (MEASURED_PEAKS.json {nm})" if src == "measured" else "fallback")
     score_kernel = (("score_kernel<8> (m3s_verify_score_topk, top-k streamed inside)" if streams else
                      "score_kernel<8> + topk_kernel (m3s_verify_score_topk)") if fused else
-                    ("score_decode_kernel (m3s_index_block_scores)" if topk_pair else
-                     ("score_decode_kernel (m3s_index_score_topk, top-k streamed inside)" if streams else
-                      "score_decode_kernel + topk_kernel (m3s_index_score_topk)")))
+                    ("score_decode_kernel (m3s_index_score_topk, top-k streamed inside)" if streams else
+                     "score_decode_kernel + topk_kernel (m3s_index_score_topk)") if path == "call" else
+                    "score_decode_kernel (timed alone through m3s_index_block_scores)")
     attn_gbs = attn_bytes / (attn_ms * 1e-3) / 1e9
     return {
         "name": s.name,
@@ -867,7 +893,7 @@ def measure_workload(name, args, dev, world):
                              "copies; timed from an idle GPU, so host call overhead is included"},
         "gpu_launches": launches_per_step * args.steps,
         "step_graph": "one graph per step" if whole is not None else "one graph per phase",
-        "phases_ms_separate_graphs": {fn.__name__: round(v, 5) for fn, v in zip(phases, phase_ms)},
+        "phases_ms_separate_graphs": {fn.__name__: round(v, 5) for fn, v in zip(timing, phase_ms)},
         "clocks": clk,
         "warmup": warm,
     }

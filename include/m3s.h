@@ -110,6 +110,7 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
 #define M3S_OP_VERIFY_SCORE_TOPK 2
 #define M3S_OP_SPARSE_ATTENTION 3
 #define M3S_OP_INDEX_CANDIDATES 4
+#define M3S_OP_INDEX_ATTENTION 5
 
 /*
  * Workspace bytes an op needs (device memory the caller provides as `ws`).
@@ -387,6 +388,27 @@ int m3s_verify_score_topk(const uint16_t* q_idx, const float* w, int32_t Hi,
                           int32_t max_q, int32_t topk, int32_t init_blocks, int32_t local_blocks,
                           int32_t* topk_ids, void* ws, size_t ws_bytes, int32_t* err,
                           void* stream);
+
+/*
+ * Decode rows end to end: index scoring, top-k and block-sparse attention in
+ * two launches. #2744, Design / Index and Design / Attention: the indexer's
+ * top-k block ids of each row address the blocks the row attends over. The
+ * scorer leaves, for every row, each of its CTAs' top-k candidate keys over the
+ * blocks it scored (the key order of m3s_index_score_topk: score, ties to the
+ * lower id, forced blocks first); the attention merges a row's candidates
+ * before it reads the row's pages. topk_ids, out and lse are what
+ * m3s_index_score_topk followed by m3s_sparse_attention return (same ids, and
+ * the attention then computes the same sums in the same order).
+ * Arguments as for those two calls; topk_ids int32 [R][topk] is written.
+ * ws_bytes >= m3s_workspace_bytes(M3S_OP_INDEX_ATTENTION, ...) (no zeroing
+ * needed: every call writes what it reads). R <= 8192.
+ */
+int m3s_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_fp4_plane idx_k,
+                        const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k, m3s_fp4_plane v,
+                        const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* row_req,
+                        const int32_t* row_len, int32_t R, int32_t topk, int32_t init_blocks,
+                        int32_t local_blocks, float sm_scale, int32_t* topk_ids, uint16_t* out, float* lse,
+                        void* ws, size_t ws_bytes, int32_t* err, void* stream);
 
 /*
  * Block-sparse attention over the selected NVFP4 pages. "NVFP4 sparse KV",

@@ -24,6 +24,7 @@ STATUS = {1: "M3S_ERR_INVALID", 2: "M3S_ERR_UNSUPPORTED", 3: "M3S_ERR_WORKSPACE"
 DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_PAGE, DEVERR_ROW, DEVERR_QRANGE, DEVERR_TIMEOUT = \
     1, 2, 4, 8, 16, 32
 OP_INDEX_SCORE_TOPK, OP_VERIFY_SCORE_TOPK, OP_SPARSE_ATTENTION, OP_INDEX_CANDIDATES = 1, 2, 3, 4
+OP_INDEX_ATTENTION = 5
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 HEAD_DIM = PAGE = 128
 
@@ -79,6 +80,9 @@ _SIGS = {
     "m3s_index_score_candidates": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _P, _P, _P, _P, _I32,
                                                   _I32, _I32, _I32, _I32, _P, _P, _SZ, _P, _P]),
     "m3s_merge_candidates": (ctypes.c_int, [_P, _I32, _I32, _I32, _P, _P]),
+    "m3s_index_attention": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _I32, Plane, Plane, _P, _I32,
+                                           _I32, _P, _P, _I32, _I32, _I32, _I32, ctypes.c_float, _P, _P,
+                                           _P, _P, _SZ, _P, _P]),
     "m3s_version": (ctypes.c_char_p, []),
 }
 
@@ -367,3 +371,33 @@ def m3s_merge_candidates(cand_keys, topk_ids=None, stream=None):
     rc = load().m3s_merge_candidates(_ptr(cand_keys), n, R, topk, _ptr(topk_ids), _stream(stream))
     _check(rc, "m3s_merge_candidates")
     return topk_ids
+
+
+def m3s_index_attention(q_idx, w, idx_codes, idx_scales, q, hkv: int, k_codes, k_scales, v_codes,
+                        v_scales, block_table, row_req, row_len, topk: int, sm_scale: float,
+                        topk_ids=None, out=None, lse=None, ws=None, err=None, stream=None,
+                        init_blocks: int = 0, local_blocks: int = 0):
+    """Index scoring, top-k and attention of decode rows (two launches);
+    returns (topk_ids int32 [R, topk], out bf16 [R, Hq, 128])."""
+    _index_inputs(q_idx, w, block_table, row_req, row_len)
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise TypeError("q must be a contiguous bfloat16 tensor [R, Hq, 128]")
+    R, Hi = q_idx.shape[0], q_idx.shape[1]
+    Hq = q.shape[1]
+    B, bt_stride = block_table.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((R, topk), dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous float32 tensor [R, Hq]")
+    if ws is None:
+        nb = m3s_workspace_bytes(OP_INDEX_ATTENTION, R, B, bt_stride, Hq, hkv, Hi, topk)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    rc = load().m3s_index_attention(
+        _ptr(q_idx), _ptr(w), Hi, plane(idx_codes, idx_scales), _ptr(q), Hq, hkv, plane(k_codes, k_scales),
+        plane(v_codes, v_scales), _ptr(block_table), bt_stride, B, _ptr(row_req), _ptr(row_len), R, topk,
+        init_blocks, local_blocks, sm_scale, _ptr(topk_ids), _ptr(out), _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
+    _check(rc, "m3s_index_attention")
+    return topk_ids, out

@@ -16,6 +16,8 @@ extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_
   switch (op) {
     case M3S_OP_INDEX_CANDIDATES:   // always the streaming form
       return round16(m3s::topk_ws_bytes(R, 1, topk));
+    case M3S_OP_INDEX_ATTENTION:    // the scorer's candidate lists and each row's slot range
+      return round16(m3s::index_attention_ws_bytes(R, topk));
     case M3S_OP_INDEX_SCORE_TOPK:   // one tile per row
       return round16(m3s::score_topk_ws_bytes(R, 1, R, max_blocks, topk));
     case M3S_OP_VERIFY_SCORE_TOPK: {   // tiles of up to 8 rows of one request

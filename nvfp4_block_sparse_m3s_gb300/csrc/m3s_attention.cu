@@ -33,7 +33,7 @@
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
-#include "m3s_device.cuh"
+#include "m3s_score_common.cuh"
 
 namespace m3s {
 namespace {
@@ -56,6 +56,11 @@ struct AttnArgs {
   uint16_t* out;
   float* lse;
   int32_t* err;
+  // candidates mode (ids == nullptr): the scorer's per-CTA candidate lists and
+  // each row's (first slot, lists); the row's ids are written to ids_out
+  const unsigned long long* cand;
+  const int2* meta;
+  int32_t* ids_out;
 };
 
 // Per-warp partial outputs are stored at [head][dim + dim / 32] in rows of
@@ -82,6 +87,8 @@ struct __align__(16) AttnFixed {
   float cta_m[16];
   float cta_l[16];
   uint64_t bar[4];            // two stages per warp group
+  uint64_t cand_bar;          // candidates mode: the staging copy of the row's lists
+  int sel_id[M3S_MAX_TOPK];   // candidates mode: the row's selected ids, ascending
   int page[M3S_MAX_TOPK];
   int ntok[M3S_MAX_TOPK];
   int nblocks;
@@ -115,6 +122,45 @@ __device__ __forceinline__ float pow2_f32_nonpos(int d) {
   return d >= -149 ? __uint_as_float(1u << (d + 149)) : 0.f;
 }
 
+// Candidates mode, the whole CTA: the row's candidate lists (mt.y lists of
+// topk keys in consecutive slots from mt.x: one contiguous run) staged into buf
+// by one bulk copy (thread 0; or, when the run is not 16-byte aligned, loads by
+// every thread), then merged pairwise by all warps, level by level, into list 0
+// (the row's top-k keys, descending). Kept out of line: inlined, merge code of
+// this kind slowed the block loop of the whole kernel (measured: decode-row
+// attention 20 us against 12). Returns false (the row gets no block) when the
+// lists do not fit in buf or the copy's bounded wait runs out.
+__device__ __noinline__ bool merge_row_candidates(const AttnArgs& a, int2 mt, unsigned long long* buf,
+                                                  size_t buf_bytes, uint64_t* bar, int nthreads) {
+  const int tid = threadIdx.x;
+  const int nkeys = mt.y * a.topk;
+  const unsigned long long* src = a.cand + static_cast<size_t>(mt.x) * a.topk;
+  // (the copy may read up to 8 bytes past the run: the workspace's slot area is
+  // followed by its 256-byte padding and the row ranges)
+  const uint32_t bytes = (static_cast<uint32_t>(nkeys) * 8 + 15) & ~15u;
+  if (nkeys == 0) return true;
+  if (bytes > buf_bytes) return false;   // (more lists than the stages hold: never with the workspace's slots)
+  if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    if (tid == 0) {
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(buf, src, bytes, bar);
+    }
+    // one decision for the whole CTA (a late copy seen by some threads only)
+    if (__syncthreads_or(!mbar_wait(bar, 0))) {
+      if (tid == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
+      mbar_wait(bar, 0);
+      return false;
+    }
+  } else {
+    for (int e = tid; e < nkeys; e += nthreads) buf[e] = __ldcg(src + e);
+    __syncthreads();
+  }
+  tree_merge_lists(buf, 1, mt.y, a.topk, nthreads);   // (a CTA barrier after each level)
+  fence_proxy_async();   // bulk copies refill the stage memory read and written here
+  __syncthreads();
+  return true;
+}
+
 template <bool MX, int NW>
 __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(const AttnArgs a) {
   // a page's K (or V) scale bytes, and where they sit in a stage
@@ -133,6 +179,7 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
 
   if (tid == 0) {
     for (int i = 0; i < 2 * kGroups; ++i) mbar_init(&sm.bar[i], 1);
+    mbar_init(&sm.cand_bar, 1);
     mbar_fence_init();
     // Before the wait, bring this row's q and a share of the block table into
     // L2: no earlier kernel of the step writes the block table, and a q line a
@@ -170,6 +217,15 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
   // The block list of this split: warp 0 reads the ids (together with the row's
   // request and length), checks them, looks the pages up in parallel and
   // compacts the valid ones; the lane that finds block 0 or 1 starts its copy.
+  // Candidates mode: the whole CTA merges the row's candidate lists first.
+  const bool cands = a.cand != nullptr;
+  int2 mt = make_int2(0, 0);
+  bool cands_ok = true;
+  if (cands) {
+    mt = a.meta[r];
+    cands_ok = merge_row_candidates(a, mt, reinterpret_cast<unsigned long long*>(stage0),
+                                    static_cast<size_t>(2 * kGroups) * kStageB, &sm.cand_bar, kThreads);
+  }
   // block i of the list goes to group i mod kGroups, as that group's
   // (i / kGroups)-th block, into the group's stage 2 group + (that & 1)
   auto issue = [&](int i, int page) {
@@ -188,19 +244,46 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
   if (warp == 0) {
     __syncwarp();   // the barriers lane 0 initialised
     const int i0 = split * a.ips, i1 = min(a.topk, i0 + a.ips);
-    const int id_first = i0 + lane < i1 ? a.ids[static_cast<size_t>(r) * a.topk + i0 + lane] : -1;
+    const int id_first = !cands && i0 + lane < i1 ? a.ids[static_cast<size_t>(r) * a.topk + i0 + lane] : -1;
     const int len = a.row_len[r];
     const int req = a.row_req[r];
     const bool row_ok = req >= 0 && len > 0;
     const bool row_bad = row_ok && (req >= a.B || len > a.bt_stride * kPage);
     if (row_bad && lane == 0 && split == 0 && kvh == 0) raise(a.err, M3S_DEVERR_ROW);
     const int nb = (len + kPage - 1) / kPage;
+    if (cands) {   // the merged top-k keys: ids ranked ascending into sel_id
+      const WarpTopk sel = warp_load(reinterpret_cast<const unsigned long long*>(stage0), a.topk, lane);
+      const bool live = cands_ok && mt.y > 0;
+      const unsigned long long ka = live ? sel.a : 0ull, kb = live ? sel.b : 0ull;
+      const int ia = ka ? select_key_id(ka) : 0x7FFFFFFF;
+      const int ib = kb ? select_key_id(kb) : 0x7FFFFFFF;
+      const int cnt = __popc(__ballot_sync(0xffffffffu, ka != 0ull)) + __popc(__ballot_sync(0xffffffffu, kb != 0ull));
+      int ra = 0, rb = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int xa = __shfl_sync(0xffffffffu, ia, j);
+        const int xb = __shfl_sync(0xffffffffu, ib, j);
+        ra += (xa < ia) + (xb < ia);
+        rb += (xa < ib) + (xb < ib);
+      }
+      if (ka) sm.sel_id[ra] = ia;
+      if (kb) sm.sel_id[rb] = ib;
+      for (int i = cnt + lane; i < a.topk; i += 32) sm.sel_id[i] = -1;
+      if (split == 0 && kvh == 0 && a.ids_out) {
+        for (int i = lane; i < a.topk; i += 32) a.ids_out[static_cast<size_t>(r) * a.topk + i] = -1;
+        __syncwarp();
+        if (ka) a.ids_out[static_cast<size_t>(r) * a.topk + ra] = ia;
+        if (kb) a.ids_out[static_cast<size_t>(r) * a.topk + rb] = ib;
+      }
+      fence_proxy_async();   // the stage memory read above is refilled by bulk copies below
+      __syncwarp();
+    }
     int n = 0;
     for (int base = i0; base < i1; base += 32) {
       const int i = base + lane;
       int page = -1, ntok = 0;
       if (row_ok && !row_bad && i < i1) {
-        const int id = base == i0 ? id_first : a.ids[static_cast<size_t>(r) * a.topk + i];
+        const int id = cands ? sm.sel_id[i] : (base == i0 ? id_first : a.ids[static_cast<size_t>(r) * a.topk + i]);
         if (id >= 0) {
           if (id >= nb || id >= a.bt_stride) {
             if (kvh == 0) raise(a.err, M3S_DEVERR_BLOCK_ID);
@@ -602,13 +685,14 @@ size_t attention_smem(int nw, bool mx) {
 
 }  // namespace m3s
 
-extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k,
-                                    m3s_fp4_plane v, const int32_t* block_table,
-                                    int32_t bt_stride, int32_t B, const int32_t* row_req,
-                                    const int32_t* row_len, const int32_t* topk_ids, int32_t topk,
-                                    int32_t R, float sm_scale, uint16_t* out, float* lse, void* ws,
-                                    size_t ws_bytes, int32_t* err, void* stream) {
-  using namespace m3s;
+namespace m3s {
+
+// m3s_sparse_attention, or (topk_ids == nullptr) its candidates mode: the row's
+// top-k merged from the scorer's lists cand / meta, its ids written to ids_out.
+// The argument checks of m3s_sparse_attention (before anything is launched).
+int check_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k, m3s_fp4_plane v,
+                    const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* row_req,
+                    const int32_t* row_len, bool have_ids, int32_t topk, int32_t R, const uint16_t* out) {
   if (R < 0 || B < 0 || Hq < 1 || Hkv < 1 || topk < 0 || bt_stride < 0) return M3S_ERR_INVALID;
   if (Hq % Hkv != 0) return M3S_ERR_INVALID;
   if (Hq / Hkv > M3S_MAX_GQA || topk > M3S_MAX_TOPK) return M3S_ERR_UNSUPPORTED;
@@ -620,19 +704,28 @@ extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, 
   if (k.format != v.format) return M3S_ERR_UNSUPPORTED;   // one format per cache
   if (R == 0) return M3S_OK;
   if (R > 65535) return M3S_ERR_UNSUPPORTED;
-  if (!q || !out || !row_req || !row_len || (topk > 0 && !topk_ids)) return M3S_ERR_INVALID;
+  if (!q || !out || !row_req || !row_len || (topk > 0 && !have_ids)) return M3S_ERR_INVALID;
   if (!aligned16(q) || !aligned16(out)) return M3S_ERR_INVALID;
   if (k.num_pages > 0 && (!k.codes || !k.scales || !v.codes || !v.scales || !aligned16(k.codes) ||
                           !aligned16(k.scales) || !aligned16(v.codes) || !aligned16(v.scales)))
     return M3S_ERR_INVALID;
   if (B > 0 && (bt_stride < 1 || !block_table)) return M3S_ERR_INVALID;
+  return M3S_OK;
+}
+
+int launch_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k, m3s_fp4_plane v,
+                     const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* row_req,
+                     const int32_t* row_len, const int32_t* topk_ids, int32_t topk, int32_t R,
+                     float sm_scale, uint16_t* out, float* lse, int32_t* err, cudaStream_t stream,
+                     const unsigned long long* cand, const int2* meta, int32_t* ids_out) {
+  const int rc = check_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len,
+                                 topk_ids != nullptr || (cand && meta), topk, R, out);
+  if (rc != M3S_OK || R == 0) return rc;
   int ips = 0;
   const int nsplit = attention_splits(R, Hkv, topk, &ips);
-  (void)ws;
-  (void)ws_bytes;
   AttnArgs a{q, Hq, Hkv, Hq / Hkv, k.codes, k.scales, v.codes, v.scales, k.num_pages, block_table,
              bt_stride, row_req, row_len, topk_ids, topk, R, B,
-             sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err};
+             sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err, cand, meta, ids_out};
   // two warp groups when the grid has at most one CTA per SM (each SM then
   // computes two of its blocks at once), else one (more CTAs resident per SM)
   const bool mx = k.format == M3S_FMT_MXFP4;
@@ -644,8 +737,22 @@ extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, 
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
       cudaSuccess)
     return M3S_ERR_LAUNCH;
-  if (launch_kernel(kernel, dim3(nsplit, Hkv, R), dim3(nw * 32), smem, static_cast<cudaStream_t>(stream), nsplit,
-                    a) != cudaSuccess)
+  if (launch_kernel(kernel, dim3(nsplit, Hkv, R), dim3(nw * 32), smem, stream, nsplit, a) != cudaSuccess)
     return M3S_ERR_LAUNCH;
   return M3S_OK;
+}
+
+}  // namespace m3s
+
+extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k,
+                                    m3s_fp4_plane v, const int32_t* block_table,
+                                    int32_t bt_stride, int32_t B, const int32_t* row_req,
+                                    const int32_t* row_len, const int32_t* topk_ids, int32_t topk,
+                                    int32_t R, float sm_scale, uint16_t* out, float* lse, void* ws,
+                                    size_t ws_bytes, int32_t* err, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  return m3s::launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, topk_ids,
+                               topk, R, sm_scale, out, lse, err, static_cast<cudaStream_t>(stream),
+                               nullptr, nullptr, nullptr);
 }

@@ -950,6 +950,59 @@ extern "C" int m3s_merge_candidates(const uint64_t* cand_keys, int32_t n_lists, 
 }
 
 // ---------------------------------------------------------------------------
+// Decode rows end to end in two launches: the scorer leaves each CTA's top-k
+// candidates of every row it scores (and each row's slot range); the
+// attention merges a row's candidates before it reads its pages.
+// ---------------------------------------------------------------------------
+namespace m3s {
+int check_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k, m3s_fp4_plane v,
+                    const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* row_req,
+                    const int32_t* row_len, bool have_ids, int32_t topk, int32_t R, const uint16_t* out);
+int launch_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k, m3s_fp4_plane v,
+                     const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* row_req,
+                     const int32_t* row_len, const int32_t* topk_ids, int32_t topk, int32_t R,
+                     float sm_scale, uint16_t* out, float* lse, int32_t* err, cudaStream_t stream,
+                     const unsigned long long* cand, const int2* meta, int32_t* ids_out);
+}  // namespace m3s
+
+extern "C" int m3s_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_fp4_plane idx_k,
+                                   const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k,
+                                   m3s_fp4_plane v, const int32_t* block_table, int32_t bt_stride,
+                                   int32_t B, const int32_t* row_req, const int32_t* row_len, int32_t R,
+                                   int32_t topk, int32_t init_blocks, int32_t local_blocks, float sm_scale,
+                                   int32_t* topk_ids, uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                                   int32_t* err, void* stream) {
+  using namespace m3s;
+  int32_t no_ids = 0;   // (top-k 0 writes no id)
+  int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk > 0 ? topk_ids : &no_ids);
+  if (rc != M3S_OK) return rc;
+  rc = check_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, true, topk, R, out);
+  if (rc != M3S_OK || R == 0) return rc;
+  if (!row_req || !row_len || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
+  if (R > kMaxTiles) return M3S_ERR_UNSUPPORTED;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (topk == 0)   // nothing selected: every row attends over no token
+    return launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, topk_ids, 0, R,
+                            sm_scale, out, lse, err, st, nullptr, nullptr, nullptr);
+  if (ws_bytes < m3s_workspace_bytes(M3S_OP_INDEX_ATTENTION, R, B, bt_stride, Hq, Hkv, Hi, topk, 1))
+    return M3S_ERR_WORKSPACE;
+  if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
+  ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
+              row_req, nullptr, row_len, R, B, R, 1, nullptr, bt_stride > 0 ? bt_stride : 1, err,
+              idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.cand = reinterpret_cast<unsigned long long*>(base);
+  a.meta = reinterpret_cast<int2*>(base + index_attention_meta_offset(R, topk));
+  a.topk = topk;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  rc = launch_score_decode(a, st);
+  if (rc != M3S_OK) return rc;
+  return launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, nullptr, topk, R,
+                          sm_scale, out, lse, err, st, a.cand, a.meta, topk_ids);
+}
+
+// ---------------------------------------------------------------------------
 // m3s_index_score_topk_static: m3s_index_score_topk with its block-score
 // scratch in a file-scope device array instead of a caller workspace.
 //

@@ -39,6 +39,7 @@ struct ScoreArgs {
   const int32_t* blk_base;    // per request: the request's id of the call's block 0 (or nullptr)
   const int32_t* blk_count;   // per request: blocks of the call's slice (with blk_base)
   float* seg_scores;          // verify path: per CTA, [QT][bt_stride] block maxima of its segment
+  int2* meta;                 // partials mode (no merge here): per tile (first slot, lists), or nullptr
 };
 
 template <int QT>
@@ -92,12 +93,13 @@ __device__ TileInfo<QT> tile_info(const ScoreArgs& a, int t, bool report) {
 // A tile with blocks costs c set-up units plus one per block in the work split;
 // an empty tile costs nothing.
 struct TileLayout {
-  long long* bnd;   // bnd[k] = floor(C k / grid): CTA k's first cost position (k <= grid)
+  long long* bnd;   // bnd[k] = floor(C k / g): CTA k's first cost position (k <= g; C beyond)
   int* pre;
   unsigned* nz;
   int* nzc;
   int ntiles;
   int c;
+  int g;   // the CTAs the cost is cut over: min(grid, C), so each has at least one unit
   static constexpr size_t bytes(int ntiles) {
     return static_cast<size_t>(kMaxGrid + 1) * 8 + static_cast<size_t>(ntiles + 1) * 4 +
            2 * static_cast<size_t>((ntiles + 32) / 32) * 4;
@@ -208,7 +210,8 @@ __device__ __forceinline__ void tile_prefix(const ScoreArgs& a, TileLayout& L, i
   }
   __syncthreads();
   const long long C = L.total_cost();
-  for (int k = tid; k <= static_cast<int>(gridDim.x); k += nthreads) L.bnd[k] = C * k / gridDim.x;
+  L.g = static_cast<int>(min(static_cast<long long>(gridDim.x), max(C, 1ll)));
+  for (int k = tid; k <= static_cast<int>(gridDim.x); k += nthreads) L.bnd[k] = k <= L.g ? C * k / L.g : C;
   __syncthreads();
 }
 
@@ -504,11 +507,12 @@ __device__ void write_unscored_rows(const ScoreArgs& a, const TileLayout& L, int
   auto blank = [&](int r) {
     for (int i = tid; i < a.topk; i += nthreads) {
       if (a.ids) a.ids[static_cast<size_t>(r) * a.topk + i] = -1;
-      else a.keys_out[static_cast<size_t>(r) * a.topk + i] = 0ull;
+      else if (a.keys_out) a.keys_out[static_cast<size_t>(r) * a.topk + i] = 0ull;
     }
   };
   for (int t = blockIdx.x; t < L.ntiles; t += G) {
     if (L.blocks(t) != 0) continue;
+    if (a.meta && tid == 0) a.meta[t] = make_int2(0, 0);   // no candidate lists
     const int2 rows = tile_rows<QT>(a, t);
     for (int r = rows.x; r < rows.x + rows.y; ++r) blank(r);
   }
@@ -540,7 +544,7 @@ template <int QT>
 __device__ void tile_finish(const ScoreArgs& a, const TileLayout& L, int t, int seg_blocks,
                             unsigned long long* buf, int buf_keys, int* vslot, int* cnt, int nthreads) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
-  const int G = gridDim.x, kc = a.topk;
+  const int G = L.g, kc = a.topk;
   // thread 0's ticket addition is in flight while the CTA works out which CTAs
   // hold blocks of the tile (all the merge needs; unused unless this CTA merges)
   unsigned old = 0u;
@@ -626,6 +630,15 @@ __host__ __device__ constexpr size_t topk_ws_bytes(int ntiles, int qt, int topk,
 // Measured on the decode batches (1-8 rows) and the 16 x 8 verify batch, the
 // two-launch form was the faster one; on the 8192-row prefill chunk (1024
 // tiles), streaming.
+// m3s_index_attention's workspace: candidate lists for R + kMaxGrid - 1 slots
+// of topk keys, then each row's (first slot, lists).
+__host__ __device__ constexpr size_t index_attention_meta_offset(int R, int topk) {
+  return (static_cast<size_t>(R + kMaxGrid - 1) * topk * 8 + 255) & ~static_cast<size_t>(255);
+}
+__host__ __device__ constexpr size_t index_attention_ws_bytes(int R, int topk) {
+  return index_attention_meta_offset(R, topk) + static_cast<size_t>(R) * 8;
+}
+
 __host__ __device__ constexpr bool topk_streams(long long ntiles) { return ntiles > kMaxGrid; }
 
 // Workspace bytes of a score + top-k call: the streaming state, or the block

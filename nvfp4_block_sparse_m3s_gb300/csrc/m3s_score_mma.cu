@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
   // ends with a few CTAs merging candidates, so those signal only when their
   // blocks are scored (early waiting CTAs of the next kernel were measured to
   // slow the step down).
-  if (!a.cand) pdl_trigger();
+  const bool late = a.cand && !a.meta;   // the grid ends merging candidates
+  if (!late) pdl_trigger();
   pdl_wait();
 
   tile_prefix<1>(a, L, red, kThreads);
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
   const int2 range = L.cta_range(blockIdx.x);
   const int lo = range.x, hi = range.y;
   int tile = tile_at(pre, ntiles, lo);
-  if (a.cand && lo >= hi) pdl_trigger();   // no blocks
+  if (late && lo >= hi) pdl_trigger();   // no blocks
 
   uint32_t phase_bits = 0;  // per-stage mbarrier parity of this warp
   bool aborted = false;
@@ -125,6 +126,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
     const int seg_lo = pos - pre[tile];
     const int seg_hi = min(hi, pre[tile + 1]) - pre[tile];
     const TileInfo<1> ti = tile_info<1>(a, tile, false);
+    if (a.meta && seg_lo == 0 && tid == 0) {   // this CTA holds the tile's first block
+      const int2 cc = L.covering_ctas(tile, L.g);
+      a.meta[tile] = make_int2(tile + cc.x, cc.y - cc.x + 1);   // its lists: consecutive slots
+    }
 
     // ---- the row's queries (one fragment word per thread), weights and length:
     // the loads go out first, so their round trip overlaps the block-table
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
       __syncwarp();
       if (hh + 2 < nhalf) issue(hh + 2);
     }
-    if (a.cand && pre[tile] + seg_hi >= hi) pdl_trigger();   // this CTA's blocks are scored
+    if (late && pre[tile] + seg_hi >= hi) pdl_trigger();   // this CTA's blocks are scored
     if (a.cand) {
       // the segment's candidates: the 16 warps' lists merged by warp 0 into
       // slot tile + CTA; then the tile's ticket (the last CTA merges the tile)
@@ -386,8 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
       }
       if (warp == 0) write_keys(list, a.topk, a.cand + static_cast<size_t>(tile + blockIdx.x) * a.topk, lane);
       __syncthreads();
-      tile_finish<1>(a, L, tile, seg_hi - seg_lo, reinterpret_cast<unsigned long long*>(&sm.stage[0][0][0]),
-                     static_cast<int>(sizeof(sm.stage) / 8), sm.vslot, &sm.fin, kThreads);
+      if (!a.meta)
+        tile_finish<1>(a, L, tile, seg_hi - seg_lo, reinterpret_cast<unsigned long long*>(&sm.stage[0][0][0]),
+                       static_cast<int>(sizeof(sm.stage) / 8), sm.vslot, &sm.fin, kThreads);
     }
     pos = pre[tile] + seg_hi;
     ++tile;
