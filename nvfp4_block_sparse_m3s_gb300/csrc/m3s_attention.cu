@@ -61,6 +61,7 @@ struct AttnArgs {
   const unsigned long long* cand;
   const int2* meta;
   int32_t* ids_out;
+  int nslots;   // candidate slots in cand
 };
 
 // Per-warp partial outputs are stored at [head][dim + dim / 32] in rows of
@@ -89,6 +90,8 @@ struct __align__(16) AttnFixed {
   uint64_t bar[4];            // two stages per warp group
   uint64_t cand_bar;          // candidates mode: the staging copy of the row's lists
   int sel_id[M3S_MAX_TOPK];   // candidates mode: the row's selected ids, ascending
+  unsigned long long sel_tau; // candidates mode: the selection's lower bound
+  int sel_n;                  // ... and its candidate count
   int page[M3S_MAX_TOPK];
   int ntok[M3S_MAX_TOPK];
   int nblocks;
@@ -122,43 +125,125 @@ __device__ __forceinline__ float pow2_f32_nonpos(int d) {
   return d >= -149 ? __uint_as_float(1u << (d + 149)) : 0.f;
 }
 
-// Candidates mode, the whole CTA: the row's candidate lists (mt.y lists of
-// topk keys in consecutive slots from mt.x: one contiguous run) staged into buf
-// by one bulk copy (thread 0; or, when the run is not 16-byte aligned, loads by
-// every thread), then merged pairwise by all warps, level by level, into list 0
-// (the row's top-k keys, descending). Kept out of line: inlined, merge code of
-// this kind slowed the block loop of the whole kernel (measured: decode-row
-// attention 20 us against 12). Returns false (the row gets no block) when the
-// lists do not fit in buf or the copy's bounded wait runs out.
-__device__ __noinline__ bool merge_row_candidates(const AttnArgs& a, int2 mt, unsigned long long* buf,
-                                                  size_t buf_bytes, uint64_t* bar, int nthreads) {
-  const int tid = threadIdx.x;
-  const int nkeys = mt.y * a.topk;
-  const unsigned long long* src = a.cand + static_cast<size_t>(mt.x) * a.topk;
+// Candidates mode, the whole CTA: the row's top-k from its candidate lists
+// (mt.y lists of topk keys, each descending, in consecutive slots from mt.x:
+// one contiguous run), its ids ranked ascending into sel_id (-1 padded); split 0
+// of the first KV head also writes them to ids_out. The run is staged into buf
+// by one bulk copy (thread 0; loads by every thread when it is not 16-byte
+// aligned). Selection by counting, in three CTA-wide passes: the k-th largest
+// list head is a lower bound for the row's k-th key (the k largest heads are
+// k keys at least that large), so only keys at or above it (at most k lists'
+// worth) are candidates; each candidate's rank is the number of larger ones,
+// and the k best land at their ranks. (More than kSelCap candidates: a
+// pairwise merge of all lists instead.) Kept out of line: inlined, merge code
+// of this kind slowed the block loop of the whole kernel (measured: decode-row
+// attention 20 us against 12). Returns false when the copy's bounded wait runs
+// out (the row then gets no block).
+constexpr int kSelCap = 512;
+__device__ __noinline__ bool select_row_candidates(const AttnArgs& a, int2 mt, int r, int split, int kvh,
+                                                   unsigned long long* buf, size_t buf_bytes, uint64_t* bar,
+                                                   int nthreads, int* sel_id, unsigned long long* tau_s,
+                                                   int* n_s) {
+  const int tid = threadIdx.x, k = a.topk;
+  // a range outside the slots is reported and skipped (the scorer writes every
+  // row's range each call; this guards against a stale or foreign workspace)
+  if (mt.x < 0 || mt.y < 0 || mt.y > a.nslots || mt.x > a.nslots - mt.y) {
+    if (tid == 0) raise(a.err, M3S_DEVERR_ROW);
+    mt = make_int2(0, 0);
+  }
+  const int nl = mt.y;
+  const int nkeys = nl * k;
+  const unsigned long long* src = a.cand + static_cast<size_t>(mt.x) * k;
   // (the copy may read up to 8 bytes past the run: the workspace's slot area is
   // followed by its 256-byte padding and the row ranges)
   const uint32_t bytes = (static_cast<uint32_t>(nkeys) * 8 + 15) & ~15u;
-  if (nkeys == 0) return true;
-  if (bytes > buf_bytes) return false;   // (more lists than the stages hold: never with the workspace's slots)
-  if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+  unsigned long long* cand = buf + ((nkeys + 1) & ~1);   // kSelCap candidates
+  unsigned long long* top = cand + kSelCap;              // the k best, descending
+  bool ok = static_cast<size_t>(bytes) + (kSelCap + M3S_MAX_TOPK) * 8 + M3S_MAX_TOPK * 4 <= buf_bytes;
+  if (ok && nkeys > 0) {
+    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+      if (tid == 0) {
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s(buf, src, bytes, bar);
+      }
+      // one decision for the whole CTA (a late copy seen by some threads only)
+      if (__syncthreads_or(!mbar_wait(bar, 0))) {
+        if (tid == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
+        mbar_wait(bar, 0);
+        ok = false;
+      }
+    } else {
+      for (int e = tid; e < nkeys; e += nthreads) buf[e] = __ldcg(src + e);
+      __syncthreads();
+    }
+  }
+  int nsel = 0;   // keys selected (<= k)
+  if (ok && nkeys > 0) {
+    // the lower bound: the k-th largest head (every nonzero key when fewer lists)
     if (tid == 0) {
-      mbar_expect_tx(bar, bytes);
-      bulk_g2s(buf, src, bytes, bar);
+      *tau_s = 1ull;
+      *n_s = 0;
     }
-    // one decision for the whole CTA (a late copy seen by some threads only)
-    if (__syncthreads_or(!mbar_wait(bar, 0))) {
-      if (tid == 0) raise(a.err, M3S_DEVERR_TIMEOUT);
-      mbar_wait(bar, 0);
-      return false;
+    __syncthreads();
+    if (nl >= k) {
+      for (int j = tid; j < nl; j += nthreads) {
+        const unsigned long long h = buf[j * k];
+        int rank = 0;
+#pragma unroll 8
+        for (int i = 0; i < nl; ++i) rank += buf[i * k] > h;
+        if (rank == k - 1) *tau_s = h > 1ull ? h : 1ull;   // (zero heads: empty lists)
+      }
+      __syncthreads();
     }
-  } else {
-    for (int e = tid; e < nkeys; e += nthreads) buf[e] = __ldcg(src + e);
+    const unsigned long long tau = *tau_s;
+    for (int e = tid; e < nkeys; e += nthreads) {
+      const unsigned long long x = buf[e];
+      if (x >= tau) {
+        const int s = atomicAdd(n_s, 1);
+        if (s < kSelCap) cand[s] = x;
+      }
+    }
+    __syncthreads();
+    const int m = *n_s;
+    for (int i = tid; i < k; i += nthreads) top[i] = 0ull;   // (an unfilled place: no id)
+    __syncthreads();
+    if (m <= kSelCap) {
+      for (int c = tid; c < m; c += nthreads) {
+        const unsigned long long x = cand[c];
+        int rank = 0;
+#pragma unroll 8
+        for (int i = 0; i < m; ++i) rank += cand[i] > x;
+        if (rank < k) top[rank] = x;
+      }
+      nsel = min(m, k);
+    } else {   // (many equal-looking lists: merge them all)
+      tree_merge_lists(buf, 1, nl, k, nthreads);
+      for (int i = tid; i < k; i += nthreads) top[i] = buf[i];
+      nsel = k;
+    }
     __syncthreads();
   }
-  tree_merge_lists(buf, 1, mt.y, a.topk, nthreads);   // (a CTA barrier after each level)
+  // the ids, ascending (rank of each selected id among them)
+  int* top_id = reinterpret_cast<int*>(top + M3S_MAX_TOPK);
+  if (tid < nsel) top_id[tid] = top[tid] ? select_key_id(top[tid]) : -1;
+  __syncthreads();
+  if (tid < k) {
+    int id = -1, rank = tid;
+    if (tid < nsel && top_id[tid] >= 0) {
+      id = top_id[tid];
+      rank = 0;
+#pragma unroll 8
+      for (int i = 0; i < nsel; ++i) rank += top_id[i] >= 0 && top_id[i] < id;
+    } else if (tid < nsel) {   // (unfilled: after the filled ones)
+      rank = 0;
+      for (int i = 0; i < nsel; ++i) rank += top_id[i] >= 0 || i < tid;
+    }
+    sel_id[rank] = id;
+    if (split == 0 && kvh == 0 && a.ids_out) a.ids_out[static_cast<size_t>(r) * k + rank] = id;
+  }
   fence_proxy_async();   // bulk copies refill the stage memory read and written here
   __syncthreads();
-  return true;
+  return ok;
 }
 
 template <bool MX, int NW>
@@ -217,15 +302,12 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
   // The block list of this split: warp 0 reads the ids (together with the row's
   // request and length), checks them, looks the pages up in parallel and
   // compacts the valid ones; the lane that finds block 0 or 1 starts its copy.
-  // Candidates mode: the whole CTA merges the row's candidate lists first.
+  // Candidates mode: the whole CTA selects the row's top-k first.
   const bool cands = a.cand != nullptr;
-  int2 mt = make_int2(0, 0);
-  bool cands_ok = true;
-  if (cands) {
-    mt = a.meta[r];
-    cands_ok = merge_row_candidates(a, mt, reinterpret_cast<unsigned long long*>(stage0),
-                                    static_cast<size_t>(2 * kGroups) * kStageB, &sm.cand_bar, kThreads);
-  }
+  if (cands)
+    select_row_candidates(a, a.meta[r], r, split, kvh, reinterpret_cast<unsigned long long*>(stage0),
+                          static_cast<size_t>(2 * kGroups) * kStageB, &sm.cand_bar, kThreads, sm.sel_id,
+                          &sm.sel_tau, &sm.sel_n);
   // block i of the list goes to group i mod kGroups, as that group's
   // (i / kGroups)-th block, into the group's stage 2 group + (that & 1)
   auto issue = [&](int i, int page) {
@@ -251,33 +333,6 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
     const bool row_bad = row_ok && (req >= a.B || len > a.bt_stride * kPage);
     if (row_bad && lane == 0 && split == 0 && kvh == 0) raise(a.err, M3S_DEVERR_ROW);
     const int nb = (len + kPage - 1) / kPage;
-    if (cands) {   // the merged top-k keys: ids ranked ascending into sel_id
-      const WarpTopk sel = warp_load(reinterpret_cast<const unsigned long long*>(stage0), a.topk, lane);
-      const bool live = cands_ok && mt.y > 0;
-      const unsigned long long ka = live ? sel.a : 0ull, kb = live ? sel.b : 0ull;
-      const int ia = ka ? select_key_id(ka) : 0x7FFFFFFF;
-      const int ib = kb ? select_key_id(kb) : 0x7FFFFFFF;
-      const int cnt = __popc(__ballot_sync(0xffffffffu, ka != 0ull)) + __popc(__ballot_sync(0xffffffffu, kb != 0ull));
-      int ra = 0, rb = 0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int xa = __shfl_sync(0xffffffffu, ia, j);
-        const int xb = __shfl_sync(0xffffffffu, ib, j);
-        ra += (xa < ia) + (xb < ia);
-        rb += (xa < ib) + (xb < ib);
-      }
-      if (ka) sm.sel_id[ra] = ia;
-      if (kb) sm.sel_id[rb] = ib;
-      for (int i = cnt + lane; i < a.topk; i += 32) sm.sel_id[i] = -1;
-      if (split == 0 && kvh == 0 && a.ids_out) {
-        for (int i = lane; i < a.topk; i += 32) a.ids_out[static_cast<size_t>(r) * a.topk + i] = -1;
-        __syncwarp();
-        if (ka) a.ids_out[static_cast<size_t>(r) * a.topk + ra] = ia;
-        if (kb) a.ids_out[static_cast<size_t>(r) * a.topk + rb] = ib;
-      }
-      fence_proxy_async();   // the stage memory read above is refilled by bulk copies below
-      __syncwarp();
-    }
     int n = 0;
     for (int base = i0; base < i1; base += 32) {
       const int i = base + lane;
@@ -725,7 +780,8 @@ int launch_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k
   const int nsplit = attention_splits(R, Hkv, topk, &ips);
   AttnArgs a{q, Hq, Hkv, Hq / Hkv, k.codes, k.scales, v.codes, v.scales, k.num_pages, block_table,
              bt_stride, row_req, row_len, topk_ids, topk, R, B,
-             sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err, cand, meta, ids_out};
+             sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err, cand, meta, ids_out,
+             R + kMaxGrid - 1};
   // two warp groups when the grid has at most one CTA per SM (each SM then
   // computes two of its blocks at once), else one (more CTAs resident per SM)
   const bool mx = k.format == M3S_FMT_MXFP4;
