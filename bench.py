@@ -583,14 +583,15 @@ def measure_workload(name, args, dev, world):
     stream = torch.cuda.current_stream()
 
     def pre():
-        # the row map, then the batched store, chained on the stream (each
-        # launch overlaps its predecessor's tail through the programmatic
-        # dependency; a fork / join would cost a full graph edge)
-        M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
+        # the step's writes and its row map: the batched store with the row map
+        # in the same launch, or the row map chained before the quantise-at-write
+        # (a fork / join on two streams would cost a full graph edge)
         if write_path == "store":
-            M.m3s_nvfp4_store_batch([(d["k_new"], kc, ks), (d["v_new"], vc, vs),
-                                     (d["ik_new"], ic, is_)], d["slots"], err)
+            M.m3s_nvfp4_store_batch_rows([(d["k_new"], kc, ks), (d["v_new"], vc, vs),
+                                          (d["ik_new"], ic, is_)], d["slots"], d["cu_q"], d["seq_len"], R,
+                                         row_req, row_len, err)
         else:
+            M.m3s_decode_rows(d["cu_q"], d["seq_len"], R, row_req, row_len)
             fused_w = write_path == "fused"
             dst = {"k_new": (kc, ks), "v_new": (vc, vs), "ik_new": (ic, is_)} if fused_w else staging
             M.m3s_qk_norm_rope_store(
@@ -698,7 +699,7 @@ def measure_workload(name, args, dev, world):
     # the attention, no top-k launch)
     ntiles = B * ((max(s.q_rows) + 7) // 8) if fused else R
     streams = (fused or path == "call") and ntiles > MAX_GRID
-    pre_launches = 2 + (1 if write_path == "staged" else 0)
+    pre_launches = {"store": 1, "fused": 2, "staged": 3}[write_path]
     if not fused and path == "fused":
         launches_per_step = pre_launches + 2
     elif not fused and path == "pair":

@@ -181,6 +181,19 @@ int m3s_nvfp4_store_batch(const m3s_store_job* jobs, int32_t njobs, int32_t T,
                           const int64_t* slot_mapping, int32_t* err, void* stream);
 
 /*
+ * m3s_nvfp4_store_batch and m3s_decode_rows in one launch: the step's writes
+ * and its row map (#2744, Design / Attention: the row map is computed on
+ * device; #2746, Summary: the step's K/V rows are quantised into the pages).
+ * The store arguments as for m3s_nvfp4_store_batch (T == 0 or njobs == 0:
+ * the row map alone), the row-map arguments and outputs as for
+ * m3s_decode_rows (R == 0: the store alone). Same results as the two calls.
+ */
+int m3s_nvfp4_store_batch_rows(const m3s_store_job* jobs, int32_t njobs, int32_t T,
+                               const int64_t* slot_mapping, const int32_t* cu_q, const int32_t* seq_len,
+                               int32_t B, int32_t R, int32_t* row_req, int32_t* row_len, int32_t* err,
+                               void* stream);
+
+/*
  * Quantise-at-write. #2744, Follow-up: MXFP4 caches -- the quantisation moves
  * into the kernel that normalises and rotates the step's rows and writes the
  * cache, so there is no BF16 staging buffer and no separate store launch (the

@@ -83,6 +83,8 @@ _SIGS = {
     "m3s_index_attention": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _I32, Plane, Plane, _P, _I32,
                                            _I32, _P, _P, _I32, _I32, _I32, _I32, ctypes.c_float, _P, _P,
                                            _P, _P, _SZ, _P, _P]),
+    "m3s_nvfp4_store_batch_rows": (ctypes.c_int, [ctypes.c_void_p, _I32, _I32, _P, _P, _P, _I32, _I32, _P,
+                                                  _P, _P, _P]),
     "m3s_version": (ctypes.c_char_p, []),
 }
 
@@ -171,6 +173,31 @@ def m3s_nvfp4_store_batch(jobs, slot_mapping: torch.Tensor, err: torch.Tensor | 
     rc = load().m3s_nvfp4_store_batch(arr, len(jobs), T, _ptr(slot_mapping), _ptr(err),
                                       _stream(stream))
     _check(rc, "m3s_nvfp4_store_batch")
+
+
+def m3s_nvfp4_store_batch_rows(jobs, slot_mapping: torch.Tensor, cu_q: torch.Tensor, seq_len: torch.Tensor,
+                               R: int, row_req=None, row_len=None, err=None, stream=None):
+    """m3s_nvfp4_store_batch and m3s_decode_rows in one launch; returns (row_req, row_len)."""
+    assert slot_mapping.dtype == torch.int64
+    arr = (StoreJob * max(1, len(jobs)))()
+    T = slot_mapping.shape[0]
+    for i, (src, codes, scales) in enumerate(jobs):
+        assert src.dtype == torch.bfloat16 and src.dim() == 3 and src.shape[0] == T
+        assert src.stride(2) == 1 and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
+        arr[i] = StoreJob(src.data_ptr(), src.stride(0), src.shape[1], plane(codes, scales))
+    for t in (cu_q, seq_len):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError("cu_q and seq_len must be contiguous int32 tensors")
+    dev = cu_q.device
+    if row_req is None:
+        row_req = torch.empty(R, dtype=torch.int32, device=dev)
+    if row_len is None:
+        row_len = torch.empty(R, dtype=torch.int32, device=dev)
+    rc = load().m3s_nvfp4_store_batch_rows(arr, len(jobs), T, _ptr(slot_mapping), _ptr(cu_q), _ptr(seq_len),
+                                           seq_len.shape[0], R, _ptr(row_req), _ptr(row_len), _ptr(err),
+                                           _stream(stream))
+    _check(rc, "m3s_nvfp4_store_batch_rows")
+    return row_req, row_len
 
 
 def m3s_qk_norm_rope_store(jobs, slot_mapping, rope_cos=None, rope_sin=None, rotary_dim: int = 0,

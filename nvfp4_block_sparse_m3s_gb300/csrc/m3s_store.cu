@@ -84,13 +84,43 @@ struct StoreJob {
 
 struct StoreBatch {
   StoreJob job[M3S_MAX_STORE_JOBS];
+  // the row map in the same launch (grid row njobs), or rows_job = -1
+  int rows_job;
+  const int32_t* cu_q;
+  const int32_t* seq_len;
+  int32_t B, R;
+  int32_t* row_req;
+  int32_t* row_len;
 };
+
+// Row r's request and causal length (m3s_decode_rows): a binary search over cu_q.
+__device__ __forceinline__ void row_of(const int32_t* __restrict__ cu_q, const int32_t* __restrict__ seq_len,
+                                      int32_t B, int r, int32_t* req_out, int32_t* len_out) {
+  int32_t req = -1, len = 0;
+  if (B > 0 && r < cu_q[B]) {
+    int lo = 0, hi = B;  // cu_q[lo] <= r < cu_q[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (cu_q[mid] <= r) lo = mid; else hi = mid;
+    }
+    const int qb = cu_q[lo + 1] - cu_q[lo];
+    req = lo;
+    len = seq_len[lo] - qb + (r - cu_q[lo]) + 1;
+  }
+  *req_out = req;
+  *len_out = len;
+}
 
 __global__ void __launch_bounds__(256) nvfp4_store_kernel(const StoreBatch batch,
                                                          const int64_t* __restrict__ slots,
                                                          int32_t* err) {
   pdl_trigger();
   pdl_wait();
+  if (static_cast<int>(blockIdx.y) == batch.rows_job) {   // the row map's grid row
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < batch.R) row_of(batch.cu_q, batch.seq_len, batch.B, r, &batch.row_req[r], &batch.row_len[r]);
+    return;
+  }
   const StoreJob& jb = batch.job[blockIdx.y];
   const uint16_t* __restrict__ src = jb.src;
   const int64_t stride = jb.stride;
@@ -326,19 +356,7 @@ __global__ void decode_rows_kernel(const int32_t* __restrict__ cu_q,
   pdl_wait();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
-  int32_t req = -1, len = 0;
-  if (B > 0 && r < cu_q[B]) {
-    int lo = 0, hi = B;  // cu_q[lo] <= r < cu_q[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (cu_q[mid] <= r) lo = mid; else hi = mid;
-    }
-    const int qb = cu_q[lo + 1] - cu_q[lo];
-    req = lo;
-    len = seq_len[lo] - qb + (r - cu_q[lo]) + 1;
-  }
-  row_req[r] = req;
-  row_len[r] = len;
+  row_of(cu_q, seq_len, B, r, &row_req[r], &row_len[r]);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -358,8 +376,11 @@ int check_job(const uint16_t* src, int64_t stride, int32_t H, const m3s_fp4_plan
 }
 
 int launch_store(const m3s_store_job* jobs, int32_t njobs, int32_t T, const int64_t* slots,
-                 int32_t* err, cudaStream_t st) {
+                 int32_t* err, cudaStream_t st, const int32_t* cu_q = nullptr,
+                 const int32_t* seq_len = nullptr, int32_t B = 0, int32_t R = 0,
+                 int32_t* row_req = nullptr, int32_t* row_len = nullptr) {
   StoreBatch b{};
+  b.rows_job = -1;
   int64_t most = 0;
   for (int i = 0; i < njobs; ++i) {
     const m3s_store_job& j = jobs[i];
@@ -368,9 +389,21 @@ int launch_store(const m3s_store_job* jobs, int32_t njobs, int32_t T, const int6
                         static_cast<int64_t>(j.dst.num_pages) * kPage};
     most = b.job[i].total_threads > most ? b.job[i].total_threads : most;
   }
-  const int64_t blocks = (most + 255) / 256;
+  int64_t blocks = (most + 255) / 256;
+  int rows = njobs;
+  if (R > 0) {   // the row map as one more grid row
+    b.rows_job = njobs;
+    b.cu_q = cu_q;
+    b.seq_len = seq_len;
+    b.B = B;
+    b.R = R;
+    b.row_req = row_req;
+    b.row_len = row_len;
+    blocks = blocks > (R + 255) / 256 ? blocks : (R + 255) / 256;
+    ++rows;
+  }
   if (blocks > 0x7FFFFFFF) return M3S_ERR_UNSUPPORTED;
-  return launch_kernel(nvfp4_store_kernel, dim3(static_cast<unsigned>(blocks), njobs), dim3(256), 0,
+  return launch_kernel(nvfp4_store_kernel, dim3(static_cast<unsigned>(blocks), rows), dim3(256), 0,
                        st, 0, b, slots, err) == cudaSuccess
              ? M3S_OK
              : M3S_ERR_LAUNCH;
@@ -402,6 +435,27 @@ extern "C" int m3s_nvfp4_store_batch(const m3s_store_job* jobs, int32_t njobs, i
     if (rc != M3S_OK) return rc;
   }
   return launch_store(jobs, njobs, T, slot_mapping, err, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int m3s_nvfp4_store_batch_rows(const m3s_store_job* jobs, int32_t njobs, int32_t T,
+                                          const int64_t* slot_mapping, const int32_t* cu_q,
+                                          const int32_t* seq_len, int32_t B, int32_t R, int32_t* row_req,
+                                          int32_t* row_len, int32_t* err, void* stream) {
+  using namespace m3s;
+  if (T < 0 || njobs < 0 || njobs > M3S_MAX_STORE_JOBS || (njobs > 0 && !jobs)) return M3S_ERR_INVALID;
+  if (B < 0 || R < 0) return M3S_ERR_INVALID;
+  if (R > 0 && (!cu_q || !row_req || !row_len || (B > 0 && !seq_len))) return M3S_ERR_INVALID;
+  const bool store = T > 0 && njobs > 0;
+  if (store) {
+    if (!slot_mapping) return M3S_ERR_INVALID;
+    for (int i = 0; i < njobs; ++i) {
+      const int rc = check_job(jobs[i].src, jobs[i].src_row_stride, jobs[i].H, jobs[i].dst);
+      if (rc != M3S_OK) return rc;
+    }
+  }
+  if (!store && R == 0) return M3S_OK;
+  return launch_store(jobs, store ? njobs : 0, store ? T : 0, slot_mapping, err, static_cast<cudaStream_t>(stream),
+                      cu_q, seq_len, B, R, row_req, row_len);
 }
 
 extern "C" int m3s_qk_norm_rope_store(const m3s_write_job* jobs, int32_t njobs, int32_t T,
