@@ -60,6 +60,11 @@ def test_workspace_sizes(lib):
         256 + (8 + 255) * 1 * 16 * 8
     assert M.m3s_workspace_bytes(M.OP_INDEX_CANDIDATES, 300, 300, 24, 0, 0, 16, 16) == \
         1280 + (300 + 255) * 1 * 16 * 8
+    # the two-launch decode step: candidate lists for R + 255 slots (256-byte
+    # rounded), then an (first slot, lists) pair a row
+    assert M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == \
+        (263 * 16 * 8 + 255) // 256 * 256 + 8 * 8
+    assert M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, 8, 8, 3600, 16, 1, 16, 0) == 0
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 0, 8, 3600) == 0
     # attention merges its split-K partials on chip (thread-block cluster): no workspace
     assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == 0
@@ -93,6 +98,24 @@ def test_host_validation_rejects_before_launch(lib):
     fk = ctypes.c_void_p(1 << 20)
     assert lib.m3s_index_score_candidates(fk, fk, 16, fake_plane, fk, 4, None, None, fk, fk, 2, 2,
                                           16, 0, 0, fk, fk, 1 << 20, None, None) == M.ERR_INVALID
+    # the two-launch decode step checks the attention's arguments before it
+    # launches anything: q heads not a multiple of KV heads, GQA beyond 16
+    fk2 = ctypes.c_void_p(1 << 20)
+    P3 = M.Plane(ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 21), 4, 1)
+    assert lib.m3s_index_attention(fk2, fk2, 16, P3, fk2, 6, 4, P3, P3, fk2, 4, 2, fk2, fk2, 2, 16, 0, 0,
+                                   ctypes.c_float(0.1), fk2, fk2, None, fk2, 1 << 20, None, None) == M.ERR_INVALID
+    assert lib.m3s_index_attention(fk2, fk2, 16, P3, fk2, 32, 1, P3, P3, fk2, 4, 2, fk2, fk2, 2, 16, 0, 0,
+                                   ctypes.c_float(0.1), fk2, fk2, None, fk2, 1 << 20, None,
+                                   None) == M.ERR_UNSUPPORTED
+    assert lib.m3s_index_attention(fk2, fk2, 16, P3, fk2, 16, 1, P3, P3, fk2, 4, 2, fk2, fk2, 2, 16, 0, 0,
+                                   ctypes.c_float(0.1), fk2, fk2, None, fk2, 16, None, None) == M.ERR_WORKSPACE
+    # the store with the row map: negative counts, a row map without outputs
+    assert lib.m3s_nvfp4_store_batch_rows(None, 0, 0, None, None, None, -1, 4, None, None, None,
+                                          None) == M.ERR_INVALID
+    assert lib.m3s_nvfp4_store_batch_rows(None, 0, 0, None, fk2, fk2, 2, 4, None, None, None,
+                                          None) == M.ERR_INVALID
+    assert lib.m3s_nvfp4_store_batch_rows(None, 0, 0, None, None, None, 0, 0, None, None, None,
+                                          None) == M.OK
     # forced block counts must not be negative
     fake = ctypes.c_void_p(1 << 20)
     assert lib.m3s_block_topk(fake, 8, fake, fake, 1, 1, 8, 4, -1, 0, fake, None) == M.ERR_INVALID
