@@ -301,7 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
           }
           __syncwarp();
         }
-#pragma unroll 1
+        // (fully unrolled: the shared loads and the head-sum shuffles of one
+        // m-tile overlap the others' conversions and products; 5% faster than
+        // one m-tile at a time although ptxas then spills 12 bytes)
+#pragma unroll
         for (int mt = 0; mt < kHalfKeys / 16; ++mt) {
           const int key0 = mt * 16 + g;
           const uint4 ca = *reinterpret_cast<const uint4*>(cs + key0 * kCodeBytes + 16 * t);
