@@ -38,7 +38,9 @@
 namespace m3s {
 namespace {
 
-constexpr int kAttMaxWarps = 8;
+// How far (log2 units) a head's running maximum may rise above the reference
+// its sums are kept relative to before they are rescaled.
+constexpr float kMaxSlack = 8.f;
 
 struct AttnArgs {
   const uint16_t* q;
@@ -440,12 +442,14 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
           const int em = e8m0_max4(kw4);
           const uint32_t sj = pow2_neg_f16x2(em - static_cast<int>((kw4 >> (8 * t)) & 0xFFu));
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 qv = sm.qa[j][lane];
-            const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
-            const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
-            const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
-            mma16816(sacc[c], qv.x, qv.y, qv.z, qv.w, b0, b1);
+          for (int jw = 0; jw < 4; ++jw) {   // word jw: bytes 0, 1 = k-step 2jw, bytes 2, 3 = 2jw + 1
+            uint32_t x[4];
+            e2m1x8_to_f16x2(wv[jw], x[0], x[1], x[2], x[3]);
+#pragma unroll
+            for (int js = 0; js < 2; ++js) {
+              const uint4 qv = sm.qa[2 * jw + js][lane];
+              mma16816(sacc[c], qv.x, qv.y, qv.z, qv.w, hmul2(x[2 * js], sj), hmul2(x[2 * js + 1], sj));
+            }
           }
           // columns 2t, 2t + 1 of this tile are the tokens decoded by lanes 8t, 8t + 4
           const float fk = pow2_f32(em - 127);
@@ -459,48 +463,70 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
           const uint32_t sc = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(kss + tok * kScaleBytes + 2 * t));
           const uint32_t s0 = bcast_lo(sc), s1 = bcast_hi(sc);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint4 qv = sm.qa[j][lane];
-            const uint32_t x = wv[j >> 1] >> (16 * (j & 1));
-            const uint32_t sj = j < 4 ? s0 : s1;
-            const uint32_t b0 = hmul2(e2m1x2_to_f16x2(x & 0xFFu), sj);
-            const uint32_t b1 = hmul2(e2m1x2_to_f16x2((x >> 8) & 0xFFu), sj);
-            mma16816(sacc[c], qv.x, qv.y, qv.z, qv.w, b0, b1);
+          for (int jw = 0; jw < 4; ++jw) {   // word jw: bytes 0, 1 = k-step 2jw, bytes 2, 3 = 2jw + 1
+            uint32_t x[4];
+            e2m1x8_to_f16x2(wv[jw], x[0], x[1], x[2], x[3]);
+            const uint32_t sj = jw < 2 ? s0 : s1;
+#pragma unroll
+            for (int js = 0; js < 2; ++js) {
+              const uint4 qv = sm.qa[2 * jw + js][lane];
+              mma16816(sacc[c], qv.x, qv.y, qv.z, qv.w, hmul2(x[2 * js], sj), hmul2(x[2 * js + 1], sj));
+            }
           }
         }
       }
       // ---- online softmax (log2 domain), causal mask inside the block ----
       float mx0 = -INFINITY, mx1 = -INFINITY;
+      if (ntok >= kPage) {   // (block-uniform) every token of the block is live
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int tk = tb + 8 * c + 2 * t;
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool live = tk + e < ntok;
-          sacc[c][e] = live ? sacc[c][e] * lsc0 : -INFINITY;
-          sacc[c][2 + e] = live ? sacc[c][2 + e] * lsc1 : -INFINITY;
-          mx0 = fmaxf(mx0, sacc[c][e]);
-          mx1 = fmaxf(mx1, sacc[c][2 + e]);
+          for (int e = 0; e < 2; ++e) {
+            sacc[c][e] *= lsc0;
+            sacc[c][2 + e] *= lsc1;
+            mx0 = fmaxf(mx0, sacc[c][e]);
+            mx1 = fmaxf(mx1, sacc[c][2 + e]);
+          }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int tk = tb + 8 * c + 2 * t;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool live = tk + e < ntok;
+            sacc[c][e] = live ? sacc[c][e] * lsc0 : -INFINITY;
+            sacc[c][2 + e] = live ? sacc[c][2 + e] * lsc1 : -INFINITY;
+            mx0 = fmaxf(mx0, sacc[c][e]);
+            mx1 = fmaxf(mx1, sacc[c][2 + e]);
+          }
         }
       }
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
-      const float c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+      // The reference m of a head moves only when the block's maximum exceeds
+      // it by more than kMaxSlack (and on the head's first live token): the
+      // sums stay relative to a reference up to 2^kMaxSlack below the true
+      // maximum, so p <= 2^kMaxSlack, and the accumulators are rescaled rarely
+      // (a warp-uniform skip) instead of on every block.
+      const float n0 = mx0 > m0 + kMaxSlack ? mx0 : m0;
+      const float n1 = mx1 > m1 + kMaxSlack ? mx1 : m1;
+      if (__any_sync(0xffffffffu, n0 != m0 || n1 != m1)) {
+        const float c0 = n0 == m0 ? 1.f : exp2f(m0 - n0);   // (0 from an empty reference)
+        const float c1 = n1 == m1 ? 1.f : exp2f(m1 - n1);
+        l0 *= c0;
+        l1 *= c1;
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          o[n][0] *= c0;
+          o[n][1] *= c0;
+          o[n][2] *= c1;
+          o[n][3] *= c1;
+        }
+      }
       m0 = n0;
       m1 = n1;
-      l0 *= c0;
-      l1 *= c1;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) {
-        o[n][0] *= c0;
-        o[n][1] *= c0;
-        o[n][2] *= c1;
-        o[n][3] *= c1;
-      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -572,16 +598,16 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
           const uint32_t hi01 = ((wa[hw] >> 4) & 0x0F0F0F0Fu) | (wb[hw] & 0xF0F0F0F0u);
           const uint32_t lo23 = (wc[hw] & 0x0F0F0F0Fu) | ((wd[hw] & 0x0F0F0F0Fu) << 4);
           const uint32_t hi23 = ((wc[hw] >> 4) & 0x0F0F0F0Fu) | (wd[hw] & 0xF0F0F0F0u);
+          uint32_t xe0[4], xe1[4], xo0[4], xo1[4];   // byte bb of each word, decoded
+          e2m1x8_to_f16x2(lo01, xe0[0], xe0[1], xe0[2], xe0[3]);
+          e2m1x8_to_f16x2(lo23, xe1[0], xe1[1], xe1[2], xe1[3]);
+          e2m1x8_to_f16x2(hi01, xo0[0], xo0[1], xo0[2], xo0[3]);
+          e2m1x8_to_f16x2(hi23, xo1[0], xo1[1], xo1[2], xo1[3]);
 #pragma unroll
           for (int bb = 0; bb < 4; ++bb) {
             const int jj = 4 * hw + bb;
-            const uint32_t sh = 8 * bb;
-            const uint32_t be0 = hmul2(e2m1x2_to_f16x2((lo01 >> sh) & 0xFFu), s01);
-            const uint32_t be1 = hmul2(e2m1x2_to_f16x2((lo23 >> sh) & 0xFFu), s23);
-            const uint32_t bo0 = hmul2(e2m1x2_to_f16x2((hi01 >> sh) & 0xFFu), s01);
-            const uint32_t bo1 = hmul2(e2m1x2_to_f16x2((hi23 >> sh) & 0xFFu), s23);
-            mma16816(o[2 * jj], pa0, pa1, pa2, pa3, be0, be1);
-            mma16816(o[2 * jj + 1], pa0, pa1, pa2, pa3, bo0, bo1);
+            mma16816(o[2 * jj], pa0, pa1, pa2, pa3, hmul2(xe0[bb], s01), hmul2(xe1[bb], s23));
+            mma16816(o[2 * jj + 1], pa0, pa1, pa2, pa3, hmul2(xo0[bb], s01), hmul2(xo1[bb], s23));
           }
         }
       }
