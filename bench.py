@@ -53,6 +53,11 @@ def parse():
                          "m3s_index_score_topk then m3s_sparse_attention; pair = "
                          "m3s_index_block_scores, m3s_block_topk, m3s_sparse_attention. The scorer "
                          "and the attention are timed alone through the pair calls either way")
+    ap.add_argument("--verify-path", choices=["call", "fused"], default="call",
+                    help="verify and prefill rows: call = m3s_verify_score_topk then "
+                         "m3s_sparse_attention (measured faster on the verify batch, equal on "
+                         "prefill); fused = m3s_verify_index_attention (the verify scorer leaves "
+                         "per-CTA candidates, the attention merges them: two launches)")
     ap.add_argument("--cache-format", choices=["nvfp4", "mxfp4"], default="nvfp4",
                     help="K / V / index-K record format")
     ap.add_argument("--write-path", choices=["store", "fused", "staged"], default="store",
@@ -580,6 +585,9 @@ def measure_workload(name, args, dev, world):
     ws_ia = torch.zeros(max(16, M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, R, B, bt_stride, s.hq,
                                                       s.hkv, s.hi, s.topk)),
                         dtype=torch.uint8, device=dev)
+    ws_via = torch.zeros(max(16, M.m3s_workspace_bytes(M.OP_VERIFY_INDEX_ATTENTION, R, B, bt_stride, s.hq,
+                                                       s.hkv, s.hi, s.topk, max(s.q_rows))),
+                         dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def pre():
@@ -606,6 +614,7 @@ def measure_workload(name, args, dev, world):
     q_in = d["q"] if write_path == "store" else q_n
     qidx_in = d["q_idx"] if write_path == "store" else qidx_n
     path = getattr(args, "topk_path", "fused")
+    vpath = getattr(args, "verify_path", "call")
 
     def score():   # the verify rows' fused score + top-k
         M.m3s_verify_score_topk(qidx_in, d["w"], ic, is_, bt, d["cu_q"], row_len,
@@ -622,6 +631,11 @@ def measure_workload(name, args, dev, world):
         M.m3s_index_attention(qidx_in, d["w"], ic, is_, q_in, s.hkv, kc, ks, vc, vs, bt, row_req,
                               row_len, s.topk, SM_SCALE, ids, out, lse, ws_ia, err)
 
+    def verify_index_attention():
+        M.m3s_verify_index_attention(qidx_in, d["w"], ic, is_, q_in, s.hkv, kc, ks, vc, vs, bt, d["cu_q"],
+                                     row_req, row_len, max(s.q_rows), s.topk, SM_SCALE, ids, out, lse,
+                                     ws_via, err)
+
     def topk():
         M.m3s_block_topk(bscores, row_req, row_len, B, bt_stride, s.topk, ids)
 
@@ -635,7 +649,10 @@ def measure_workload(name, args, dev, world):
     # node between two kernels breaks their programmatic-launch overlap, so this
     # copy times those two kernels and not the step); one graph per separate
     # call for the breakdown
-    if fused:
+    if fused and vpath == "fused":
+        phases = [pre, verify_index_attention]
+        timing, score_fn = [pre, score, attn], score
+    elif fused:
         phases = [pre, score, attn]
         timing, score_fn = phases, score
     elif path == "fused":
@@ -700,7 +717,7 @@ def measure_workload(name, args, dev, world):
     ntiles = B * ((max(s.q_rows) + 7) // 8) if fused else R
     streams = (fused or path == "call") and ntiles > MAX_GRID
     pre_launches = {"store": 1, "fused": 2, "staged": 3}[write_path]
-    if not fused and path == "fused":
+    if (vpath if fused else path) == "fused":   # the scorer, then the attention merging its candidates
         launches_per_step = pre_launches + 2
     elif not fused and path == "pair":
         launches_per_step = pre_launches + 3

@@ -111,6 +111,7 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
 #define M3S_OP_SPARSE_ATTENTION 3
 #define M3S_OP_INDEX_CANDIDATES 4
 #define M3S_OP_INDEX_ATTENTION 5
+#define M3S_OP_VERIFY_INDEX_ATTENTION 6
 
 /*
  * Workspace bytes an op needs (device memory the caller provides as `ws`).
@@ -131,6 +132,13 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
  *    call leaves it that way again, so it can be reused call after call, graph
  *    replays included. A call that raised M3S_DEVERR_TIMEOUT may leave tickets
  *    set: zero the workspace again after one.
+ * Index attention (decode rows): candidate lists of topk keys for R + 255
+ * slots (rounded up to 256 bytes), then one int2 per row.
+ * Verify index attention: candidate lists of topk keys for (ntiles + 255)
+ * slots of 8 rows (rounded up to 256 bytes), a block-maximum scratch of
+ * 256 x 8 x max_blocks fp32 (rounded up likewise), then one int2 per row;
+ * 0 when ntiles exceeds 8192. Neither needs zeroing: every call writes what it
+ * reads.
  * Attention: 0 (its split-K partials are merged on chip); its ws arguments
  * are accepted and ignored.
  */
@@ -422,6 +430,30 @@ int m3s_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_f
                         const int32_t* row_len, int32_t R, int32_t topk, int32_t init_blocks,
                         int32_t local_blocks, float sm_scale, int32_t* topk_ids, uint16_t* out, float* lse,
                         void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
+/*
+ * Verify rows end to end: the fused verify scoring, top-k and block-sparse
+ * attention in two launches. #2744, Fused verify top-k (a request's rows scored
+ * together against each block, the top-k kept per chunk and merged) and
+ * Design / Attention. The verify scorer (tiles of up to 8 rows of one request,
+ * as m3s_verify_score_topk) leaves, for every row, each of its CTAs' top-k
+ * candidate keys over the blocks it scored; the attention merges a row's
+ * candidates before it reads the row's pages. topk_ids, out and lse are what
+ * m3s_verify_score_topk followed by m3s_sparse_attention return.
+ * Arguments: those of m3s_verify_score_topk (cu_q int32 [B + 1], row_len,
+ * max_q) and of m3s_sparse_attention (q, heads, K / V planes, row_req int32
+ * [R], the row map of the same rows). ws_bytes >=
+ * m3s_workspace_bytes(M3S_OP_VERIFY_INDEX_ATTENTION, R, B, bt_stride, Hq, Hkv,
+ * Hi, topk, max_q) (no zeroing needed). B * ceil(max_q / 8) <= 8192 tiles, else
+ * M3S_ERR_UNSUPPORTED.
+ */
+int m3s_verify_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_fp4_plane idx_k,
+                               const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k, m3s_fp4_plane v,
+                               const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* cu_q,
+                               const int32_t* row_req, const int32_t* row_len, int32_t R, int32_t max_q,
+                               int32_t topk, int32_t init_blocks, int32_t local_blocks, float sm_scale,
+                               int32_t* topk_ids, uint16_t* out, float* lse, void* ws, size_t ws_bytes,
+                               int32_t* err, void* stream);
 
 /*
  * Block-sparse attention over the selected NVFP4 pages. "NVFP4 sparse KV",

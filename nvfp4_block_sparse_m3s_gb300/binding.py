@@ -25,6 +25,7 @@ DEVERR_SLOT, DEVERR_BLOCK_ID, DEVERR_PAGE, DEVERR_ROW, DEVERR_QRANGE, DEVERR_TIM
     1, 2, 4, 8, 16, 32
 OP_INDEX_SCORE_TOPK, OP_VERIFY_SCORE_TOPK, OP_SPARSE_ATTENTION, OP_INDEX_CANDIDATES = 1, 2, 3, 4
 OP_INDEX_ATTENTION = 5
+OP_VERIFY_INDEX_ATTENTION = 6
 FMT_NVFP4, FMT_MXFP4 = 0, 1
 HEAD_DIM = PAGE = 128
 
@@ -83,6 +84,9 @@ _SIGS = {
     "m3s_index_attention": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _I32, Plane, Plane, _P, _I32,
                                            _I32, _P, _P, _I32, _I32, _I32, _I32, ctypes.c_float, _P, _P,
                                            _P, _P, _SZ, _P, _P]),
+    "m3s_verify_index_attention": (ctypes.c_int, [_P, _P, _I32, Plane, _P, _I32, _I32, Plane, Plane, _P,
+                                                  _I32, _I32, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                                                  ctypes.c_float, _P, _P, _P, _P, _SZ, _P, _P]),
     "m3s_nvfp4_store_batch_rows": (ctypes.c_int, [ctypes.c_void_p, _I32, _I32, _P, _P, _P, _I32, _I32, _P,
                                                   _P, _P, _P]),
     "m3s_version": (ctypes.c_char_p, []),
@@ -427,4 +431,34 @@ def m3s_index_attention(q_idx, w, idx_codes, idx_scales, q, hkv: int, k_codes, k
         init_blocks, local_blocks, sm_scale, _ptr(topk_ids), _ptr(out), _ptr(lse), _ptr(ws),
         ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
     _check(rc, "m3s_index_attention")
+    return topk_ids, out
+
+
+def m3s_verify_index_attention(q_idx, w, idx_codes, idx_scales, q, hkv: int, k_codes, k_scales, v_codes,
+                               v_scales, block_table, cu_q, row_req, row_len, max_q: int, topk: int,
+                               sm_scale: float, topk_ids=None, out=None, lse=None, ws=None, err=None,
+                               stream=None, init_blocks: int = 0, local_blocks: int = 0):
+    """Verify scoring, top-k and attention of verify rows (two launches);
+    returns (topk_ids int32 [R, topk], out bf16 [R, Hq, 128])."""
+    _index_inputs(q_idx, w, block_table, cu_q, row_req, row_len)
+    if q.dtype != torch.bfloat16 or not q.is_contiguous():
+        raise TypeError("q must be a contiguous bfloat16 tensor [R, Hq, 128]")
+    R, Hi = q_idx.shape[0], q_idx.shape[1]
+    Hq = q.shape[1]
+    B, bt_stride = block_table.shape
+    if topk_ids is None:
+        topk_ids = torch.empty((R, topk), dtype=torch.int32, device=q.device)
+    if out is None:
+        out = torch.empty((R, Hq, 128), dtype=torch.bfloat16, device=q.device)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise TypeError("lse must be a contiguous float32 tensor [R, Hq]")
+    if ws is None:
+        nb = m3s_workspace_bytes(OP_VERIFY_INDEX_ATTENTION, R, B, bt_stride, Hq, hkv, Hi, topk, max_q)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=q.device)
+    rc = load().m3s_verify_index_attention(
+        _ptr(q_idx), _ptr(w), Hi, plane(idx_codes, idx_scales), _ptr(q), Hq, hkv, plane(k_codes, k_scales),
+        plane(v_codes, v_scales), _ptr(block_table), bt_stride, B, _ptr(cu_q), _ptr(row_req), _ptr(row_len), R,
+        max_q, topk, init_blocks, local_blocks, sm_scale, _ptr(topk_ids), _ptr(out), _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(err), _stream(stream))
+    _check(rc, "m3s_verify_index_attention")
     return topk_ids, out

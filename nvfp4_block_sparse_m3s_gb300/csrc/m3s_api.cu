@@ -24,6 +24,12 @@ extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_
       const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;
       return round16(m3s::score_topk_ws_bytes(B > 0 ? static_cast<long long>(B) * cpr : 0, 8, R, max_blocks, topk));
     }
+    case M3S_OP_VERIFY_INDEX_ATTENTION: {   // candidate lists, block-maximum scratch, row ranges
+      const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;
+      const long long nt = B > 0 ? static_cast<long long>(B) * cpr : 0;
+      if (nt > m3s::kMaxTiles) return 0;
+      return round16(m3s::verify_attention_ws_bytes(static_cast<int>(nt), R, topk, max_blocks));
+    }
     case M3S_OP_SPARSE_ATTENTION:
       // split-K partials are combined inside a thread-block cluster: no workspace
       return 0;

@@ -59,11 +59,13 @@ struct AttnArgs {
   float* lse;
   int32_t* err;
   // candidates mode (ids == nullptr): the scorer's per-CTA candidate lists and
-  // each row's (first slot, lists); the row's ids are written to ids_out
+  // each row's (first list, lists), its lists cand_stride lists apart; the
+  // row's ids are written to ids_out
   const unsigned long long* cand;
   const int2* meta;
   int32_t* ids_out;
-  int nslots;   // candidate slots in cand
+  int nlists;        // lists of topk keys in cand
+  int cand_stride;   // 1 (decode rows: a row's lists are consecutive) or 8 (verify tiles)
 };
 
 // Per-warp partial outputs are stored at [head][dim + dim / 32] in rows of
@@ -128,14 +130,17 @@ __device__ __forceinline__ float pow2_f32_nonpos(int d) {
 }
 
 // Candidates mode, the whole CTA: the row's top-k from its candidate lists
-// (mt.y lists of topk keys, each descending, in consecutive slots from mt.x:
-// one contiguous run), its ids ranked ascending into sel_id (-1 padded); split 0
-// of the first KV head also writes them to ids_out. The run is staged into buf
-// by one bulk copy (thread 0; loads by every thread when it is not 16-byte
-// aligned). Selection by counting, in three CTA-wide passes: the k-th largest
+// (mt.y lists of topk keys, each descending, list j at list index
+// mt.x + j * cand_stride), its ids ranked ascending into sel_id (-1 padded);
+// split 0 of the first KV head also writes them to ids_out. Consecutive lists
+// (decode rows) are one contiguous run, staged into buf by one bulk copy
+// (thread 0); strided lists, or a run that is not 16-byte aligned, by loads
+// from every thread. Selection by counting, in three CTA-wide passes: the k-th largest
 // list head is a lower bound for the row's k-th key (the k largest heads are
-// k keys at least that large), so only keys at or above it (at most k lists'
-// worth) are candidates; each candidate's rank is the number of larger ones,
+// k keys at least that large; with fewer lists than k every key is a
+// candidate: bounding by the smallest of the lists' ceil(k / nl)-th keys
+// instead timed 0.25 us slower on the skewed decode step), so only keys at or
+// above it are candidates; each candidate's rank is the number of larger ones,
 // and the k best land at their ranks. (More than kSelCap candidates: a
 // pairwise merge of all lists instead.) Kept out of line: inlined, merge code
 // of this kind slowed the block loop of the whole kernel (measured: decode-row
@@ -147,9 +152,11 @@ __device__ __noinline__ bool select_row_candidates(const AttnArgs& a, int2 mt, i
                                                    int nthreads, int* sel_id, unsigned long long* tau_s,
                                                    int* n_s) {
   const int tid = threadIdx.x, k = a.topk;
-  // a range outside the slots is reported and skipped (the scorer writes every
+  // a range outside the lists is reported and skipped (the scorer writes every
   // row's range each call; this guards against a stale or foreign workspace)
-  if (mt.x < 0 || mt.y < 0 || mt.y > a.nslots || mt.x > a.nslots - mt.y) {
+  const int cs = a.cand_stride;
+  if (mt.x < 0 || mt.y < 0 || mt.y > a.nlists ||
+      (mt.y > 0 && static_cast<long long>(mt.x) + static_cast<long long>(mt.y - 1) * cs >= a.nlists)) {
     if (tid == 0) raise(a.err, M3S_DEVERR_ROW);
     mt = make_int2(0, 0);
   }
@@ -163,7 +170,7 @@ __device__ __noinline__ bool select_row_candidates(const AttnArgs& a, int2 mt, i
   unsigned long long* top = cand + kSelCap;              // the k best, descending
   bool ok = static_cast<size_t>(bytes) + (kSelCap + M3S_MAX_TOPK) * 8 + M3S_MAX_TOPK * 4 <= buf_bytes;
   if (ok && nkeys > 0) {
-    if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+    if (cs == 1 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
       if (tid == 0) {
         mbar_expect_tx(bar, bytes);
         bulk_g2s(buf, src, bytes, bar);
@@ -174,14 +181,18 @@ __device__ __noinline__ bool select_row_candidates(const AttnArgs& a, int2 mt, i
         mbar_wait(bar, 0);
         ok = false;
       }
-    } else {
-      for (int e = tid; e < nkeys; e += nthreads) buf[e] = __ldcg(src + e);
+    } else {   // (list e / k at src + (e / k) * cs * k)
+      for (int e = tid; e < nkeys; e += nthreads)
+        buf[e] = __ldcg(src + static_cast<size_t>(e / k) * cs * k + e % k);
       __syncthreads();
     }
   }
   int nsel = 0;   // keys selected (<= k)
   if (ok && nkeys > 0) {
-    // the lower bound: the k-th largest head (every nonzero key when fewer lists)
+    // the lower bound: with nl >= k lists, the k-th largest head; with fewer,
+    // the smallest of the lists' c-th keys, c = ceil(k / nl) (each list holds c
+    // keys at least that large, nl * c >= k in all); at least 1 (zero keys are
+    // empty slots)
     if (tid == 0) {
       *tau_s = 1ull;
       *n_s = 0;
@@ -798,7 +809,8 @@ int launch_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k
                      const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* row_req,
                      const int32_t* row_len, const int32_t* topk_ids, int32_t topk, int32_t R,
                      float sm_scale, uint16_t* out, float* lse, int32_t* err, cudaStream_t stream,
-                     const unsigned long long* cand, const int2* meta, int32_t* ids_out) {
+                     const unsigned long long* cand, const int2* meta, int32_t* ids_out, int cand_lists,
+                     int cand_stride) {
   const int rc = check_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len,
                                  topk_ids != nullptr || (cand && meta), topk, R, out);
   if (rc != M3S_OK || R == 0) return rc;
@@ -807,7 +819,7 @@ int launch_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k
   AttnArgs a{q, Hq, Hkv, Hq / Hkv, k.codes, k.scales, v.codes, v.scales, k.num_pages, block_table,
              bt_stride, row_req, row_len, topk_ids, topk, R, B,
              sm_scale * 1.4426950408889634f, nsplit, ips, out, lse, err, cand, meta, ids_out,
-             R + kMaxGrid - 1};
+             cand_lists, cand_stride};
   // two warp groups when the grid has at most one CTA per SM (each SM then
   // computes two of its blocks at once), else one (more CTAs resident per SM)
   const bool mx = k.format == M3S_FMT_MXFP4;
@@ -836,5 +848,5 @@ extern "C" int m3s_sparse_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, 
   (void)ws_bytes;
   return m3s::launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, topk_ids,
                                topk, R, sm_scale, out, lse, err, static_cast<cudaStream_t>(stream),
-                               nullptr, nullptr, nullptr);
+                               nullptr, nullptr, nullptr, 0, 1);
 }

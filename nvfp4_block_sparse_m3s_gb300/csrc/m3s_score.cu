@@ -163,8 +163,10 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
   ScoreSmem<QT>& sm = *reinterpret_cast<ScoreSmem<QT>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   TileLayout L;
+  // (partials mode, meta set: candidate lists without the tiles' merges)
+  const bool late = a.cand && !a.meta;   // the grid ends merging candidates
   L.bind(reinterpret_cast<uint8_t*>(&sm) + sizeof(ScoreSmem<QT>), a.ntiles,
-         a.cand ? kTileSetUpStreaming : kTileSetUp);
+         late ? kTileSetUpStreaming : kTileSetUp);
   const int* pre = L.pre;
   __shared__ int red[C::kWarps];
 
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   // with the streaming top-k the next kernel is let launch only when this CTA's
   // blocks are scored (its waiting CTAs slowed the step when launched early)
-  if (!a.cand) pdl_trigger();
+  if (!late) pdl_trigger();
   pdl_wait();
 
   // ---- exclusive prefix of block counts over tiles, then this CTA's range ----
@@ -207,7 +209,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
   const int2 range = L.cta_range(blockIdx.x);
   const int lo = range.x, hi = range.y;
   int tile = tile_at(pre, ntiles, lo);
-  if (a.cand && lo >= hi) pdl_trigger();   // no blocks
+  if (late && lo >= hi) pdl_trigger();   // no blocks
 
   int g0 = 0;               // sequence number of the segment's first block in this CTA
   bool mma_issued = false;  // MMA thread: a commit may still be outstanding
@@ -220,6 +222,12 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
     const int nseg = seg_hi - seg_lo;
     const TileInfo<QT> ti = tile_info<QT>(a, tile, false);
     const int32_t* bt_row = a.block_table + static_cast<size_t>(ti.req) * a.bt_stride;
+    if (a.meta && seg_lo == 0 && tid < ti.nrows) {   // this CTA holds the tile's first block
+      // row rho's lists: slots tile + c of the covering CTAs c, QT lists apart
+      const int2 cc = L.covering_ctas(tile, L.g);
+      if (cc.x != static_cast<int>(blockIdx.x)) raise(a.err, M3S_DEVERR_ROW);   // (invariant)
+      a.meta[ti.row0 + tid] = make_int2((tile + cc.x) * QT + tid, cc.y - cc.x + 1);
+    }
 
     // ---- stage the tile's queries (the B operand), weights and lengths. Each
     // (row, head) is scaled by 2^-e_h before its f16 conversion (its largest
@@ -471,7 +479,7 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       }
     }
     __syncthreads();  // every role is done with this segment (and its queries)
-    if (a.cand && pre[tile] + seg_hi >= hi) pdl_trigger();   // this CTA's blocks are scored
+    if (late && pre[tile] + seg_hi >= hi) pdl_trigger();   // this CTA's blocks are scored
     if (a.cand) {
       // the segment's candidates: warp rho takes row rho's block maxima from the
       // CTA's score scratch 32 at a time and keeps their top-k (a key enters
@@ -484,24 +492,48 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
         const float* row_sc = a.seg_scores + (static_cast<size_t>(blockIdx.x) * QT + rho) * a.bt_stride;
         WarpTopk list;
         list.clear();
-        for (int j0 = 0; j0 < nseg; j0 += 32) {
-          const int j = j0 + lane;
-          const int blk = seg_lo + j;
-          unsigned long long key = 0ull;
-          if (j < nseg && blk * kPage < rl_r)
-            key = select_key(__ldcg(row_sc + j), blk, nbr, a.init_blocks, a.local_blocks);
-          unsigned over = __ballot_sync(0xffffffffu, key > list.kth);
-          while (over) {   // ascending lanes: each key is inserted in turn
-            const int l = __ffs(over) - 1;
-            over &= over - 1;
-            list.insert(__shfl_sync(0xffffffffu, key, l), a.topk, lane);
+        // the maxima 32 x kListBatch at a time (their loads issued together);
+        // a chunk with more than kInsertMax keys above the list's k-th is sorted
+        // across the lanes and merged in (a bitonic split), fewer are inserted
+        // one by one (the first chunks of a segment insert almost every key:
+        // one at a time that took 11 us a segment on the verify batch)
+        constexpr int kListBatch = 4, kInsertMax = 4;
+        for (int j0 = 0; j0 < nseg; j0 += 32 * kListBatch) {
+          unsigned long long key[kListBatch];
+#pragma unroll
+          for (int u = 0; u < kListBatch; ++u) {
+            const int j = j0 + 32 * u + lane;
+            const int blk = seg_lo + j;
+            key[u] = (j < nseg && blk * kPage < rl_r)
+                         ? select_key(__ldcg(row_sc + j), blk, nbr, a.init_blocks, a.local_blocks)
+                         : 0ull;
+          }
+#pragma unroll
+          for (int u = 0; u < kListBatch; ++u) {
+            unsigned over = __ballot_sync(0xffffffffu, key[u] > list.kth);
+            if (__popc(over) > kInsertMax) {
+              WarpTopk c;
+              c.a = key[u];
+              c.b = 0ull;
+              c.kth = 0ull;
+              warp_sort_desc(c, 32, lane);   // the chunk, descending in slots 0 .. 31
+              warp_merge2(list, c, a.topk, lane);
+              list.kth = __shfl_sync(0xffffffffu, a.topk > 32 ? list.b : list.a, (a.topk - 1) & 31);
+            } else {
+              while (over) {   // ascending lanes: each key is inserted in turn
+                const int l = __ffs(over) - 1;
+                over &= over - 1;
+                list.insert(__shfl_sync(0xffffffffu, key[u], l), a.topk, lane);
+              }
+            }
           }
         }
         write_keys(list, a.topk, a.cand + (static_cast<size_t>(tile + blockIdx.x) * QT + rho) * a.topk, lane);
       }
       __syncthreads();
-      tile_finish<QT>(a, L, tile, nseg, reinterpret_cast<unsigned long long*>(&sm.stage[0][0]),
-                      static_cast<int>(sizeof(sm.stage) / 8), sm.vslot, &sm.fin, C::kThreads);
+      if (!a.meta)
+        tile_finish<QT>(a, L, tile, nseg, reinterpret_cast<unsigned long long*>(&sm.stage[0][0]),
+                        static_cast<int>(sizeof(sm.stage) / 8), sm.vslot, &sm.fin, C::kThreads);
     }
     g0 += nseg;
     pos = pre[tile] + seg_hi;
@@ -962,7 +994,8 @@ int launch_attention(const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k
                      const int32_t* block_table, int32_t bt_stride, int32_t B, const int32_t* row_req,
                      const int32_t* row_len, const int32_t* topk_ids, int32_t topk, int32_t R,
                      float sm_scale, uint16_t* out, float* lse, int32_t* err, cudaStream_t stream,
-                     const unsigned long long* cand, const int2* meta, int32_t* ids_out);
+                     const unsigned long long* cand, const int2* meta, int32_t* ids_out, int cand_lists,
+                     int cand_stride);
 }  // namespace m3s
 
 extern "C" int m3s_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_fp4_plane idx_k,
@@ -983,7 +1016,7 @@ extern "C" int m3s_index_attention(const uint16_t* q_idx, const float* w, int32_
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (topk == 0)   // nothing selected: every row attends over no token
     return launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, topk_ids, 0, R,
-                            sm_scale, out, lse, err, st, nullptr, nullptr, nullptr);
+                            sm_scale, out, lse, err, st, nullptr, nullptr, nullptr, 0, 1);
   if (ws_bytes < m3s_workspace_bytes(M3S_OP_INDEX_ATTENTION, R, B, bt_stride, Hq, Hkv, Hi, topk, 1))
     return M3S_ERR_WORKSPACE;
   if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
@@ -999,7 +1032,58 @@ extern "C" int m3s_index_attention(const uint16_t* q_idx, const float* w, int32_
   rc = launch_score_decode(a, st);
   if (rc != M3S_OK) return rc;
   return launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, nullptr, topk, R,
-                          sm_scale, out, lse, err, st, a.cand, a.meta, topk_ids);
+                          sm_scale, out, lse, err, st, a.cand, a.meta, topk_ids, R + kMaxGrid - 1, 1);
+}
+
+// Verify rows (tiles of up to 8 rows of one request) the same way: the verify
+// scorer in partials mode leaves each CTA's top-k of every row it scores (the
+// streaming form's lists, without the tiles' merges) and each row's list range,
+// and the attention merges a row's lists before it reads the row's pages.
+extern "C" int m3s_verify_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi,
+                                          m3s_fp4_plane idx_k, const uint16_t* q, int32_t Hq, int32_t Hkv,
+                                          m3s_fp4_plane k, m3s_fp4_plane v, const int32_t* block_table,
+                                          int32_t bt_stride, int32_t B, const int32_t* cu_q,
+                                          const int32_t* row_req, const int32_t* row_len, int32_t R,
+                                          int32_t max_q, int32_t topk, int32_t init_blocks,
+                                          int32_t local_blocks, float sm_scale, int32_t* topk_ids,
+                                          uint16_t* out, float* lse, void* ws, size_t ws_bytes, int32_t* err,
+                                          void* stream) {
+  using namespace m3s;
+  int32_t no_ids = 0;   // (top-k 0 writes no id)
+  int rc = check_common(q_idx, w, Hi, idx_k, block_table, bt_stride, R, B, topk, topk > 0 ? topk_ids : &no_ids);
+  if (rc != M3S_OK) return rc;
+  rc = check_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, true, topk, R, out);
+  if (rc != M3S_OK || R == 0) return rc;
+  if (!cu_q || !row_req || !row_len || max_q < 0 || init_blocks < 0 || local_blocks < 0) return M3S_ERR_INVALID;
+  const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;
+  const long long ntiles = static_cast<long long>(B) * cpr;   // B == 0: every row is padding
+  if (ntiles > kMaxTiles) return M3S_ERR_UNSUPPORTED;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (topk == 0)   // nothing selected: every row attends over no token
+    return launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, topk_ids, 0, R,
+                            sm_scale, out, lse, err, st, nullptr, nullptr, nullptr, 0, 1);
+  if (ws_bytes < m3s_workspace_bytes(M3S_OP_VERIFY_INDEX_ATTENTION, R, B, bt_stride, Hq, Hkv, Hi, topk, max_q))
+    return M3S_ERR_WORKSPACE;
+  if (!ws || !aligned16(ws)) return M3S_ERR_INVALID;
+  const int nt = static_cast<int>(ntiles);
+  ScoreArgs a{q_idx, w, Hi, idx_k.codes, idx_k.scales, idx_k.num_pages, block_table, bt_stride,
+              nullptr, cu_q, row_len, R, B, nt, cpr, nullptr, bt_stride > 0 ? bt_stride : 1, err,
+              idx_k.format == M3S_FMT_MXFP4 ? 1 : 0};
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.cand = reinterpret_cast<unsigned long long*>(base);
+  a.seg_scores = reinterpret_cast<float*>(base + verify_attention_seg_offset(nt, topk));
+  a.meta = reinterpret_cast<int2*>(base + verify_attention_meta_offset(nt, topk, bt_stride));
+  a.topk = topk;
+  a.init_blocks = init_blocks;
+  a.local_blocks = local_blocks;
+  if (nt > 0) {
+    rc = launch_score<8>(a, st);
+    if (rc != M3S_OK) return rc;
+  } else {   // no tile: every row is padding, with an empty list range
+    if (cudaMemsetAsync(a.meta, 0, static_cast<size_t>(R) * 8, st) != cudaSuccess) return M3S_ERR_LAUNCH;
+  }
+  return launch_attention(q, Hq, Hkv, k, v, block_table, bt_stride, B, row_req, row_len, nullptr, topk, R,
+                          sm_scale, out, lse, err, st, a.cand, a.meta, topk_ids, (nt + kMaxGrid - 1) * 8, 8);
 }
 
 // ---------------------------------------------------------------------------

@@ -509,10 +509,10 @@ __device__ void write_unscored_rows(const ScoreArgs& a, const TileLayout& L, int
       if (a.ids) a.ids[static_cast<size_t>(r) * a.topk + i] = -1;
       else if (a.keys_out) a.keys_out[static_cast<size_t>(r) * a.topk + i] = 0ull;
     }
+    if (a.meta && tid == 0) a.meta[r] = make_int2(0, 0);   // no candidate lists
   };
   for (int t = blockIdx.x; t < L.ntiles; t += G) {
     if (L.blocks(t) != 0) continue;
-    if (a.meta && tid == 0) a.meta[t] = make_int2(0, 0);   // no candidate lists
     const int2 rows = tile_rows<QT>(a, t);
     for (int r = rows.x; r < rows.x + rows.y; ++r) blank(r);
   }
@@ -637,6 +637,21 @@ __host__ __device__ constexpr size_t index_attention_meta_offset(int R, int topk
 }
 __host__ __device__ constexpr size_t index_attention_ws_bytes(int R, int topk) {
   return index_attention_meta_offset(R, topk) + static_cast<size_t>(R) * 8;
+}
+
+// m3s_verify_index_attention's workspace: the candidate lists (slots of 8 rows
+// x topk keys, as in the streaming form), the CTAs' block-maximum scratch
+// ([grid][8][bt_stride] fp32), then each row's list range (int2 per row).
+__host__ __device__ constexpr size_t verify_attention_seg_offset(int ntiles, int topk) {
+  return (topk_cand_bytes(ntiles, 8, topk) + 255) & ~static_cast<size_t>(255);
+}
+__host__ __device__ constexpr size_t verify_attention_meta_offset(int ntiles, int topk, int bt_stride) {
+  return (verify_attention_seg_offset(ntiles, topk) +
+          static_cast<size_t>(kMaxGrid) * 8 * (bt_stride > 0 ? bt_stride : 1) * 4 + 255) &
+         ~static_cast<size_t>(255);
+}
+__host__ __device__ constexpr size_t verify_attention_ws_bytes(int ntiles, int R, int topk, int bt_stride) {
+  return verify_attention_meta_offset(ntiles, topk, bt_stride) + static_cast<size_t>(R) * 8;
 }
 
 __host__ __device__ constexpr bool topk_streams(long long ntiles) { return ntiles > kMaxGrid; }

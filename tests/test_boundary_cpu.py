@@ -65,6 +65,15 @@ def test_workspace_sizes(lib):
     assert M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == \
         (263 * 16 * 8 + 255) // 256 * 256 + 8 * 8
     assert M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, 8, 8, 3600, 16, 1, 16, 0) == 0
+    # the two-launch verify step: lists for (16 tiles + 255) slots of 8 rows, a
+    # 256 x 8 x 1500 fp32 block-maximum scratch, an int2 per row (each part
+    # 256-byte rounded); 0 past 8192 tiles
+    cand = (16 + 255) * 8 * 16 * 8
+    seg = 256 * 8 * 1500 * 4
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_INDEX_ATTENTION, 128, 16, 1500, 16, 1, 16, 16, 8) == \
+        ((cand + 255) // 256 * 256 + seg + 255) // 256 * 256 + 128 * 8
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_INDEX_ATTENTION, 128, 16, 1500, 16, 1, 16, 0, 8) == 0
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_INDEX_ATTENTION, 128, 8193, 1500, 16, 1, 16, 16, 8) == 0
     assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 0, 8, 3600) == 0
     # attention merges its split-K partials on chip (thread-block cluster): no workspace
     assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == 0
@@ -109,6 +118,17 @@ def test_host_validation_rejects_before_launch(lib):
                                    None) == M.ERR_UNSUPPORTED
     assert lib.m3s_index_attention(fk2, fk2, 16, P3, fk2, 16, 1, P3, P3, fk2, 4, 2, fk2, fk2, 2, 16, 0, 0,
                                    ctypes.c_float(0.1), fk2, fk2, None, fk2, 16, None, None) == M.ERR_WORKSPACE
+    # the two-launch verify step: the attention's checks, then cu_q, the tile
+    # count and the workspace, before anything is launched
+    def via(Hq=16, Hkv=1, cu_q=fk2, B=2, max_q=8, ws_bytes=1 << 30):
+        return lib.m3s_verify_index_attention(fk2, fk2, 16, P3, fk2, Hq, Hkv, P3, P3, fk2, 4, B, cu_q, fk2, fk2,
+                                              2, max_q, 16, 0, 0, ctypes.c_float(0.1), fk2, fk2, None, fk2,
+                                              ws_bytes, None, None)
+    assert via(Hq=6, Hkv=4) == M.ERR_INVALID
+    assert via(cu_q=None) == M.ERR_INVALID
+    assert via(max_q=-1) == M.ERR_INVALID
+    assert via(B=8193) == M.ERR_UNSUPPORTED
+    assert via(ws_bytes=16) == M.ERR_WORKSPACE
     # the store with the row map: negative counts, a row map without outputs
     assert lib.m3s_nvfp4_store_batch_rows(None, 0, 0, None, None, None, -1, 4, None, None, None,
                                           None) == M.ERR_INVALID
