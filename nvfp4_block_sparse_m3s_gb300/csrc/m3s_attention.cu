@@ -189,10 +189,7 @@ __device__ __noinline__ bool select_row_candidates(const AttnArgs& a, int2 mt, i
   }
   int nsel = 0;   // keys selected (<= k)
   if (ok && nkeys > 0) {
-    // the lower bound: with nl >= k lists, the k-th largest head; with fewer,
-    // the smallest of the lists' c-th keys, c = ceil(k / nl) (each list holds c
-    // keys at least that large, nl * c >= k in all); at least 1 (zero keys are
-    // empty slots)
+    // the lower bound: the k-th largest head (every nonzero key when fewer lists)
     if (tid == 0) {
       *tau_s = 1ull;
       *n_s = 0;
