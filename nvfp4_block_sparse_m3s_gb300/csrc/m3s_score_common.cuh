@@ -215,6 +215,17 @@ __device__ __forceinline__ void tile_prefix(const ScoreArgs& a, TileLayout& L, i
   __syncthreads();
 }
 
+// This CTA's share (of the grid's) of an input's bytes, brought into L2 ahead
+// of its use; a hint only, skipped for an unaligned base.
+__device__ __forceinline__ void prefetch_share_l2(const void* base, size_t bytes) {
+  if (!base || bytes == 0 || (reinterpret_cast<uintptr_t>(base) & 15u) != 0) return;
+  const size_t chunk = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~static_cast<size_t>(15);
+  const size_t off = static_cast<size_t>(blockIdx.x) * chunk;
+  if (off >= bytes) return;
+  const size_t n = min(chunk, bytes - off) & ~static_cast<size_t>(15);
+  if (n > 0) bulk_prefetch_l2(static_cast<const uint8_t*>(base) + off, static_cast<uint32_t>(n));
+}
+
 // First tile whose block range holds position lo (pre[t] <= lo < pre[t+1]).
 __device__ __forceinline__ int tile_at(const int* pre, int ntiles, int lo) {
   int l = 0, h = ntiles;

@@ -106,6 +106,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
   // slow the step down).
   const bool late = a.cand && !a.meta;   // the grid ends merging candidates
   if (!late) pdl_trigger();
+  // Before the wait, each CTA brings its share of the queries, weights and
+  // block table into L2: the set-up after the wait is a chain of dependent
+  // loads, each a DRAM miss after an L2 flush otherwise. (A hint only: a line
+  // an earlier kernel writes later is updated in L2, which every read goes
+  // through.)
+  if (tid == 0) {
+    prefetch_share_l2(a.q_idx, static_cast<size_t>(a.R) * a.Hi * kHeadDim * 2);
+    prefetch_share_l2(a.w, static_cast<size_t>(a.R) * a.Hi * 4);
+    prefetch_share_l2(a.block_table, static_cast<size_t>(a.B) * a.bt_stride * 4);
+  }
   pdl_wait();
 
   tile_prefix<1>(a, L, red, kThreads);
