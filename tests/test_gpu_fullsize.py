@@ -7,7 +7,11 @@ the same launch configuration, checked on what the oracle can compute one by one
   tokens, stored by the CUDA path), bit-exact at their slots;
 * for the first and last row of each sampled request: block scores within 1e-4
   relative (index path), the top-k set (tie band 1e-5, ties to the lower id) and
-  attention over the selected blocks within 1e-2.
+  attention over the selected blocks within 1e-2;
+* decode rows, the benchmark's step as it launches it: the batched store of the
+  step's new rows with the row map in the same launch (the row map of every row
+  bit-exact), then m3s_index_attention, whose ids, BF16 outputs and lse equal
+  the separate calls' above on every row, bit for bit.
 
 The oracle quantises only the sampled requests (its inputs are the workload's
 own seeded BF16 rows, never the device's planes)."""
@@ -16,6 +20,7 @@ import numpy as np
 import pytest
 import torch
 
+from nvfp4_block_sparse_m3s_gb300 import binding as M
 from nvfp4_block_sparse_m3s_gb300 import workloads as W
 from oracle import m3s_oracle as O
 from step_helpers import (ATTN_RTOL, SM_SCALE, DeviceCache, OracleCache, attention_rel_err,
@@ -81,3 +86,22 @@ def test_full_size_sampled_rows(lib, name, reqs):
     assert e <= ATTN_RTOL, e
     got_lse = lse.cpu().numpy()
     np.testing.assert_allclose(got_lse[rows], lse_ref[rows], rtol=1e-4, atol=1e-4)
+
+    if not fused:
+        # the two-launch decode step: re-storing the step's new rows writes the
+        # same bytes, so the planes checked above are unchanged
+        new = torch.from_numpy(np.asarray(wl.new_tok, dtype=np.int64)).to(dev.kc.device)
+        rr2, rl2 = M.m3s_nvfp4_store_batch_rows(
+            [(dev.k_src[new].contiguous(), dev.kc, dev.ks), (dev.v_src[new].contiguous(), dev.vc, dev.vs),
+             (dev.ik_src[new].contiguous(), dev.ic, dev.is_)],
+            dev.slot_all[new].contiguous(), dev.cu_q, dev.seq_len, R, err=dev.err)
+        lse2 = torch.full((R, s.hq), float("nan"), dtype=torch.float32, device=dev.kc.device)
+        ids2, out2 = M.m3s_index_attention(dev.q_idx, dev.w, dev.ic, dev.is_, dev.q, s.hkv, dev.kc, dev.ks,
+                                           dev.vc, dev.vs, dev.block_table, rr2, rl2, s.topk, SM_SCALE,
+                                           lse=lse2, err=dev.err)
+        torch.cuda.synchronize()
+        assert int(dev.err.item()) == 0, int(dev.err.item())
+        assert np.array_equal(rr2.cpu().numpy(), rr) and np.array_equal(rl2.cpu().numpy(), rl)
+        assert np.array_equal(ids2.cpu().numpy(), gids)
+        assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+        np.testing.assert_array_equal(lse2.cpu().numpy(), got_lse)
