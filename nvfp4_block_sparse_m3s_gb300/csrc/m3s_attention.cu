@@ -535,12 +535,15 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
       }
       m0 = n0;
       m1 = n1;
+      // (a head whose reference is still -inf has only masked logits: -inf - 0
+      // gives p = 0 with no test per element)
+      const float b0 = n0 == -INFINITY ? 0.f : n0, b1 = n1 == -INFINITY ? 0.f : n1;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float p0 = n0 == -INFINITY ? 0.f : exp2f(sacc[c][e] - n0);
-          const float p1 = n1 == -INFINITY ? 0.f : exp2f(sacc[c][2 + e] - n1);
+          const float p0 = exp2f(sacc[c][e] - b0);
+          const float p1 = exp2f(sacc[c][2 + e] - b1);
           sacc[c][e] = p0;
           sacc[c][2 + e] = p1;
           l0 += p0;

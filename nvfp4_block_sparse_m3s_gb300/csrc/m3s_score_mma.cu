@@ -191,10 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
       const int s = hh & 1;
       const int blk = first + (hh >> 1) * kWarps;
       const int half = hh & 1;
-      const int page = pw.get(bt_row, blk, kWarps, seg_hi, lane);
-      int ok = 0;
+      const int page = pw.get(bt_row, blk, kWarps, seg_hi, lane);   // (warp-uniform)
+      const bool ok = !aborted && page >= 0 && page < a.num_pages;
       if (lane == 0 && !aborted) {
-        if (page < 0 || page >= a.num_pages) {
+        if (!ok) {
           if (half == 0) raise(a.err, M3S_DEVERR_PAGE);
         } else {
           // (no proxy fence: every generic read of this stage has returned, its
@@ -206,10 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1) score_decode_kernel(const ScoreAr
           bulk_g2s(sm.stage[warp][s] + kHalfCodeBytes,
                    a.scales + static_cast<size_t>(page) * (kPage * kKeyScaleBytes) + half * kHalfScaleB,
                    kHalfScaleB, &sm.bar[warp][s]);
-          ok = 1;
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       valid_bits = (valid_bits & ~(1u << s)) | (static_cast<uint32_t>(ok) << s);
     };
 
