@@ -38,6 +38,15 @@
 namespace m3s {
 namespace {
 
+// 2^x by the PTX ex2.approx.ftz instruction (inputs here are at most 2^8;
+// results below 2^-126 flush to 0, far below the resolution of the fp32 sum
+// they join).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // How far (log2 units) a head's running maximum may rise above the reference
 // its sums are kept relative to before they are rescaled.
 constexpr float kMaxSlack = 8.f;
@@ -483,7 +492,12 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
           }
         }
       }
-      // ---- online softmax (log2 domain), causal mask inside the block ----
+      // ---- online softmax (log2 domain), causal mask inside the block. (The
+      // logits are scaled one by one before the maximum: the reference is a
+      // rounded logit and each term's exponent is a rounded logit minus it, so
+      // the largest term is exactly 2^0 at any magnitude; folding the scale
+      // into an fma with the reference took the product's rounding error, up
+      // to 2^88 for logits near 2^112, into the exponent.) ----
       float mx0 = -INFINITY, mx1 = -INFINITY;
       if (ntok >= kPage) {   // (block-uniform) every token of the block is live
 #pragma unroll
@@ -542,8 +556,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 4 : 1) attention_kernel(con
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float p0 = exp2f(sacc[c][e] - b0);
-          const float p1 = exp2f(sacc[c][2 + e] - b1);
+          const float p0 = ex2_ftz(sacc[c][e] - b0);
+          const float p1 = ex2_ftz(sacc[c][2 + e] - b1);
           sacc[c][e] = p0;
           sacc[c][2 + e] = p1;
           l0 += p0;
