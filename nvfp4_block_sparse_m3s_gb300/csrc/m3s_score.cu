@@ -335,8 +335,12 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
       const int wq = warp & 3;                   // lane quarter: keys 32 wq .. 32 wq + 31
       constexpr int kHalfRows = QT / 2;
       int rlen[QT];
+      int rlen_min = INT_MAX;   // over the tile's rows: a block below it is causal for every row
 #pragma unroll
-      for (int rho = 0; rho < QT; ++rho) rlen[rho] = sm.lensm[rho];
+      for (int rho = 0; rho < QT; ++rho) {
+        rlen[rho] = sm.lensm[rho];
+        if (rho < ti.nrows) rlen_min = min(rlen_min, rlen[rho]);
+      }
       const float rscale = sm.rowscale[etid < QT ? etid : 0];   // this thread's row's 2^e_ref
       PageWindow pw;
       for (int j = ((ep - g0) % C::kNEpi + C::kNEpi) % C::kNEpi; j < nseg; j += C::kNEpi) {
@@ -396,11 +400,19 @@ __global__ void __launch_bounds__(Cfg<QT>::kBoundThreads, 1)
           tc_fence_before();
           mbar_arrive(&sm.dempty[ds]);
         }
+        if ((blk + 1) * kPage <= rlen_min) {   // (warp-uniform) every key is causal for every row
 #pragma unroll
-        for (int rho = 0; rho < QT; ++rho) {
-          const uint32_t key = ordered_bits(tok < rlen[rho] ? sc[rho] : -INFINITY);
-          const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
-          if (lane == 0) sm.blkmax[ds][ud & 1][wq][rho] = mx;
+          for (int rho = 0; rho < QT; ++rho) {
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, ordered_bits(sc[rho]));
+            if (lane == 0) sm.blkmax[ds][ud & 1][wq][rho] = mx;
+          }
+        } else {
+#pragma unroll
+          for (int rho = 0; rho < QT; ++rho) {
+            const uint32_t key = ordered_bits(tok < rlen[rho] ? sc[rho] : -INFINITY);
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, key);
+            if (lane == 0) sm.blkmax[ds][ud & 1][wq][rho] = mx;
+          }
         }
         named_bar_sync(1 + ep, 128);
         if (*reinterpret_cast<volatile int*>(&sm.abort)) break;  // uniform: read after the barrier
