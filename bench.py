@@ -101,8 +101,8 @@ NCU_TRAFFIC = {
                     "m3s_device.cuh": "858cf15362eb44ad"},
     },
     ("verify", "score_kernel"): {
-        "bytes": 143_923_200 + 4_278_272,
-        "sources": {"m3s_score.cu": "64d7e9057789b963",
+        "bytes": 143_932_160 + 3_994_368,
+        "sources": {"m3s_score.cu": "0e6af4207f397d38",
                     "m3s_score_common.cuh": "3c3b6d020be854f4",
                     "m3s_device.cuh": "858cf15362eb44ad"},
     },
