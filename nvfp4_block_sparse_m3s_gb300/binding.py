@@ -131,12 +131,15 @@ def _stream(stream) -> int:
 def plane(codes: torch.Tensor, scales: torch.Tensor) -> Plane:
     """The C plane of a (codes, scales) pair; its format follows the scale records'
     width (8 bytes: NVFP4, 4 bytes: MXFP4)."""
-    assert codes.dtype == torch.uint8 and scales.dtype == torch.uint8
-    assert codes.dim() == 4 and codes.shape[2:] == (PAGE, HEAD_DIM // 2)
-    assert scales.shape[:3] == codes.shape[:3] and scales.shape[3] in (HEAD_DIM // 16, HEAD_DIM // 32)
-    assert codes.is_contiguous() and scales.is_contiguous()
-    fmt = FMT_MXFP4 if scales.shape[3] == HEAD_DIM // 32 else FMT_NVFP4
-    return Plane(codes.data_ptr(), scales.data_ptr(), codes.shape[0], codes.shape[1], fmt)
+    cs, ss = codes.shape, scales.shape
+    if (codes.dtype is not torch.uint8 or scales.dtype is not torch.uint8 or len(cs) != 4 or len(ss) != 4
+            or cs[2] != PAGE or cs[3] != HEAD_DIM // 2 or ss[0] != cs[0] or ss[1] != cs[1] or ss[2] != PAGE
+            or (ss[3] != HEAD_DIM // 16 and ss[3] != HEAD_DIM // 32)
+            or not codes.is_contiguous() or not scales.is_contiguous()):
+        raise TypeError("a plane is contiguous uint8 codes [P, H, 128, 64] and scales [P, H, 128, 8] "
+                        "(NVFP4) or [P, H, 128, 4] (MXFP4)")
+    return Plane(codes.data_ptr(), scales.data_ptr(), cs[0], cs[1],
+                 FMT_MXFP4 if ss[3] == HEAD_DIM // 32 else FMT_NVFP4)
 
 
 def new_plane(num_pages: int, heads: int, device="cuda", mx: bool = False
@@ -155,25 +158,33 @@ def m3s_workspace_bytes(op: int, R: int, B: int, max_blocks: int, Hq: int = 0, H
 def m3s_nvfp4_store(src: torch.Tensor, slot_mapping: torch.Tensor, codes: torch.Tensor,
                     scales: torch.Tensor, err: torch.Tensor | None = None, stream=None) -> None:
     """src bf16 [T, H, 128] (rows may be strided), slot_mapping int64 [T]."""
-    assert src.dtype == torch.bfloat16 and src.dim() == 3 and src.shape[2] == HEAD_DIM
-    assert src.stride(2) == 1 and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
-    assert slot_mapping.dtype == torch.int64
-    T, H = src.shape[0], src.shape[1]
-    rc = load().m3s_nvfp4_store(_ptr(src), src.stride(0), T, H, _ptr(slot_mapping),
-                                plane(codes, scales), _ptr(err), _stream(stream))
+    if slot_mapping.dtype is not torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    T = src.shape[0] if src.dim() == 3 else -1
+    job = _store_job(src, T, codes, scales)
+    rc = load().m3s_nvfp4_store(_ptr(src), src.stride(0), T, src.shape[1], _ptr(slot_mapping),
+                                job.dst, _ptr(err), _stream(stream))
     _check(rc, "m3s_nvfp4_store")
+
+
+def _store_job(src: torch.Tensor, T: int, codes: torch.Tensor, scales: torch.Tensor) -> StoreJob:
+    """One job of the batched stores: src bf16 [T, H, 128] (rows may be strided)."""
+    sh = src.shape
+    if (src.dtype is not torch.bfloat16 or len(sh) != 3 or sh[0] != T or sh[2] != HEAD_DIM
+            or src.stride(2) != 1 or (sh[1] != 1 and src.stride(1) != HEAD_DIM)):
+        raise TypeError("a store job's rows are bfloat16 [T, H, 128] with unit element and head strides")
+    return StoreJob(src.data_ptr(), src.stride(0), sh[1], plane(codes, scales))
 
 
 def m3s_nvfp4_store_batch(jobs, slot_mapping: torch.Tensor, err: torch.Tensor | None = None,
                           stream=None) -> None:
     """jobs: sequence of (src bf16 [T, H, 128], codes, scales) sharing ``slot_mapping``."""
-    assert slot_mapping.dtype == torch.int64
+    if slot_mapping.dtype is not torch.int64:
+        raise TypeError("slot_mapping must be int64")
     arr = (StoreJob * max(1, len(jobs)))()
     T = slot_mapping.shape[0]
     for i, (src, codes, scales) in enumerate(jobs):
-        assert src.dtype == torch.bfloat16 and src.dim() == 3 and src.shape[0] == T
-        assert src.stride(2) == 1 and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
-        arr[i] = StoreJob(src.data_ptr(), src.stride(0), src.shape[1], plane(codes, scales))
+        arr[i] = _store_job(src, T, codes, scales)
     rc = load().m3s_nvfp4_store_batch(arr, len(jobs), T, _ptr(slot_mapping), _ptr(err),
                                       _stream(stream))
     _check(rc, "m3s_nvfp4_store_batch")
@@ -182,13 +193,12 @@ def m3s_nvfp4_store_batch(jobs, slot_mapping: torch.Tensor, err: torch.Tensor | 
 def m3s_nvfp4_store_batch_rows(jobs, slot_mapping: torch.Tensor, cu_q: torch.Tensor, seq_len: torch.Tensor,
                                R: int, row_req=None, row_len=None, err=None, stream=None):
     """m3s_nvfp4_store_batch and m3s_decode_rows in one launch; returns (row_req, row_len)."""
-    assert slot_mapping.dtype == torch.int64
+    if slot_mapping.dtype is not torch.int64:
+        raise TypeError("slot_mapping must be int64")
     arr = (StoreJob * max(1, len(jobs)))()
     T = slot_mapping.shape[0]
     for i, (src, codes, scales) in enumerate(jobs):
-        assert src.dtype == torch.bfloat16 and src.dim() == 3 and src.shape[0] == T
-        assert src.stride(2) == 1 and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
-        arr[i] = StoreJob(src.data_ptr(), src.stride(0), src.shape[1], plane(codes, scales))
+        arr[i] = _store_job(src, T, codes, scales)
     for t in (cu_q, seq_len):
         if t.dtype != torch.int32 or not t.is_contiguous():
             raise TypeError("cu_q and seq_len must be contiguous int32 tensors")
@@ -217,9 +227,11 @@ def m3s_qk_norm_rope_store(jobs, slot_mapping, rope_cos=None, rope_sin=None, rot
         if weight is not None and (weight.dtype != torch.float32 or not weight.is_contiguous()):
             raise TypeError("norm_weight must be a contiguous float32 [128] tensor")
         T = src.shape[0] if T is None else T
-        assert src.shape[0] == T and (src.shape[1] == 1 or src.stride(1) == HEAD_DIM)
+        if src.shape[0] != T or (src.shape[1] != 1 and src.stride(1) != HEAD_DIM):
+            raise TypeError("every job has T rows of [H, 128] with unit head stride")
         if isinstance(dst, torch.Tensor):
-            assert dst.dtype == torch.bfloat16 and dst.shape == src.shape and dst.stride(2) == 1
+            if dst.dtype is not torch.bfloat16 or dst.shape != src.shape or dst.stride(2) != 1:
+                raise TypeError("a BF16 destination has the source's shape and unit element stride")
             arr[i] = WriteJob(src.data_ptr(), src.stride(0), src.shape[1], _ptr(weight), int(rope),
                               Plane(), dst.data_ptr(), dst.stride(0))
         else:
