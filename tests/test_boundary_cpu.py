@@ -206,3 +206,29 @@ def test_quantise_at_write_host_validation(lib):
     assert call([job()], slots=None) == M.ERR_INVALID           # plane job without slots
     assert call([job()] * 7) == M.ERR_INVALID                    # too many jobs
     assert call([job(rope=1), job(out=fake, out_stride=256)], T=0) == M.OK
+
+
+def test_binding_checks_raise_type_errors_on_host_tensors():
+    """The binding's argument checks are explicit TypeErrors (they hold under
+    python -O): plane layouts, store rows. Host tensors suffice: nothing is
+    launched before the checks."""
+    import torch
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    codes = torch.zeros((4, 1, 128, 64), dtype=torch.uint8)
+    nv = torch.zeros((4, 1, 128, 8), dtype=torch.uint8)
+    mx = torch.zeros((4, 1, 128, 4), dtype=torch.uint8)
+    assert M.plane(codes, nv).format == M.FMT_NVFP4
+    assert M.plane(codes, mx).format == M.FMT_MXFP4
+    p = M.plane(codes, nv)
+    assert (p.num_pages, p.num_heads) == (4, 1)
+    for bad in ((codes.float(), nv), (codes, nv.float()), (codes[:, :, :, :32], nv), (codes, nv[:2]),
+                (codes, torch.zeros((4, 1, 128, 6), dtype=torch.uint8)), (codes.transpose(0, 1), nv),
+                (codes[..., ::2], nv)):
+        with pytest.raises(TypeError):
+            M.plane(*bad)
+    rows = torch.zeros((5, 1, 128), dtype=torch.bfloat16)
+    M._store_job(rows, 5, codes, nv)
+    for bad_rows, T in ((rows.float(), 5), (rows, 4), (rows[:, :, :64], 5),
+                        (torch.zeros((5, 2, 256), dtype=torch.bfloat16)[:, :, :128], 5)):
+        with pytest.raises(TypeError):
+            M._store_job(bad_rows, T, codes, nv)
