@@ -137,3 +137,40 @@ def test_workspace_and_top_k_zero(lib):
                                           dev.vs, dev.block_table, dev.cu_q, row_req, row_len, 3, 0, SM_SCALE)
     torch.cuda.synchronize()
     assert (out.float() == 0).all()
+
+
+def test_no_requests_every_row_padding(lib):
+    """B = 0 (an empty block table, cu_q = [0]): the verify call launches no
+    scorer tile and every row gets no id, a zero output and lse -inf; the
+    decode call (one tile per row) gives the same; R = 0 is a no-op."""
+    dev = torch.device("cuda")
+    R, Hq, Hi, topk = 5, 16, 16, 16
+    ic, is_ = M.new_plane(4, 1, dev)
+    kc, ks = M.new_plane(4, 1, dev)
+    vc, vs = M.new_plane(4, 1, dev)
+    bt = torch.empty((0, 8), dtype=torch.int32, device=dev)
+    cu_q = torch.zeros(1, dtype=torch.int32, device=dev)
+    row_req = torch.full((R,), -1, dtype=torch.int32, device=dev)
+    row_len = torch.zeros(R, dtype=torch.int32, device=dev)
+    q_idx = torch.randn((R, Hi, 128), device=dev).to(torch.bfloat16)
+    w = torch.ones((R, Hi), device=dev)
+    q = torch.randn((R, Hq, 128), device=dev).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for fused in ("verify", "decode"):
+        lse = torch.zeros((R, Hq), dtype=torch.float32, device=dev)
+        ids = torch.zeros((R, topk), dtype=torch.int32, device=dev)
+        out = torch.full((R, Hq, 128), 1.0, dtype=torch.bfloat16, device=dev)
+        if fused == "verify":
+            M.m3s_verify_index_attention(q_idx, w, ic, is_, q, 1, kc, ks, vc, vs, bt, cu_q, row_req, row_len,
+                                         4, topk, SM_SCALE, topk_ids=ids, out=out, lse=lse, err=err)
+        else:
+            M.m3s_index_attention(q_idx, w, ic, is_, q, 1, kc, ks, vc, vs, bt, row_req, row_len, topk,
+                                  SM_SCALE, topk_ids=ids, out=out, lse=lse, err=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0, f"{fused}: device error bits {int(err.item())}"
+        assert (ids == -1).all(), fused
+        assert (out.float() == 0).all() and torch.isneginf(lse).all(), fused
+    ids0, out0 = M.m3s_verify_index_attention(q_idx[:0], w[:0], ic, is_, q[:0], 1, kc, ks, vc, vs, bt, cu_q,
+                                              row_req[:0], row_len[:0], 4, topk, SM_SCALE, err=err)
+    torch.cuda.synchronize()
+    assert ids0.shape == (0, topk) and out0.shape == (0, Hq, 128) and int(err.item()) == 0
