@@ -86,25 +86,28 @@ def peaks():
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
 # dominant kernel, from one ncu capture of this bench's workload (summary under
 # profiles/). It is reported only while the kernel's sources hash to what was
-# captured; after any change it is null until the counters are taken again.
+# captured; after a change to the kernel it is null until the counters are
+# taken again. (The hashes moved once without a new capture: the removal of
+# device helpers no kernel called, with every kernel's registers, shared
+# memory and stack as ptxas reported them before.)
 NCU_TRAFFIC = {
     ("skewed", "score_decode_kernel"): {
         "bytes": 110_826_496 + 3_570_688,
         "sources": {"m3s_score_mma.cu": "e33f51210c0f3b77",
-                    "m3s_score_common.cuh": "3c3b6d020be854f4",
-                    "m3s_device.cuh": "858cf15362eb44ad"},
+                    "m3s_score_common.cuh": "fd432d016e7fe20e",
+                    "m3s_device.cuh": "8c6b356f0523f4a3"},
     },
     ("skewed-mxfp4", "score_decode_kernel"): {
         "bytes": 104_680_960 + 3_654_400,
         "sources": {"m3s_score_mma.cu": "e33f51210c0f3b77",
-                    "m3s_score_common.cuh": "3c3b6d020be854f4",
-                    "m3s_device.cuh": "858cf15362eb44ad"},
+                    "m3s_score_common.cuh": "fd432d016e7fe20e",
+                    "m3s_device.cuh": "8c6b356f0523f4a3"},
     },
     ("verify", "score_kernel"): {
         "bytes": 143_932_160 + 3_994_368,
         "sources": {"m3s_score.cu": "0e6af4207f397d38",
-                    "m3s_score_common.cuh": "3c3b6d020be854f4",
-                    "m3s_device.cuh": "858cf15362eb44ad"},
+                    "m3s_score_common.cuh": "fd432d016e7fe20e",
+                    "m3s_device.cuh": "8c6b356f0523f4a3"},
     },
 }
 

@@ -273,13 +273,6 @@ __device__ __forceinline__ int select_key_id(unsigned long long key) {
   return static_cast<int>((key >> 32) == 0xFFFFFFFEull ? lo : 0xFFFFFFFFu - lo);
 }
 
-// The largest of a warp's 64-bit values (every lane gets it).
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
-  const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(v >> 32));
-  const uint32_t lo = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(v >> 32) == hi ? static_cast<uint32_t>(v) : 0u);
-  return (static_cast<unsigned long long>(hi) << 32) | lo;
-}
-
 // A warp's running top-k (k <= 64) of distinct keys, sorted descending: slot s
 // lives in lane s % 32, register s / 32; empty slots hold 0.
 struct WarpTopk {
