@@ -224,9 +224,14 @@ def _tiny_index_case(seed, L, hi=2, nb_pages=None):
 
 def test_scores_brute_force_and_topk_all_subsets():
     """Token scores by explicit Python loops; the top-k set is the best of every
-    k-subset under (higher block score, then lower id)."""
-    for seed, L, k in [(11, 300, 2), (12, 512, 3), (13, 129, 1), (14, 385, 2)]:
+    k-subset under (higher block score, then lower id). The last two cases give
+    the second head a negative weight: the formula puts no sign on w_h, so a
+    head can only lower a token's score (block scores may then be negative)."""
+    for seed, L, k, neg in [(11, 300, 2, False), (12, 512, 3, False), (13, 129, 1, False),
+                            (14, 385, 2, False), (15, 300, 2, True), (16, 640, 3, True)]:
         bt, c, s, q, w, _ = _tiny_index_case(seed, L)
+        if neg:
+            w[0, 1] = -2.0 * w[0, 1]
         rr, rl = np.array([0], np.int32), np.array([L], np.int32)
         ids, bsc, err = O.index_score_topk(q, w, c, s, bt, rr, rl, k)
         assert err == 0
@@ -253,6 +258,17 @@ def test_scores_brute_force_and_topk_all_subsets():
         best_sub = max(itertools.combinations(range(nb), kk), key=rank_key)
         assert list(ids[0][:kk]) == sorted(best_sub)
         assert (ids[0][kk:] == -1).all()
+
+
+def test_block_max_closed_form():
+    """A block's score is the largest score of its causal tokens: with token
+    scores increasing in t that is the block's last causal token, with scores
+    decreasing its first token, for lengths with a ragged last block."""
+    for L in (1, 127, 128, 129, 300, 512):
+        t = np.arange(L, dtype=np.float64)
+        nb = (L + 127) // 128
+        assert O.block_max(t, L).tolist() == [float(min(128 * (b + 1), L) - 1) for b in range(nb)]
+        assert O.block_max(-t, L).tolist() == [-float(128 * b) for b in range(nb)]
 
 
 def test_zero_queries_select_lowest_ids():
@@ -697,6 +713,13 @@ def test_norm_rope_special_cases():
     c = np.full((1, 1, 128), W.f32_to_bf16_bits(np.float32([-0.75]))[0], dtype=np.uint16)
     y = O.bf16_to_f64(O.norm_rope_rows(c, np.ones(128, np.float32), None, None, 0, 1e-6))
     assert np.allclose(y, -0.75 / math.sqrt(0.5625 + 1e-6), rtol=2.0 ** -8)
+    # eps equal to the mean square: a constant row of a = 2^-10 with eps = 2^-20
+    # normalises to a / sqrt(a^2 + eps) = 1 / sqrt(2)
+    a = np.full((1, 1, 128), W.f32_to_bf16_bits(np.float32([2.0 ** -10]))[0], dtype=np.uint16)
+    y = O.bf16_to_f64(O.norm_rope_rows(a, np.ones(128, np.float32), None, None, 0, 2.0 ** -20))
+    assert np.allclose(y, 1 / math.sqrt(2), rtol=2.0 ** -8)
+    y64 = O.norm_rope_rows_f64(a, np.ones(128), None, None, 0, 2.0 ** -20)
+    assert np.allclose(y64, 1 / math.sqrt(2), rtol=1e-14)
     cos, sin = _rope_tables(4, 64)
     xr = O.bf16_to_f64(x)
     yr = O.bf16_to_f64(O.norm_rope_rows(x, None, cos, sin, 128, 1e-6))
