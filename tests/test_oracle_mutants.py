@@ -113,6 +113,34 @@ MUTANTS = {
     "rmsnorm f64: eps outside the root": [("np.sqrt(ss / HEAD_DIM + float(eps))", "(np.sqrt(ss / HEAD_DIM) + float(eps))")],
     "bf16 rounding: ties away from zero": [("r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "r = (u + 0x8000) >> 16")],
     "bf16 rounding: truncation": [("r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16", "r = u >> 16")],
+    "f32 sum of squares: butterfly one level short": [("for off in (16, 8, 4, 2, 1):", "for off in (16, 8, 4, 2):")],
+    "fused write: RoPE on every job": [("cos if rope else None, sin if rope else None", "cos, sin")],
+    "fused write: RMSNorm weight ignored": [("rows = norm_rope_rows(src, weight,", "rows = norm_rope_rows(src, None,")],
+    # more of the scoring and attention paths
+    "mx quantiser: sign dropped": [("code = ((sign << np.uint8(3)) | mag).reshape(lead + (HEAD_DIM,))",
+                                    "code = (mag + 0 * sign).reshape(lead + (HEAD_DIM,))")],
+    "nvfp4 groups strided, not contiguous": [
+        ("x = bf16_to_f64(bits).reshape(lead + (SCALE_BYTES, GROUP))",
+         "x = bf16_to_f64(bits).reshape(lead + (GROUP, SCALE_BYTES)).swapaxes(-1, -2)")],
+    "request's pages in reverse order": [
+        ("x = dequantize(codes[pages[:nb], head], scales[pages[:nb], head])",
+         "x = dequantize(codes[pages[:nb][::-1], head], scales[pages[:nb][::-1], head])")],
+    "scoring: bad page not reported": [("        err |= ERR_PAGE\n    return pages, err",
+                                        "        err |= 0\n    return pages, err")],
+    "scoring: row past the block table not reported": [("        err |= ERR_ROW\n", "        err |= 0\n")],
+    "scoring: token cache keyed by request only": [("key = (b, nb)", "key = b")],
+    "forced: init blocks counted from the end": [("init = ids < init_blocks", "init = ids >= nb - init_blocks")],
+    "attention: softmax without the maximum": [("p = np.exp(logits - m)", "p = np.exp(logits)")],
+    "attention: lse in base 2": [("lse[r, h] = m + math.log(l)", "lse[r, h] = m + math.log2(l)")],
+    "attention: ids past the causal length attended": [("if i >= nb or i >= block_table.shape[1]:",
+                                                        "if i >= block_table.shape[1]:")],
+    "attention: bad page not reported": [("            err |= ERR_PAGE\n            continue",
+                                          "            continue")],
+    "attention: K of the next KV head": [("kh = np.concatenate([dequantize(k_codes[p, kvh, :n], k_scales[p, kvh, :n])",
+                                           "kh = np.concatenate([dequantize(k_codes[p, (kvh + 1) % hkv, :n], "
+                                           "k_scales[p, (kvh + 1) % hkv, :n])")],
+    "row map: padding rows take the last request": [("row_req = np.full(R, -1, dtype=np.int32)",
+                                                     "row_req = np.full(R, len(seq_len) - 1, dtype=np.int32)")],
 }
 
 

@@ -271,6 +271,50 @@ def test_block_max_closed_form():
         assert O.block_max(-t, L).tolist() == [-float(128 * b) for b in range(nb)]
 
 
+def test_rows_of_a_request_score_alone_or_together():
+    """Scoring a request's rows in one call gives each row what scoring it alone
+    gives, for rows whose causal lengths cross block boundaries (253..260
+    tokens: 2 and 3 blocks), in increasing and in decreasing row order."""
+    bt, c, s, _, _, _ = _tiny_index_case(41, 260)
+    R = 8
+    q = W.bf16_tensor(41, "rq", (R, 2, 128))
+    w = W.uniform(41, "rw", 0, 2 * R).astype(np.float32).reshape(R, 2)
+    for lens in (np.arange(253, 261), np.arange(260, 252, -1)):
+        rl = lens.astype(np.int32)
+        ids, bs, err = O.index_score_topk(q, w, c, s, bt, np.zeros(R, np.int32), rl, 2)
+        assert err == 0
+        for r in range(R):
+            ids1, bs1, _ = O.index_score_topk(q[r:r + 1], w[r:r + 1], c, s, bt, np.zeros(1, np.int32),
+                                              rl[r:r + 1], 2)
+            assert len(bs[r]) == (int(rl[r]) + 127) // 128
+            assert np.array_equal(bs[r], bs1[0]) and np.array_equal(ids[r], ids1[0])
+
+
+def test_bad_pages_rows_and_ids_are_reported():
+    """Error bits and skipped rows: in scoring, a block-table entry outside the
+    pool (PAGE) and a row longer than its block table (ROW); in attention, a
+    page outside the pool (PAGE). A reported row gets no ids, or zero output and
+    lse -inf."""
+    bt, c, s, q, w, _ = _tiny_index_case(42, 300)
+    P = c.shape[0]
+    bad = bt.copy()
+    bad[0, 1] = P
+    ids, _, err = O.index_score_topk(q, w, c, s, bad, np.zeros(1, np.int32), np.array([300], np.int32), 2)
+    assert err == O.ERR_PAGE and (ids == -1).all()
+    bad[0, 1] = -3
+    _, _, err = O.index_score_topk(q, w, c, s, bad, np.zeros(1, np.int32), np.array([300], np.int32), 2)
+    assert err == O.ERR_PAGE
+    long = np.array([bt.shape[1] * 128 + 1], np.int32)
+    ids, _, err = O.index_score_topk(q, w, c, s, bt, np.zeros(1, np.int32), long, 2)
+    assert err & O.ERR_ROW and (ids == -1).all()
+    bt, kc, ks, vc, vs, qa = _attn_case(43, 300)
+    bad = bt.copy()
+    bad[0, 2] = kc.shape[0]
+    out, lse, err = O.sparse_attention(qa, 1, kc, ks, vc, vs, bad, np.zeros(1, np.int32),
+                                       np.array([300], np.int32), np.array([[0, 2]]), 0.1)
+    assert err == O.ERR_PAGE and not out.any() and np.isneginf(lse).all()
+
+
 def test_zero_queries_select_lowest_ids():
     """All-zero queries give every block the score 0; ties go to the lower block id
     (the pages' fused top-k tie test uses zero queries)."""
@@ -726,6 +770,21 @@ def test_norm_rope_special_cases():
     n0 = np.hypot(xr[..., :64], xr[..., 64:])
     n1 = np.hypot(yr[..., :64], yr[..., 64:])
     assert np.all(np.abs(n1 - n0) <= n0 * 2.0 ** -7 + 1e-30)
+
+
+def test_fused_write_job_without_norm_or_rope_is_the_plain_store():
+    """A job with no weight and no RoPE stores its rows as the plain store does,
+    byte for byte, while another job of the same call is rotated."""
+    T, P = 200, 3
+    src = W.bf16_tensor(44, "fw", (T, 1, 128), 2, 10.0)
+    slots = W.permutation(44, "fs", P * 128)[:T].astype(np.int64)
+    cos, sin = _rope_tables(T, 32)
+    plain = O.new_planes(P, 1)
+    assert O.nvfp4_store(src, slots, *plain) == 0
+    fused, rotated = O.new_planes(P, 1), O.new_planes(P, 1)
+    O.qk_norm_rope_store([(src, None, False, fused), (src, None, True, rotated)], slots, cos, sin, 64, 1e-6)
+    assert np.array_equal(fused[0], plain[0]) and np.array_equal(fused[1], plain[1])
+    assert not np.array_equal(rotated[0], plain[0])
 
 
 def test_quantise_at_write_equals_staging_then_store():
