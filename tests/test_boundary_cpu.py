@@ -232,3 +232,44 @@ def test_binding_checks_raise_type_errors_on_host_tensors():
                         (torch.zeros((5, 2, 256), dtype=torch.bfloat16)[:, :, :128], 5)):
         with pytest.raises(TypeError):
             M._store_job(bad_rows, T, codes, nv)
+
+
+def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
+    """A C11 host program (gcc -pedantic -Werror, no C++) that takes the address
+    of every declared function links against libm3s.so, and on a machine
+    without a GPU its host-only calls work: the version, a workspace size
+    (equal to the ctypes binding's) and an argument check answered before any
+    launch."""
+    import subprocess
+
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    from nvfp4_block_sparse_m3s_gb300 import build as B
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    names = declared_functions()
+    prog = "\n".join([
+        "#include <stdio.h>",
+        '#include "m3s.h"',
+        "typedef void (*fn_t)(void);",
+        "static fn_t all_fns[] = {" + ", ".join(f"(fn_t){n}" for n in names) + "};",
+        "int main(void) {",
+        "  m3s_fp4_plane p = {NULL, NULL, 4, 4, M3S_FMT_NVFP4};",
+        "  size_t ws = m3s_workspace_bytes(M3S_OP_INDEX_ATTENTION, 8, 8, 4096, 16, 1, 16, 16, 1);",
+        "  int rc = m3s_sparse_attention(NULL, 6, 4, p, p, NULL, 1, 1, NULL, NULL, NULL, 16, 1, 0.1f,",
+        "                                NULL, NULL, NULL, 0, NULL, NULL);",
+        '  printf("%s|%zu|%d|%d\\n", m3s_version(), ws, rc, (int)(sizeof(all_fns) / sizeof(all_fns[0])));',
+        "  return 0;",
+        "}",
+    ])
+    src = tmp_path / "host.c"
+    src.write_text(prog)
+    exe = tmp_path / "host"
+    libdir = os.path.dirname(B.LIB)
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-L", libdir, "-lm3s", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.strip().split("|")
+    assert out[0] == lib.m3s_version().decode()
+    assert int(out[1]) == M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, 8, 8, 4096, 16, 1, 16, 16, 1) > 0
+    assert int(out[2]) == M.ERR_INVALID
+    assert int(out[3]) == len(names)
