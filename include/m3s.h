@@ -445,7 +445,9 @@ int m3s_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_f
  * [R], the row map of the same rows). ws_bytes >=
  * m3s_workspace_bytes(M3S_OP_VERIFY_INDEX_ATTENTION, R, B, bt_stride, Hq, Hkv,
  * Hi, topk, max_q) (no zeroing needed). B * ceil(max_q / 8) <= 8192 tiles, else
- * M3S_ERR_UNSUPPORTED.
+ * M3S_ERR_UNSUPPORTED. Rows at or past cu_q[B] (all of them when B = 0) get
+ * no ids (-1), zero output and lse -inf; topk = 0 launches only the attention,
+ * which gives every row that result.
  */
 int m3s_verify_index_attention(const uint16_t* q_idx, const float* w, int32_t Hi, m3s_fp4_plane idx_k,
                                const uint16_t* q, int32_t Hq, int32_t Hkv, m3s_fp4_plane k, m3s_fp4_plane v,
