@@ -273,3 +273,17 @@ def test_header_is_plain_c_and_the_library_links_from_c(lib, tmp_path):
     assert int(out[1]) == M.m3s_workspace_bytes(M.OP_INDEX_ATTENTION, 8, 8, 4096, 16, 1, 16, 16, 1) > 0
     assert int(out[2]) == M.ERR_INVALID
     assert int(out[3]) == len(names)
+
+
+def test_binding_signatures_match_the_header():
+    """The ctypes binding declares every header function, with as many
+    parameters as the declaration (an undeclared one would pass 64-bit
+    pointers as C int; a count that drifted would shift the arguments)."""
+    from nvfp4_block_sparse_m3s_gb300 import binding as M
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    decls = dict(re.findall(r"\b(m3s_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text))
+    assert set(decls) == set(declared_functions()) == set(M._SIGS)
+    for name, params in decls.items():
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(M._SIGS[name][1]) == n, (name, n, len(M._SIGS[name][1]))
