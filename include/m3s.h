@@ -115,7 +115,10 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
 
 /*
  * Workspace bytes an op needs (device memory the caller provides as `ws`).
- * A pure host function of its arguments; 0 for unknown ops.
+ * A pure host function of its arguments; 0 for unknown ops, and 0 for shapes
+ * the calls reject with M3S_ERR_UNSUPPORTED before they look at the
+ * workspace: more than 8192 tiles (index ops: R > 8192; verify ops:
+ * B * ceil(max_q / 8) > 8192).
  *   R rows, B requests, max_blocks = block-table width (bt_stride), Hq / Hkv
  *   q and KV heads, Hi index heads, topk, max_q = the largest rows-per-request
  *   the verify call will see (the cu_q differences).
@@ -136,9 +139,8 @@ typedef m3s_fp4_plane m3s_nvfp4_plane; /* the NVFP4-only name of the same type *
  * slots (rounded up to 256 bytes), then one int2 per row.
  * Verify index attention: candidate lists of topk keys for (ntiles + 255)
  * slots of 8 rows (rounded up to 256 bytes), a block-maximum scratch of
- * 256 x 8 x max_blocks fp32 (rounded up likewise), then one int2 per row;
- * 0 when ntiles exceeds 8192. Neither needs zeroing: every call writes what it
- * reads.
+ * 256 x 8 x max_blocks fp32 (rounded up likewise), then one int2 per row.
+ * Neither needs zeroing: every call writes what it reads.
  * Attention: 0 (its split-K partials are merged on chip); its ws arguments
  * are accepted and ignored.
  */

@@ -13,16 +13,21 @@ extern "C" size_t m3s_workspace_bytes(int op, int32_t R, int32_t B, int32_t max_
   (void)Hq;
   (void)Hkv;
   if (R <= 0 || topk <= 0) return 0;
+  // more tiles than the calls take: they return M3S_ERR_UNSUPPORTED before
+  // they look at the workspace, so there is no size to give
+  const bool index_tiles_ok = R <= m3s::kMaxTiles;   // index ops: a tile per row
   switch (op) {
     case M3S_OP_INDEX_CANDIDATES:   // always the streaming form
-      return round16(m3s::topk_ws_bytes(R, 1, topk));
+      return index_tiles_ok ? round16(m3s::topk_ws_bytes(R, 1, topk)) : 0;
     case M3S_OP_INDEX_ATTENTION:    // the scorer's candidate lists and each row's slot range
-      return round16(m3s::index_attention_ws_bytes(R, topk));
+      return index_tiles_ok ? round16(m3s::index_attention_ws_bytes(R, topk)) : 0;
     case M3S_OP_INDEX_SCORE_TOPK:   // one tile per row
-      return round16(m3s::score_topk_ws_bytes(R, 1, R, max_blocks, topk));
+      return index_tiles_ok ? round16(m3s::score_topk_ws_bytes(R, 1, R, max_blocks, topk)) : 0;
     case M3S_OP_VERIFY_SCORE_TOPK: {   // tiles of up to 8 rows of one request
       const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;
-      return round16(m3s::score_topk_ws_bytes(B > 0 ? static_cast<long long>(B) * cpr : 0, 8, R, max_blocks, topk));
+      const long long nt = B > 0 ? static_cast<long long>(B) * cpr : 0;
+      if (nt > m3s::kMaxTiles) return 0;
+      return round16(m3s::score_topk_ws_bytes(nt, 8, R, max_blocks, topk));
     }
     case M3S_OP_VERIFY_INDEX_ATTENTION: {   // candidate lists, block-maximum scratch, row ranges
       const int cpr = max_q > 0 ? (max_q + 7) / 8 : 1;

@@ -79,6 +79,14 @@ def test_workspace_sizes(lib):
     assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8, 8, 3600, 16, 1, 16, 16) == 0
     assert M.m3s_workspace_bytes(M.OP_SPARSE_ATTENTION, 8192, 1, 2112, 16, 1, 16, 16) == 0
     assert M.m3s_workspace_bytes(99, 8, 8, 8) == 0
+    # more than 8192 tiles: the calls reject the shape first, so there is no size
+    # (also no signed overflow for the largest int32 row count)
+    for op in (M.OP_INDEX_SCORE_TOPK, M.OP_INDEX_CANDIDATES, M.OP_INDEX_ATTENTION):
+        assert M.m3s_workspace_bytes(op, 8192, 8192, 64, 16, 1, 16, 16) > 0
+        assert M.m3s_workspace_bytes(op, 8193, 8193, 64, 16, 1, 16, 16) == 0
+        assert M.m3s_workspace_bytes(op, 2 ** 31 - 1, 8, 64, 16, 1, 16, 16) == 0
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 128, 1025, 64, 0, 0, 16, 16, 64) == 0
+    assert M.m3s_workspace_bytes(M.OP_VERIFY_SCORE_TOPK, 128, 1024, 64, 0, 0, 16, 16, 64) > 0
 
 
 def test_host_validation_rejects_before_launch(lib):
